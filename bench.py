@@ -1,0 +1,426 @@
+"""Benchmark of the paged-KV-cache decode hot path on one GB300 (or N replicas).
+
+One step = pa_reshape_and_cache of the batch's new tokens + pa_decode over
+every sequence (attention kernel and, for split-KV, the merge kernel), on a
+seeded synthetic batch whose KV cache is already resident in HBM.
+
+Prints ONE JSON line (rank 0).  ``value`` is attended-KV GB/s of the whole job
+(sum over ranks of sum_i L_i*Hkv*D*2*elt bytes per step / step time, max
+over ranks).  ``roofline`` reports the decode call against the measured HBM
+copy bandwidth.  ``e2e`` repeats the measurement through the public API with
+the step's inputs copied from pinned host memory and the output copied back
+inside the timed region.  ``cpu_baseline`` times the float64 CPU oracle on a
+bounded sample of the same batch.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl reference]
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+# The CPU oracle leg runs single-threaded; fix BLAS threads before NumPy loads.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_296_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged-decode attended-KV GB/s (fraction of GB300 HBM peak); µs per decode step"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = ["pa_decode_kernel.cuh", "pa_ptx.cuh", "pa_decode_launch.cuh"]
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_296_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config_id):
+    """DRAM bytes per decode launch from the committed ncu summary, if it still
+    describes the current kernel source (else None)."""
+    path = os.path.join(PROFILE_DIR, f"paged_decode_kernel_config{config_id}.md")
+    try:
+        text = open(path, encoding="utf-8").read()
+    except OSError:
+        return None
+    m_src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"dram_bytes_per_decode_call:\s*([0-9.eE+]+)", text)
+    if not m_src or not m_tr or m_src.group(1) != kernel_source_hash():
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[4][1:5])
+                          if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside),
+                "power_w_max": max(r[3] for r in inside),
+                "samples": len(inside), "reasons": reasons}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(W, seconds, pool_cpu_rows):
+    """Time the float64 oracle over whole sequences of W until ``seconds`` pass.
+
+    ``pool_cpu_rows(blocks)`` returns the pool rows of those physical blocks
+    as raw bits on the host.  Returns (attended bytes processed, elapsed s,
+    sequences processed).
+    """
+    from oracle import paged_attention as ref  # test infrastructure: only this leg runs it
+    spec = W.spec
+    elt = 1 if spec.kv_dtype == "e4m3" else 2
+    q_bits = W.q.cpu()
+    q_bits = q_bits.view(torch.int16).numpy().view(np.uint16)
+    done_bytes, elapsed, nseq = 0, 0.0, 0
+    lens = W.context_lens.cpu().numpy()
+    tables = W.block_tables.cpu().numpy()
+    for i in range(spec.num_seqs):
+        L = int(lens[i])
+        nblk = -(-L // 16)
+        blocks = tables[i, :nblk].astype(np.int64)
+        pool = pool_cpu_rows(blocks)                      # [nblk, 16, 2, Hkv, D] bits
+        table = np.arange(max(nblk, 1))[None, :]
+        t = time.perf_counter()
+        ref.paged_decode(q_bits[i:i + 1], spec.q_dtype, pool, table, np.array([L]), W.scale,
+                         spec.kv_dtype, W.kv_scale)
+        elapsed += time.perf_counter() - t
+        done_bytes += L * spec.num_kv_heads * spec.head_size * 2 * elt
+        nseq += 1
+        if elapsed >= seconds:
+            break
+    return done_bytes, elapsed, nseq
+
+
+def oracle_rows_fn(W):
+    """Pool rows of given physical blocks as the oracle sees them, built from the
+    generator's own arrays (never from memory the CUDA path wrote): the 16-bit
+    pool as drawn, or the oracle's quantisation of the fp32 source values."""
+    if W.spec.kv_dtype == "e4m3":
+        from oracle import paged_attention as ref
+
+        def rows(blocks):
+            src = W.pool_src[torch.from_numpy(blocks).to(W.pool_src.device)].cpu().contiguous()
+            return ref.fp8_quantise(src.view(torch.int32).numpy().view(np.uint32), "f32",
+                                    W.kv_scale)
+        return rows
+
+    def rows(blocks):
+        t = W.pool[torch.from_numpy(blocks).to(W.pool.device)].cpu()
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return rows
+
+
+# ---------------------------------------------------------------- main legs
+
+def config_block(spec, W, extra):
+    c = {"workload": spec.name, "num_seqs": spec.num_seqs, "num_q_heads": spec.num_q_heads,
+         "num_kv_heads": spec.num_kv_heads, "head_size": spec.head_size, "block_size": 16,
+         "q_dtype": spec.q_dtype, "kv_dtype": spec.kv_dtype,
+         "mean_context": float(W.context_lens.float().mean()),
+         "num_blocks": W.num_blocks, "seed": W.seed}
+    c.update(extra)
+    return c
+
+
+def run_ours(args, world, rank, local):
+    from paged_kv_cache_296_gb300 import binding as pa
+    from paged_kv_cache_296_gb300.runner import DecodeStep, step_bytes, unique_kv_bytes
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    pa.load()
+    spec = wl.SPECS[args.config]
+    W = wl.make_workload(spec, args.config + 1000 * rank, device=str(device))
+    S = DecodeStep(W, device=device, partition_size=args.partition_size)
+    total_bytes, kv_bytes = step_bytes(W)
+    stream = torch.cuda.current_stream(device)
+
+    for _ in range(args.warmup):
+        S.step()
+    torch.cuda.synchronize(device)
+    pa.pa_device_status(clear=True)
+
+    sampler = ClockSampler(device.index)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(n):
+        ev[i][0].record(stream)
+        S.write()
+        ev[i][1].record(stream)
+        S.decode()
+        ev[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    t_wall1 = time.time()
+    sampler.stop()
+    total_ms = start.elapsed_time(end)
+    decode_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    write_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    ms_step = max_over_ranks(total_ms / n, world, device)
+    status = pa.pa_device_status(clear=True)
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x}: a kernel gave up waiting")
+
+    # ---- e2e through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {k: getattr(S, k).cpu().pin_memory() for k in
+                ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")}
+        out_host = torch.empty(S.out.shape, dtype=S.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+
+        def e2e_step():
+            for k, t in host.items():
+                getattr(S, k).copy_(t, non_blocking=True)
+            S.step()
+            out_host.copy_(S.out, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        s2.record(stream)
+        for _ in range(n):
+            e2e_step()
+        e2.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+        e2e_ms = max_over_ranks(s2.elapsed_time(e2) / n, world, device)
+        e2e_gbs = sum_over_ranks(kv_bytes, world, device) / (e2e_ms * 1e-3) / 1e9
+        e2e = {"value": round(e2e_gbs, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    # ---- CPU oracle baseline (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        b, secs, nseq = oracle_sample(W, args.cpu_seconds, oracle_rows_fn(W))
+        cpu = {"value": round(b / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"float64 NumPy oracle, {nseq} of {spec.num_seqs} sequences of this "
+                         f"batch (all heads), {secs:.1f} s, 1 BLAS thread"}
+
+    all_kv = sum_over_ranks(kv_bytes, world, device)
+    value = all_kv / (ms_step * 1e-3) / 1e9
+    dec_ms = statistics.mean(decode_ms)
+    peak, peak_kind = hbm_peak()
+    achieved = total_bytes / (dec_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(args.config)
+    launches = S.launches_per_step * n
+    uniq = unique_kv_bytes(W) if spec.lens[0] == "shared_prefix" else None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": n, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "us_per_step": round(ms_step * 1e3, 2),
+        "us_decode_call": round(dec_ms * 1e3, 2),
+        "us_write_call": round(statistics.mean(write_ms) * 1e3, 2),
+        "frac_of_hbm_peak": round(value / peak, 4),
+        "seqs_per_s": round(spec.num_seqs * world / (ms_step * 1e-3), 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": spec.kv_dtype if spec.kv_dtype == spec.q_dtype else f"{spec.q_dtype}+{spec.kv_dtype}",
+        "data": "synthetic (seeded N(0,1) K/V/q; no model weights)",
+        "config": config_block(spec, W, {
+            "partition_tokens": S.partition_tokens,
+            "l2": f"inputs larger than L2: {kv_bytes / 1e9:.3f} GB of KV read per step, no flush",
+            "parallelism": f"replicas{world}" if world > 1 else "single GPU"}),
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (attention kernel + split-KV merge)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": total_bytes,
+                     "traffic": traffic},
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if uniq is not None:
+        line["unique_kv_gbs"] = round(uniq * world / (ms_step * 1e-3) / 1e9, 2)
+    clocks = sampler.summary(t_wall0, t_wall1)
+    line["clocks"] = clocks
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args, world, rank, local):
+    """The CPU oracle as the reference arm: rank 0 alone, a bounded sample per step."""
+    if rank != 0:
+        return
+    spec = wl.SPECS[args.config]
+    W = wl.make_workload(spec, args.config, device="cpu")
+    rows = oracle_rows_fn(W)
+    per_step = max(1.0, args.ref_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(W, per_step, rows)
+    tot_b, tot_s, nseq = 0, 0.0, 0
+    for _ in range(args.steps):
+        b, s, k = oracle_sample(W, per_step, rows)
+        tot_b += b
+        tot_s += s
+        nseq += k
+    value = tot_b / tot_s / 1e9
+    cpu = {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": f"float64 NumPy oracle, {nseq} sequences over {args.steps} steps "
+                     f"({tot_s:.1f} s), 1 BLAS thread"}
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) K/V/q; no model weights)",
+            "config": config_block(spec, W, {"parallelism": "host cores, one thread"}),
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--config", type=int, default=2, choices=sorted(wl.SPECS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--partition-size", type=int, default=0)
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--ref-seconds", type=float, default=60.0)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * pa.h -- C ABI of the GB300 paged-KV-cache decode library (libpagedattn.so).
+ *
+ * The library implements the data-parallel hot path of a paged KV cache:
+ * the per-step write of new keys/values into a pool of fixed-size blocks and
+ * single-query ("decode") attention for every running sequence, reaching its
+ * keys/values through a per-sequence block table.
+ *
+ * Sources: "vLLM 部署深度指南" (section PagedAttention 方案: 16 tokens per
+ * block and the logical-view / block-table figure; section 代码层面理解: the
+ * preallocated pool [num_blocks, block_size, 2, num_heads, head_size],
+ * allocate() and append_kv()); "vLLM GitHub 项目：探索高效 LLM 推理服务"
+ * (section 二: the block table maps logical to physical blocks, physical
+ * blocks need not be contiguous, several tables may point at one block;
+ * decode is memory-bandwidth bound).
+ *
+ * ---------------------------------------------------------------- conventions
+ * Pool layout.  One tensor [num_blocks, block_size, 2, num_kv_heads, head_size]
+ * of the cache dtype.  Index 2 selects K (0) or V (1).  `k_cache` is the
+ * address of element (0, 0, 0, 0, 0) and `v_cache` of (0, 0, 1, 0, 0); both
+ * views share token stride 2*num_kv_heads*head_size elements and block stride
+ * block_size times that.  Element (blk, t, h, d) of the K view is at
+ *   k_cache + ((blk*block_size + t) * 2*num_kv_heads + h) * head_size + d.
+ * A flat slot s names token row s = blk*block_size + t of the pool.
+ *
+ * Memory.  Every pointer argument is device memory owned by the caller
+ * (except where a parameter says "host"), 16-byte aligned unless stated.  The
+ * library never allocates, frees or keeps a reference past the call.
+ *
+ * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).
+ * Compute calls only enqueue work and return; results are visible once the
+ * stream reaches them.  No compute call synchronises.
+ *
+ * Errors.  Every entry point validates its scalar arguments and pointer
+ * alignment on the host before launching anything, and returns a pa_status.
+ * On error nothing is enqueued and pa_last_error() describes the problem.
+ * Launch failures reported by the CUDA runtime return PA_ERR_CUDA.  Index
+ * values inside device arrays (block ids, slots, lengths) are not checked by
+ * the compute calls: out-of-range block ids read zeros and out-of-range slots
+ * are skipped, so no access leaves the pool, but the result is then
+ * meaningless.  pa_check_tables() validates them on request.
+ *
+ * Supported values: block_size == 16; head_size in {64, 128};
+ * num_q_heads % num_kv_heads == 0 with 1 <= num_q_heads/num_kv_heads <= 8;
+ * q/out dtype PA_F16 or PA_BF16; cache dtype equal to the q dtype, or
+ * PA_E4M3 with either q dtype.  Others return PA_ERR_UNSUPPORTED.
+ *
+ * Determinism: identical inputs give bit-identical outputs.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types.  PA_F32 is accepted only as the source of a PA_E4M3 write. */
+typedef enum {
+  PA_F16 = 0,  /* IEEE binary16 */
+  PA_BF16 = 1, /* bfloat16 */
+  PA_E4M3 = 2, /* OCP 8-bit float E4M3 (bias 7, max 448, NaN 0x7F/0xFF) */
+  PA_F32 = 3   /* IEEE binary32 */
+} pa_dtype;
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1, /* null pointer, negative size, misalignment, bad combination */
+  PA_ERR_UNSUPPORTED = 2, /* a shape or dtype outside the supported set above */
+  PA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than pa_decode_workspace_size() */
+  PA_ERR_CUDA = 4,        /* the CUDA runtime or driver reported an error */
+  PA_ERR_BAD_INDEX = 5    /* pa_check_tables() found out-of-range indices */
+} pa_status;
+
+/*
+ * pa_reshape_and_cache -- write one step's new keys and values into the pool.
+ *
+ * Defined by append_kv() ("vLLM 部署深度指南", section 代码层面理解: write the new
+ * token's K/V into its physical block) with the slot naming that block and
+ * the offset inside it (section PagedAttention 方案, logical-view figure).
+ *
+ * For every token n with 0 <= slot_mapping[n] < num_blocks*block_size:
+ *   pool[s / block_size, s % block_size, 0, :, :] = enc(k[n])
+ *   pool[s / block_size, s % block_size, 1, :, :] = enc(v[n])
+ * Tokens with slot_mapping[n] < 0 (padding) or past the pool are skipped.
+ *
+ * k, v          [n_tokens, num_kv_heads, head_size] of src_dtype; token n
+ *               starts at element n*src_token_stride (0 = num_kv_heads*head_size,
+ *               i.e. contiguous).  The stride in bytes must be a multiple of 16.
+ * k_cache, v_cache  the pool's K and V views (see conventions), kv_dtype.
+ * slot_mapping  int64 [n_tokens].
+ * kv_dtype == src_dtype (PA_F16/PA_BF16): the element bits are copied.
+ * kv_dtype == PA_E4M3 (src PA_F16, PA_BF16 or PA_F32): each element becomes
+ *   e4m3_rn_satfinite(float32(x) / kv_scale), one IEEE float32 division and
+ *   one round-to-nearest-even to E4M3 saturating at +-448 (NaN stays NaN).
+ *   kv_scale must be finite and > 0; it is ignored for 16-bit caches.
+ * Distinct tokens must name distinct slots (the last writer is unspecified).
+ */
+pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                               const int64_t* slot_mapping, int64_t n_tokens,
+                               int64_t src_token_stride, int num_blocks, int num_kv_heads,
+                               int head_size, int block_size, pa_dtype src_dtype,
+                               pa_dtype kv_dtype, float kv_scale, void* stream);
+
+/*
+ * pa_decode -- single-query attention for every sequence through its block table.
+ *
+ * Paging changes only where K/V live, so the result is standard attention
+ * ("vLLM GitHub 项目…", section 二; "vLLM 部署深度指南", section PagedAttention 方案):
+ * for sequence i with L = context_lens[i] and query head h (G = num_q_heads /
+ * num_kv_heads, KV head h / G),
+ *   K_i[j] = pool[block_tables[i, j / 16], j % 16, 0, h / G, :]   (j < L)
+ *   out[i, h, :] = softmax(scale * q[i, h, :] . K_i^T) . V_i
+ * with K/V dequantised as code * kv_scale for a PA_E4M3 cache.  L == 0 gives
+ * zeros.  context_lens count every cached token, including one written this
+ * step by pa_reshape_and_cache (which must be enqueued first).
+ *
+ * out, q        [num_seqs, num_q_heads, head_size] of q_dtype, contiguous.
+ * block_tables  int32 [num_seqs, max_blocks_per_seq], row-major; entries past
+ *               ceil(L / 16) are never read.
+ * context_lens  int32 [num_seqs], 0 <= L <= max_blocks_per_seq * 16.
+ * num_blocks    number of blocks in the pool (bounds the loads).
+ * partition_size  tokens per split-KV partition: 0 = library choice, else a
+ *               multiple of 16.  Sequences longer than one partition are
+ *               processed as partitions whose fp32 partial results are merged
+ *               by log-sum-exp (a second kernel on the same stream).
+ * workspace     device scratch of at least pa_decode_workspace_size(...) bytes
+ *               (256-byte aligned) for those partials; may be NULL when that
+ *               size is 0.  Its contents need no initialisation.  Calls that
+ *               share a workspace must not overlap in time.
+ */
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                    int max_blocks_per_seq, int num_blocks, int num_q_heads, int num_kv_heads,
+                    int head_size, int block_size, float scale, pa_dtype q_dtype,
+                    pa_dtype kv_dtype, float kv_scale, int partition_size, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/*
+ * pa_decode_workspace_size -- bytes of workspace pa_decode needs for these
+ * arguments (0 when no sequence can span more than one partition).  Host only;
+ * returns 0 and sets pa_last_error() for invalid arguments.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_size,
+                                int max_blocks_per_seq, int block_size, int partition_size);
+
+/*
+ * pa_decode_partition_size -- the partition size pa_decode uses when given
+ * partition_size (0 = the library's choice).  Host only; -1 on invalid input.
+ */
+int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_blocks_per_seq,
+                             int block_size, int partition_size);
+
+/*
+ * pa_gather_kv -- copy each sequence's cached K and V, in token order, into
+ * contiguous buffers: the block-table gather alone, bit for bit.
+ *
+ * Logical token j of sequence i is pool row block_tables[i, j/16]*16 + j%16
+ * ("vLLM 部署深度指南", section PagedAttention 方案, logical-view figure).
+ *   k_out[cu_seqlens[i] + j, :, :] = pool[block_tables[i, j/16], j%16, 0, :, :]
+ *   v_out[...]                      = pool[...,                        1, :, :]
+ * k_out, v_out  [cu_seqlens[num_seqs], num_kv_heads, head_size] of kv_dtype.
+ * cu_seqlens    int64 [num_seqs + 1] output row offsets (device); sequence i
+ *               fills rows [cu_seqlens[i], cu_seqlens[i] + context_lens[i]).
+ * Rows whose block id is out of range are left unwritten.
+ */
+pa_status pa_gather_kv(void* k_out, void* v_out, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* context_lens,
+                       const int64_t* cu_seqlens, int num_seqs, int max_blocks_per_seq,
+                       int num_blocks, int num_kv_heads, int head_size, int block_size,
+                       pa_dtype kv_dtype, void* stream);
+
+/*
+ * pa_check_tables -- validate the index arrays of one step (not on the hot path).
+ *
+ * Counts into counts_dev (int32 [3], device, overwritten):
+ *   [0] sequences with context_lens[i] < 0 or > max_blocks_per_seq*block_size;
+ *   [1] table entries j < ceil(L_i / block_size) outside [0, num_blocks);
+ *   [2] slot_mapping entries >= num_blocks*block_size (negative = padding, fine).
+ * slot_mapping may be NULL when n_tokens == 0.  If counts_host (int32 [3],
+ * host) is non-NULL the call synchronises the stream, copies the counts there
+ * and returns PA_ERR_BAD_INDEX when any is non-zero; otherwise it only
+ * enqueues the check.
+ */
+pa_status pa_check_tables(const int32_t* block_tables, const int32_t* context_lens,
+                          const int64_t* slot_mapping, int64_t n_tokens, int num_seqs,
+                          int max_blocks_per_seq, int num_blocks, int block_size,
+                          int32_t* counts_dev, int32_t* counts_host, void* stream);
+
+/*
+ * pa_device_status -- error bits raised by kernels on the current device
+ * instead of trapping (1 = a bounded wait inside a kernel timed out and the
+ * kernel returned early; its outputs are then invalid).  Synchronises the
+ * device.  `clear` != 0 resets the bits.  Returns 0xFFFFFFFF if the status
+ * word cannot be read.
+ */
+uint32_t pa_device_status(int clear);
+
+/* Message describing the last error returned on the calling thread ("" if none). */
+const char* pa_last_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

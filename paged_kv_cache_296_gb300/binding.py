@@ -1,0 +1,210 @@
+"""Python binding of libpagedattn.so: argument marshalling only.
+
+Every function has the name of the C entry point it calls (see include/pa.h)
+and turns torch tensors into the pointers, sizes and dtype codes that entry
+point takes; all computation runs in the library's CUDA kernels on the
+tensors' device and the current torch stream.  There is no fallback: if the
+library is missing or a call fails, an exception is raised.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libpagedattn.so")
+
+PA_F16, PA_BF16, PA_E4M3, PA_F32 = 0, 1, 2, 3
+STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
+                3: "PA_ERR_WORKSPACE", 4: "PA_ERR_CUDA", 5: "PA_ERR_BAD_INDEX"}
+
+#: Every function include/pa.h declares, with (restype, argtypes).
+_P, _I, _I64, _F, _SZ, _U32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                               ctypes.c_size_t, ctypes.c_uint32)
+SIGNATURES = {
+    "pa_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "pa_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _F, _I,
+                       _P, _SZ, _P]),
+    "pa_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "pa_decode_partition_size": (_I, [_I, _I, _I, _I, _I]),
+    "pa_gather_kv": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
+    "pa_check_tables": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P]),
+    "pa_device_status": (_U32, [_I]),
+    "pa_last_error": (ctypes.c_char_p, []),
+    "pa_version": (_I, []),
+}
+
+
+class PagedAttentionError(RuntimeError):
+    """A library call returned a non-zero pa_status."""
+
+    def __init__(self, fn, status, message):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path=LIB_PATH):
+    """Load the library (once) and declare its signatures.  Raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(fn, status):
+    if status != 0:
+        raise PagedAttentionError(fn, status, load().pa_last_error().decode())
+
+
+def dtype_code(dt):
+    if dt == torch.float16:
+        return PA_F16
+    if dt == torch.bfloat16:
+        return PA_BF16
+    if dt in (torch.uint8, getattr(torch, "float8_e4m3fn", None)):
+        return PA_E4M3
+    if dt == torch.float32:
+        return PA_F32
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def _stream(t):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def kv_views(pool):
+    """K and V views ``[num_blocks, 16, Hkv, D]`` of a pool ``[num_blocks, 16, 2, Hkv, D]``."""
+    if pool.dim() != 5 or pool.shape[2] != 2 or not pool.is_contiguous():
+        raise ValueError("pool must be a contiguous [num_blocks, block_size, 2, Hkv, D] tensor")
+    return pool[:, :, 0], pool[:, :, 1]
+
+
+def _cache_geometry(k_cache, v_cache):
+    """(num_blocks, block_size, Hkv, D) of K/V views, checking the pool strides."""
+    if k_cache.shape != v_cache.shape or k_cache.dim() != 4:
+        raise ValueError("k_cache and v_cache must be [num_blocks, block_size, Hkv, D] views")
+    nb, bs, hkv, d = k_cache.shape
+    want = (bs * 2 * hkv * d, 2 * hkv * d, d, 1)
+    if tuple(k_cache.stride()) != want or tuple(v_cache.stride()) != want:
+        raise ValueError("k_cache/v_cache must be the c=0/c=1 views of a "
+                         "[num_blocks, block_size, 2, Hkv, D] pool")
+    return nb, bs, hkv, d
+
+
+def pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, kv_scale=1.0):
+    """Write ``k``/``v`` ``[n_tokens, Hkv, D]`` into the pool at ``slot_mapping`` (int64)."""
+    nb, bs, hkv, d = _cache_geometry(k_cache, v_cache)
+    if k.shape != v.shape or k.dim() != 3 or k.stride() != v.stride() or k.stride(1) != d \
+            or k.stride(2) != 1:
+        raise ValueError("k and v must be [n_tokens, Hkv, D] with unit inner strides")
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous int64 tensor")
+    lib = load()
+    st = lib.pa_reshape_and_cache(
+        _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), k.shape[0],
+        k.stride(0), nb, hkv, d, bs, dtype_code(k.dtype), dtype_code(k_cache.dtype),
+        float(kv_scale), _stream(k_cache))
+    _check("pa_reshape_and_cache", st)
+
+
+def pa_decode_workspace_size(num_seqs, num_q_heads, head_size, max_blocks_per_seq,
+                             block_size=16, partition_size=0):
+    return int(load().pa_decode_workspace_size(num_seqs, num_q_heads, head_size,
+                                               max_blocks_per_seq, block_size, partition_size))
+
+
+def pa_decode_partition_size(num_seqs, num_kv_heads, max_blocks_per_seq, block_size=16,
+                             partition_size=0):
+    return int(load().pa_decode_partition_size(num_seqs, num_kv_heads, max_blocks_per_seq,
+                                               block_size, partition_size))
+
+
+def alloc_workspace(nbytes, device):
+    """Device scratch for pa_decode's split-KV partials (256-byte aligned), or None."""
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, kv_scale=1.0,
+              partition_size=0, workspace=None):
+    """Paged decode attention into ``out`` ``[B, Hq, D]``.
+
+    ``workspace``: a uint8 device tensor of at least ``pa_decode_workspace_size``
+    bytes; allocated here when omitted.
+    """
+    nb, bs, hkv, d = _cache_geometry(k_cache, v_cache)
+    B, hq, dq = q.shape
+    if dq != d or out.shape != q.shape or not q.is_contiguous() or not out.is_contiguous():
+        raise ValueError("q and out must be contiguous [B, Hq, D] tensors")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 \
+            or not block_tables.is_contiguous() or not context_lens.is_contiguous():
+        raise ValueError("block_tables and context_lens must be contiguous int32 tensors")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables must be [B, max_blocks], context_lens [B]")
+    mb = block_tables.shape[1]
+    need = pa_decode_workspace_size(B, hq, d, mb, bs, partition_size)
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().pa_decode(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        B, mb, nb, hq, hkv, d, bs, float(scale), dtype_code(q.dtype), dtype_code(k_cache.dtype),
+        float(kv_scale), int(partition_size), _ptr(workspace), wbytes, _stream(q))
+    _check("pa_decode", st)
+
+
+def pa_gather_kv(k_out, v_out, k_cache, v_cache, block_tables, context_lens, cu_seqlens):
+    """Copy each sequence's cached K/V rows, in token order, into ``k_out``/``v_out``."""
+    nb, bs, hkv, d = _cache_geometry(k_cache, v_cache)
+    B, mb = block_tables.shape
+    st = load().pa_gather_kv(
+        _ptr(k_out), _ptr(v_out), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        _ptr(context_lens), _ptr(cu_seqlens), B, mb, nb, hkv, d, bs, dtype_code(k_cache.dtype),
+        _stream(k_cache))
+    _check("pa_gather_kv", st)
+
+
+def pa_check_tables(block_tables, context_lens, slot_mapping, num_blocks, block_size=16):
+    """Validate index arrays; returns the three counts (see include/pa.h)."""
+    B, mb = block_tables.shape
+    counts_dev = torch.zeros(3, dtype=torch.int32, device=block_tables.device)
+    counts_host = (ctypes.c_int32 * 3)()
+    n = 0 if slot_mapping is None else slot_mapping.numel()
+    st = load().pa_check_tables(
+        _ptr(block_tables), _ptr(context_lens), _ptr(slot_mapping) if n else ctypes.c_void_p(0),
+        n, B, mb, num_blocks, block_size, _ptr(counts_dev), ctypes.cast(counts_host, ctypes.c_void_p),
+        _stream(block_tables))
+    counts = list(counts_host)
+    if st not in (0, 5):
+        _check("pa_check_tables", st)
+    return counts
+
+
+def pa_device_status(clear=True):
+    return int(load().pa_device_status(1 if clear else 0))
+
+
+def pa_last_error():
+    return load().pa_last_error().decode()
+
+
+def pa_version():
+    return int(load().pa_version())

@@ -1,0 +1,343 @@
+// extern "C" entry points of libpagedattn.so (declared in include/pa.h).
+//
+// Each entry point validates its arguments on the host, records a message for
+// pa_last_error() on failure, and otherwise enqueues kernels on the caller's
+// stream.  Nothing here allocates device memory.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdint>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+constexpr int kBlockSize = 16;
+constexpr int kDefaultPartitionTokens = 512;
+constexpr int kMaxGroup = 8;
+
+pa_status fail(pa_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+pa_status ok() {
+  g_last_error.clear();
+  return PA_OK;
+}
+
+pa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elt_bytes(pa_dtype d) {
+  switch (d) {
+    case PA_F16:
+    case PA_BF16:
+      return 2;
+    case PA_E4M3:
+      return 1;
+    case PA_F32:
+      return 4;
+  }
+  return 0;
+}
+
+// Partition size actually used, or -1 when the request is invalid.
+int partition_tokens(int max_blocks_per_seq, int requested) {
+  if (requested < 0 || requested % kBlockSize != 0) return -1;
+  return requested == 0 ? kDefaultPartitionTokens : requested;
+}
+
+int num_partitions(int max_blocks_per_seq, int part_tokens) {
+  const long long max_tokens = (long long)max_blocks_per_seq * kBlockSize;
+  const long long p = (max_tokens + part_tokens - 1) / part_tokens;
+  return (int)(p < 1 ? 1 : p);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct WorkspaceLayout {
+  size_t m_off, l_off, o_off, total;
+};
+
+WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_size, int nparts) {
+  WorkspaceLayout w{0, 0, 0, 0};
+  if (nparts <= 1) return w;
+  const size_t rows = (size_t)num_seqs * num_q_heads * nparts;
+  w.m_off = 0;
+  w.l_off = align256(rows * sizeof(float));
+  w.o_off = w.l_off + align256(rows * sizeof(float));
+  w.total = w.o_off + align256(rows * head_size * sizeof(float));
+  return w;
+}
+
+pa_status check_head_size(int head_size) {
+  if (head_size != 64 && head_size != 128)
+    return fail(PA_ERR_UNSUPPORTED, "head_size %d is not supported (64 or 128)", head_size);
+  return PA_OK;
+}
+
+pa_status check_block_size(int block_size) {
+  if (block_size != kBlockSize)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d is not supported (16 tokens per block)",
+                block_size);
+  return PA_OK;
+}
+
+pa_status check_pool(int num_blocks, int num_kv_heads) {
+  if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks must be > 0 (got %d)", num_blocks);
+  if ((long long)num_blocks * kBlockSize > 0x7FFFFFFFll)
+    return fail(PA_ERR_UNSUPPORTED, "num_blocks %d exceeds 2^31 token rows", num_blocks);
+  if (num_kv_heads <= 0)
+    return fail(PA_ERR_INVALID_ARG, "num_kv_heads must be > 0 (got %d)", num_kv_heads);
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_last_error(void) { return g_last_error.c_str(); }
+
+int pa_version(void) { return 100; }
+
+uint32_t pa_device_status(int clear) {
+  unsigned* p = nullptr;
+  if (pa::device_status_ptr(&p) != cudaSuccess) return 0xFFFFFFFFu;
+  unsigned v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return 0xFFFFFFFFu;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return 0xFFFFFFFFu;
+  if (clear && cudaMemset(p, 0, sizeof(unsigned)) != cudaSuccess) return 0xFFFFFFFFu;
+  return v;
+}
+
+pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                               const int64_t* slot_mapping, int64_t n_tokens,
+                               int64_t src_token_stride, int num_blocks, int num_kv_heads,
+                               int head_size, int block_size, pa_dtype src_dtype,
+                               pa_dtype kv_dtype, float kv_scale, void* stream) {
+  pa_status st;
+  if (n_tokens < 0) return fail(PA_ERR_INVALID_ARG, "n_tokens must be >= 0 (got %lld)", (long long)n_tokens);
+  if (n_tokens > 0x7FFFFFFFll) return fail(PA_ERR_UNSUPPORTED, "n_tokens exceeds 2^31-1");
+  if ((st = check_block_size(block_size)) != PA_OK) return st;
+  if ((st = check_head_size(head_size)) != PA_OK) return st;
+  if ((st = check_pool(num_blocks, num_kv_heads)) != PA_OK) return st;
+  const int se = elt_bytes(src_dtype), ke = elt_bytes(kv_dtype);
+  if (se == 0 || ke == 0) return fail(PA_ERR_INVALID_ARG, "unknown dtype code");
+  if (kv_dtype == PA_E4M3) {
+    if (src_dtype == PA_E4M3)
+      return fail(PA_ERR_UNSUPPORTED, "an E4M3 cache takes f16, bf16 or f32 sources");
+    if (!(kv_scale > 0.f) || kv_scale == INFINITY)
+      return fail(PA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an E4M3 cache");
+  } else if (kv_dtype == PA_F32) {
+    return fail(PA_ERR_UNSUPPORTED, "an f32 cache is not supported");
+  } else if (src_dtype != kv_dtype) {
+    return fail(PA_ERR_UNSUPPORTED, "a 16-bit cache takes sources of its own dtype");
+  }
+  const int64_t hkv_d = (int64_t)num_kv_heads * head_size;
+  if (hkv_d > (1 << 24)) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads*head_size too large");
+  const int64_t stride = src_token_stride == 0 ? hkv_d : src_token_stride;
+  if (stride < hkv_d)
+    return fail(PA_ERR_INVALID_ARG, "src_token_stride %lld is smaller than num_kv_heads*head_size",
+                (long long)src_token_stride);
+  if ((stride * se) % 16 != 0)
+    return fail(PA_ERR_INVALID_ARG, "src_token_stride must be a multiple of 16 bytes");
+  if (n_tokens == 0) return ok();
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping)
+    return fail(PA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "k, v, k_cache and v_cache must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
+    return fail(PA_ERR_INVALID_ARG, "slot_mapping must be 8-byte aligned");
+  cudaError_t e = pa::launch_reshape_and_cache(
+      k, v, k_cache, v_cache, slot_mapping, n_tokens, stride * se,
+      (int64_t)num_blocks * kBlockSize, (int)hkv_d, (int)src_dtype, (int)kv_dtype, kv_scale,
+      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "pa_reshape_and_cache launch");
+  return ok();
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_size,
+                                int max_blocks_per_seq, int block_size, int partition_size) {
+  if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || block_size != kBlockSize ||
+      (head_size != 64 && head_size != 128)) {
+    fail(PA_ERR_INVALID_ARG, "invalid arguments to pa_decode_workspace_size");
+    return 0;
+  }
+  const int part = partition_tokens(max_blocks_per_seq, partition_size);
+  if (part <= 0) {
+    fail(PA_ERR_INVALID_ARG, "partition_size must be 0 or a positive multiple of 16");
+    return 0;
+  }
+  const int np = num_partitions(max_blocks_per_seq, part);
+  return workspace_layout(num_seqs, num_q_heads, head_size, np).total;
+}
+
+int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_blocks_per_seq,
+                             int block_size, int partition_size) {
+  (void)num_seqs;
+  (void)num_kv_heads;
+  if (block_size != kBlockSize || max_blocks_per_seq <= 0) return -1;
+  return partition_tokens(max_blocks_per_seq, partition_size);
+}
+
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                    int max_blocks_per_seq, int num_blocks, int num_q_heads, int num_kv_heads,
+                    int head_size, int block_size, float scale, pa_dtype q_dtype,
+                    pa_dtype kv_dtype, float kv_scale, int partition_size, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  pa_status st;
+  if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs must be >= 0 (got %d)", num_seqs);
+  if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "num_seqs %d exceeds 65535", num_seqs);
+  if (max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be > 0 (got %d)", max_blocks_per_seq);
+  if ((st = check_block_size(block_size)) != PA_OK) return st;
+  if ((st = check_head_size(head_size)) != PA_OK) return st;
+  if ((st = check_pool(num_blocks, num_kv_heads)) != PA_OK) return st;
+  if (num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+                num_q_heads, num_kv_heads);
+  if (num_q_heads / num_kv_heads > kMaxGroup)
+    return fail(PA_ERR_UNSUPPORTED, "query heads per KV head %d exceeds %d",
+                num_q_heads / num_kv_heads, kMaxGroup);
+  if (num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads exceeds 65535");
+  if (q_dtype != PA_F16 && q_dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "q dtype must be PA_F16 or PA_BF16");
+  if (kv_dtype != q_dtype && kv_dtype != PA_E4M3)
+    return fail(PA_ERR_UNSUPPORTED, "cache dtype must equal the q dtype or be PA_E4M3");
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return fail(PA_ERR_INVALID_ARG, "scale must be finite");
+  if (kv_dtype == PA_E4M3 && (!(kv_scale > 0.f) || kv_scale == INFINITY))
+    return fail(PA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an E4M3 cache");
+  const int part = partition_tokens(max_blocks_per_seq, partition_size);
+  if (part <= 0)
+    return fail(PA_ERR_INVALID_ARG, "partition_size must be 0 or a positive multiple of 16 (got %d)",
+                partition_size);
+  const int np = num_partitions(max_blocks_per_seq, part);
+  if (np > 65535) return fail(PA_ERR_UNSUPPORTED, "too many partitions (%d)", np);
+  const WorkspaceLayout ws = workspace_layout(num_seqs, num_q_heads, head_size, np);
+  if (num_seqs == 0) return ok();
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return fail(PA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "out, q, k_cache and v_cache must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return fail(PA_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
+  if (ws.total > 0) {
+    if (!workspace || workspace_bytes < ws.total)
+      return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", ws.total,
+                  workspace ? workspace_bytes : (size_t)0);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+      return fail(PA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  }
+
+  pa::DecodeArgs a;
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.num_seqs = num_seqs;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_size = head_size;
+  a.q_dtype = (int)q_dtype;
+  a.kv_dtype = (int)kv_dtype;
+  a.scale = scale;
+  a.kv_scale = kv_dtype == PA_E4M3 ? kv_scale : 1.0f;
+  a.partition_tokens = part;
+  a.num_partitions = np;
+  auto* wsb = static_cast<uint8_t*>(workspace);
+  a.part_m = ws.total ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
+  a.part_l = ws.total ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
+  a.part_o = ws.total ? reinterpret_cast<float*>(wsb + ws.o_off) : nullptr;
+  cudaError_t e = pa::device_status_ptr(&a.status);
+  if (e != cudaSuccess) return cuda_fail(e, "pa_decode status word");
+
+  const char* why = "launch failed";
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (kv_dtype == PA_E4M3) {
+    e = pa::launch_decode_e4m3(a, s, &why);
+  } else if (kv_dtype == PA_BF16) {
+    e = pa::launch_decode_bf16(a, s, &why);
+  } else {
+    e = pa::launch_decode_f16(a, s, &why);
+  }
+  if (e == cudaErrorInvalidValue) return fail(PA_ERR_CUDA, "pa_decode: %s", why);
+  if (e != cudaSuccess) return cuda_fail(e, "pa_decode launch");
+  return ok();
+}
+
+pa_status pa_gather_kv(void* k_out, void* v_out, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* context_lens,
+                       const int64_t* cu_seqlens, int num_seqs, int max_blocks_per_seq,
+                       int num_blocks, int num_kv_heads, int head_size, int block_size,
+                       pa_dtype kv_dtype, void* stream) {
+  pa_status st;
+  if (num_seqs < 0 || num_seqs > 65535)
+    return fail(PA_ERR_INVALID_ARG, "num_seqs must be in [0, 65535] (got %d)", num_seqs);
+  if (max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be > 0 (got %d)", max_blocks_per_seq);
+  if ((st = check_block_size(block_size)) != PA_OK) return st;
+  if ((st = check_head_size(head_size)) != PA_OK) return st;
+  if ((st = check_pool(num_blocks, num_kv_heads)) != PA_OK) return st;
+  const int ke = elt_bytes(kv_dtype);
+  if (ke == 0 || kv_dtype == PA_F32) return fail(PA_ERR_UNSUPPORTED, "unsupported cache dtype");
+  if (num_seqs == 0) return ok();
+  if (!k_out || !v_out || !k_cache || !v_cache || !block_tables || !context_lens || !cu_seqlens)
+    return fail(PA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(k_out) || !aligned16(v_out) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "k_out, v_out, k_cache and v_cache must be 16-byte aligned");
+  const long long row = (long long)num_kv_heads * head_size * ke;
+  if (row > 0x7FFFFFFF) return fail(PA_ERR_UNSUPPORTED, "row too large");
+  cudaError_t e = pa::launch_gather_kv(k_out, v_out, k_cache, v_cache, block_tables, context_lens,
+                                       cu_seqlens, num_seqs, max_blocks_per_seq, num_blocks,
+                                       (int)row, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "pa_gather_kv launch");
+  return ok();
+}
+
+pa_status pa_check_tables(const int32_t* block_tables, const int32_t* context_lens,
+                          const int64_t* slot_mapping, int64_t n_tokens, int num_seqs,
+                          int max_blocks_per_seq, int num_blocks, int block_size,
+                          int32_t* counts_dev, int32_t* counts_host, void* stream) {
+  if (num_seqs < 0 || n_tokens < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
+      block_size <= 0)
+    return fail(PA_ERR_INVALID_ARG, "invalid sizes for pa_check_tables");
+  if (!counts_dev) return fail(PA_ERR_INVALID_ARG, "counts_dev is required");
+  if ((num_seqs > 0 && (!block_tables || !context_lens)) || (n_tokens > 0 && !slot_mapping))
+    return fail(PA_ERR_INVALID_ARG, "null pointer argument");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = pa::launch_check_tables(block_tables, context_lens, slot_mapping, n_tokens,
+                                          num_seqs, max_blocks_per_seq, num_blocks, block_size,
+                                          counts_dev, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pa_check_tables launch");
+  if (!counts_host) return ok();
+  e = cudaMemcpyAsync(counts_host, counts_dev, 3 * sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "pa_check_tables readback");
+  if (counts_host[0] || counts_host[1] || counts_host[2])
+    return fail(PA_ERR_BAD_INDEX,
+                "bad indices: %d context lengths, %d block-table entries, %d slots out of range",
+                counts_host[0], counts_host[1], counts_host[2]);
+  return ok();
+}
+
+}  // extern "C"

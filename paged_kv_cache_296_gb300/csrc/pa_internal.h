@@ -1,0 +1,67 @@
+// Internal host-side interface between the C entry points (pa_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pa {
+
+// Everything one pa_decode launch needs, already validated by the caller.
+struct DecodeArgs {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int num_seqs;
+  int max_blocks_per_seq;
+  int num_blocks;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_size;
+  int q_dtype;   // 0 f16, 1 bf16
+  int kv_dtype;  // 0 f16, 1 bf16, 2 e4m3
+  float scale;
+  float kv_scale;
+  int partition_tokens;
+  int num_partitions;
+  float* part_m;
+  float* part_l;
+  float* part_o;
+  unsigned* status;
+};
+
+// Per-dtype decode launchers (one translation unit each, compiled in parallel).
+cudaError_t launch_decode_f16(const DecodeArgs& a, cudaStream_t stream, const char** why);
+cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t stream, const char** why);
+cudaError_t launch_decode_e4m3(const DecodeArgs& a, cudaStream_t stream, const char** why);
+
+cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                                     const int64_t* slot_mapping, int64_t n_tokens,
+                                     int64_t src_stride_bytes, int64_t max_slot, int hkv_d,
+                                     int src_dtype, int kv_dtype, float kv_scale,
+                                     cudaStream_t stream);
+
+cudaError_t launch_gather_kv(void* k_out, void* v_out, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens,
+                             const int64_t* cu_seqlens, int num_seqs, int max_blocks_per_seq,
+                             int num_blocks, int row_bytes, cudaStream_t stream);
+
+cudaError_t launch_check_tables(const int32_t* block_tables, const int32_t* context_lens,
+                                const int64_t* slot_mapping, int64_t n_tokens, int num_seqs,
+                                int max_blocks_per_seq, int num_blocks, int block_size,
+                                int32_t* counts_dev, cudaStream_t stream);
+
+// Address of this library's device status word on the current device.
+cudaError_t device_status_ptr(unsigned** ptr);
+
+// Encodes a TMA descriptor for one view (K or V) of the pool, as used by the
+// decode kernel: rows of head_size elements per (token, kv head), 16 token
+// rows per box, 128B (or 64B) swizzle.  `desc` points to a CUtensorMap.
+bool encode_kv_tensor_map(void* desc, const void* base, int num_blocks, int num_kv_heads,
+                          int head_size, int elt_bytes, const char** why);
+
+}  // namespace pa

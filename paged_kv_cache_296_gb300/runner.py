@@ -1,0 +1,110 @@
+"""One decode step of the hot path on the GPU: reshape_and_cache, then paged decode.
+
+:class:`DecodeStep` holds a workload's device-resident state (pool, tables,
+lengths, q, the step's new k/v, output, split-KV workspace) and runs a step
+through the C ABI.  The pool is the cache: it stays in HBM between steps.
+"""
+
+import torch
+
+from . import binding as pa
+from .workloads import BLOCK_SIZE
+
+
+def fill_fp8_pool(pool_src, kv_scale, device, rows_per_call=1 << 16):
+    """An E4M3 pool quantised from fp32 values by pa_reshape_and_cache over every slot."""
+    nb, bs, _, hkv, d = pool_src.shape
+    pool = torch.zeros((nb, bs, 2, hkv, d), dtype=torch.uint8, device=device)
+    kc, vc = pa.kv_views(pool)
+    src = pool_src.reshape(nb * bs, 2, hkv, d)
+    for r0 in range(0, nb * bs, rows_per_call):
+        r1 = min(nb * bs, r0 + rows_per_call)
+        part = src[r0:r1].to(device)
+        slots = torch.arange(r0, r1, dtype=torch.int64, device=device)
+        pa.pa_reshape_and_cache(part[:, 0].contiguous(), part[:, 1].contiguous(), kc, vc, slots,
+                                kv_scale=kv_scale)
+    return pool
+
+
+class DecodeStep:
+    """Device buffers for one workload plus the step that runs on them."""
+
+    def __init__(self, W, device="cuda", partition_size=0):
+        self.W = W
+        self.device = torch.device(device)
+        spec = W.spec
+        if spec.kv_dtype == "e4m3":
+            self.pool = fill_fp8_pool(W.pool_src, W.kv_scale, self.device)
+        else:
+            # a copy: the step writes into its pool, the workload keeps the drawn values
+            self.pool = W.pool.to(self.device, copy=True)
+        self.k_cache, self.v_cache = pa.kv_views(self.pool)
+        self.q = W.q.to(self.device)
+        self.k_new = W.k_new.to(self.device)
+        self.v_new = W.v_new.to(self.device)
+        self.slot_mapping = W.slot_mapping.to(self.device)
+        self.block_tables = W.block_tables.to(self.device)
+        self.context_lens = W.context_lens.to(self.device)
+        self.out = torch.empty_like(self.q)
+        self.partition_size = partition_size
+        B, hq, d = self.q.shape
+        self.partition_tokens = pa.pa_decode_partition_size(
+            B, spec.num_kv_heads, W.max_blocks_per_seq, BLOCK_SIZE, partition_size)
+        self.workspace = pa.alloc_workspace(
+            pa.pa_decode_workspace_size(B, hq, d, W.max_blocks_per_seq, BLOCK_SIZE,
+                                        partition_size), self.device)
+        self.kv_scale = W.kv_scale
+        self.scale = W.scale
+
+    @property
+    def launches_per_step(self):
+        """Kernels one step enqueues: the write, the attention and (split-KV) the merge."""
+        lens = self.W.context_lens
+        split = bool((lens > self.partition_tokens).any())
+        return 2 + (1 if split else 0)
+
+    def write(self):
+        pa.pa_reshape_and_cache(self.k_new, self.v_new, self.k_cache, self.v_cache,
+                                self.slot_mapping, kv_scale=self.kv_scale)
+
+    def decode(self):
+        pa.pa_decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
+                     self.context_lens, self.scale, kv_scale=self.kv_scale,
+                     partition_size=self.partition_size, workspace=self.workspace)
+
+    def step(self):
+        self.write()
+        self.decode()
+        return self.out
+
+
+def step_bytes(W):
+    """Algorithmic bytes of one decode: attended K/V + q + out (and K/V alone).
+
+    Attended K/V counts every token of every sequence once per KV head:
+    ``sum_i L_i * Hkv * D * 2 * elt``.
+    """
+    spec = W.spec
+    elt = 1 if spec.kv_dtype == "e4m3" else 2
+    kv = int(W.context_lens.to(torch.int64).sum()) * spec.num_kv_heads * spec.head_size * 2 * elt
+    qo = 2 * W.q.numel() * W.q.element_size()
+    return kv + qo, kv
+
+
+def unique_kv_bytes(W):
+    """K/V bytes of distinct physical blocks' live tokens (shared prefixes counted once)."""
+    spec = W.spec
+    elt = 1 if spec.kv_dtype == "e4m3" else 2
+    seen = set()
+    total = 0
+    bt = W.block_tables.cpu().numpy()
+    for i, L in enumerate(W.context_lens.cpu().tolist()):
+        for j in range(-(-L // BLOCK_SIZE)):
+            b = int(bt[i, j])
+            n = min(BLOCK_SIZE, L - j * BLOCK_SIZE)
+            key = b
+            if key in seen:
+                continue
+            seen.add(key)
+            total += n
+    return total * spec.num_kv_heads * spec.head_size * 2 * elt

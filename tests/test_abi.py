@@ -1,0 +1,163 @@
+"""The C ABI on the host (CPU only): the library loads, exports every symbol
+include/pa.h declares, and rejects bad arguments before touching the GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_296_gb300 import binding as pa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_296_gb300 import build
+    build()
+    return pa.load()
+
+
+def header_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_\w+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = header_functions()
+    for n in ("pa_reshape_and_cache", "pa_decode", "pa_decode_workspace_size", "pa_gather_kv",
+              "pa_check_tables", "pa_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    assert set(header_functions()) == set(pa.SIGNATURES), "binding and header disagree"
+
+
+def test_version(lib):
+    assert pa.pa_version() >= 100
+
+
+FAKE = ctypes.c_void_p(0x10000)        # 16-byte aligned, never dereferenced
+MISALIGNED = ctypes.c_void_p(0x10008)
+NULL = ctypes.c_void_p(0)
+
+
+def decode_args(**over):
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, B=4, mb=8, nb=64, hq=8, hkv=2,
+             d=128, bs=16, scale=0.1, qd=pa.PA_F16, kvd=pa.PA_F16, kvs=1.0, part=0, ws=NULL,
+             wsb=0, stream=NULL)
+    a.update(over)
+    return [a[k] for k in ("out", "q", "k", "v", "bt", "cl", "B", "mb", "nb", "hq", "hkv", "d",
+                           "bs", "scale", "qd", "kvd", "kvs", "part", "ws", "wsb", "stream")]
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(out=NULL), 1),
+    (dict(q=MISALIGNED), 1),
+    (dict(d=96), 2),
+    (dict(bs=32), 2),
+    (dict(hq=6, hkv=4), 1),
+    (dict(hq=32, hkv=2), 2),             # 16 query heads per KV head
+    (dict(qd=pa.PA_E4M3), 2),
+    (dict(kvd=pa.PA_BF16), 2),           # cache dtype differs from q and is not E4M3
+    (dict(kvd=pa.PA_E4M3, kvs=0.0), 1),
+    (dict(kvd=pa.PA_E4M3, kvs=float("inf")), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(part=24), 1),                  # not a multiple of 16
+    (dict(mb=100), 3),                   # 1600 tokens > one 512-token partition: needs workspace
+    (dict(nb=0), 1),
+    (dict(B=-1), 1),
+    (dict(B=70000), 2),
+])
+def test_decode_rejects_bad_arguments(lib, over, status):
+    st = lib.pa_decode(*decode_args(**over))
+    assert st == status
+    assert pa.pa_last_error() != ""
+
+
+def test_decode_workspace_must_be_aligned(lib):
+    need = lib.pa_decode_workspace_size(4, 8, 128, 100, 16, 0)
+    st = lib.pa_decode(*decode_args(mb=100, ws=ctypes.c_void_p(0x10010), wsb=need))
+    assert st == 1
+
+
+def test_decode_zero_sequences_is_a_no_op(lib):
+    assert lib.pa_decode(*decode_args(B=0, out=NULL, q=NULL)) == 0
+    assert pa.pa_last_error() == ""
+
+
+def test_workspace_size(lib):
+    # one partition: nothing to merge, no workspace
+    assert lib.pa_decode_workspace_size(64, 32, 128, 32, 16, 0) == 0
+    assert lib.pa_decode_workspace_size(64, 32, 128, 32, 16, 512) == 0
+    # 128 blocks = 2048 tokens = 4 partitions of 512
+    rows = 64 * 32 * 4
+    al = lambda x: (x + 255) // 256 * 256
+    assert lib.pa_decode_workspace_size(64, 32, 128, 128, 16, 0) == 2 * al(rows * 4) + al(rows * 128 * 4)
+    assert lib.pa_decode_workspace_size(64, 32, 128, 128, 16, 256) == \
+        2 * al(rows * 2 * 4) + al(rows * 2 * 128 * 4)
+    assert lib.pa_decode_workspace_size(64, 32, 128, 128, 15, 0) == 0      # invalid block size
+    assert pa.pa_decode_partition_size(64, 8, 128) == 512
+    assert pa.pa_decode_partition_size(64, 8, 128, partition_size=48) == 48
+    assert pa.pa_decode_partition_size(64, 8, 128, partition_size=40) == -1
+
+
+def cache_args(**over):
+    a = dict(k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, sm=FAKE, n=4, stride=0, nb=64, hkv=2, d=128,
+             bs=16, sd=pa.PA_F16, kd=pa.PA_F16, kvs=1.0, stream=NULL)
+    a.update(over)
+    return [a[k] for k in ("k", "v", "kc", "vc", "sm", "n", "stride", "nb", "hkv", "d", "bs",
+                           "sd", "kd", "kvs", "stream")]
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(k=NULL), 1),
+    (dict(kc=MISALIGNED), 1),
+    (dict(sm=ctypes.c_void_p(0x10004)), 1),
+    (dict(n=-1), 1),
+    (dict(d=80), 2),
+    (dict(bs=8), 2),
+    (dict(sd=pa.PA_BF16), 2),                      # 16-bit cache from another dtype
+    (dict(kd=pa.PA_F32, sd=pa.PA_F32), 2),
+    (dict(kd=pa.PA_E4M3, sd=pa.PA_E4M3), 2),
+    (dict(kd=pa.PA_E4M3, kvs=-1.0), 1),
+    (dict(stride=100), 1),                         # smaller than Hkv*D
+    (dict(stride=260), 1),                         # 520 bytes: not a multiple of 16
+    (dict(nb=-5), 1),
+])
+def test_reshape_and_cache_rejects_bad_arguments(lib, over, status):
+    assert lib.pa_reshape_and_cache(*cache_args(**over)) == status
+    assert pa.pa_last_error() != ""
+
+
+def test_reshape_and_cache_zero_tokens_is_a_no_op(lib):
+    assert lib.pa_reshape_and_cache(*cache_args(n=0, k=NULL, v=NULL)) == 0
+
+
+def test_gather_and_check_reject_bad_arguments(lib):
+    st = lib.pa_gather_kv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 4, 8, 64, 2, 128, 16,
+                          pa.PA_F16, NULL)
+    assert st == 1
+    st = lib.pa_gather_kv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8, 64, 2, 128, 16,
+                          pa.PA_F32, NULL)
+    assert st == 2
+    assert lib.pa_check_tables(FAKE, FAKE, FAKE, 4, 4, 8, 64, 16, NULL, NULL, NULL) == 1
+    assert lib.pa_check_tables(FAKE, FAKE, FAKE, -1, 4, 8, 64, 16, FAKE, NULL, NULL) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import importlib
+    mod = importlib.import_module("paged_kv_cache_296_gb300.binding")
+    saved = mod._lib
+    try:
+        mod._lib = None
+        with pytest.raises(RuntimeError, match="missing"):
+            mod.load(str(tmp_path / "nope.so"))
+    finally:
+        mod._lib = saved

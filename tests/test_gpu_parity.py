@@ -1,0 +1,315 @@
+"""GPU parity: the CUDA library against the float64 oracle on the same seeded inputs.
+
+Writes and gathers must match bit for bit; attention must match within the
+stated tolerances (fp16 2e-3, bf16 1e-2, fp8-E4M3 cache 3e-2 against the
+oracle on the dequantised cache).  Unused pool slots are poisoned with NaN, so
+any stray read shows up as a NaN output.  Every call goes through the C ABI.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import e4m3
+from oracle import paged_attention as ref
+from paged_kv_cache_296_gb300 import binding as pa
+from paged_kv_cache_296_gb300 import workloads as wl
+
+import harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    pa.load()
+    pa.pa_device_status(clear=True)
+    yield
+    assert pa.pa_device_status(clear=True) == 0, "a kernel raised a device error bit"
+
+
+# ---------------------------------------------------------------- reshape_and_cache
+
+def _torch_dtype(name):
+    return {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[name]
+
+
+@pytest.mark.parametrize("src,kv", [("f16", "f16"), ("bf16", "bf16"), ("f16", "e4m3"),
+                                    ("bf16", "e4m3"), ("f32", "e4m3")])
+@pytest.mark.parametrize("head_size", [64, 128])
+def test_reshape_and_cache_bit_exact(src, kv, head_size):
+    g = torch.Generator().manual_seed(7)
+    nb, hkv, n = 40, 3, 200
+    if kv == "e4m3":
+        pool = torch.randint(0, 256, (nb, 16, 2, hkv, head_size), generator=g, dtype=torch.uint8)
+    else:
+        pool = torch.randn((nb, 16, 2, hkv, head_size), generator=g).to(_torch_dtype(kv))
+    # strided source: each token row padded by 8 elements (a fused-qkv layout)
+    stride_pad = 16 if src == "f32" else 8
+    full_k = (torch.randn((n, hkv * head_size + stride_pad), generator=g) * 3).to(_torch_dtype(src))
+    full_v = (torch.randn((n, hkv * head_size + stride_pad), generator=g) * 3).to(_torch_dtype(src))
+    if kv == "e4m3":
+        # saturation, NaN, signed zero, tiny values and exact ties on the write path
+        specials = torch.tensor([1e4, -1e4, float("nan"), -0.0, 1e-30, float("inf"),
+                                 -float("inf"), 0.1]).to(_torch_dtype(src))
+        full_k[0, :8] = specials
+        full_v[1, :8] = specials
+    k = full_k[:, :hkv * head_size].view(n, hkv, head_size)
+    v = full_v[:, :hkv * head_size].view(n, hkv, head_size)
+    perm = torch.randperm(nb * 16, generator=g)[:n].to(torch.int64)
+    perm[::7] = -1                                   # padding tokens
+    perm[5] = nb * 16 + 3                            # past the pool: skipped
+    kv_scale = 0.037
+
+    dev_pool = pool.cuda()
+    kc, vc = pa.kv_views(dev_pool)
+    pa.pa_reshape_and_cache(k.cuda(), v.cuda(), kc, vc, perm.cuda(), kv_scale=kv_scale)
+    got = H.bits_of(dev_pool.cpu())
+
+    slots = perm.numpy().copy()
+    slots[slots >= nb * 16] = -1                     # the oracle's pool has no such slot
+    want = ref.reshape_and_cache(H.bits_of(pool), H.bits_of(k.contiguous()),
+                                 H.bits_of(v.contiguous()), slots, src, kv, kv_scale)
+    if kv == "e4m3":
+        nan_w, nan_g = e4m3.is_nan_code(want), e4m3.is_nan_code(got)
+        assert np.array_equal(nan_w, nan_g)
+        assert np.array_equal(got[~nan_g], want[~nan_w])
+        assert nan_w.any()
+    else:
+        assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------- gather
+
+@pytest.mark.parametrize("kv", ["f16", "bf16", "e4m3"])
+def test_gather_bit_exact(kv):
+    spec = wl.random_spec(3, head_size=128, group=2, kv_dtype=kv, max_len=90, max_seqs=6)
+    W = wl.make_workload(spec, 31, poison=True, table_garbage=True)
+    pool = H.gpu_pool(W)
+    kc, vc = pa.kv_views(pool)
+    lens = W.context_lens.numpy()
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    total = int(cu[-1])
+    hkv, d = spec.num_kv_heads, spec.head_size
+    ko = torch.zeros((max(total, 1), hkv, d), dtype=pool.dtype, device="cuda")
+    vo = torch.zeros_like(ko)
+    pa.pa_gather_kv(ko, vo, kc, vc, W.block_tables.cuda(), W.context_lens.cuda(),
+                    torch.from_numpy(cu).cuda())
+    ko, vo = H.bits_of(ko.cpu()), H.bits_of(vo.cpu())
+    if kv == "e4m3":
+        opool = ref.fp8_quantise(H.bits_of(W.pool_src), "f32", W.kv_scale)
+    else:
+        opool = H.bits_of(W.pool)
+    for i, L in enumerate(lens):
+        k, v = ref.gather_kv(opool, W.block_tables[i].numpy(), int(L), 16)
+        for got, want in ((ko[cu[i]:cu[i + 1]], k), (vo[cu[i]:cu[i + 1]], v)):
+            if kv == "e4m3":   # NaN codes (poisoned slots) may differ in sign only
+                nan = e4m3.is_nan_code(want)
+                assert np.array_equal(e4m3.is_nan_code(got), nan)
+                assert np.array_equal(got[~nan], want[~nan])
+            else:
+                assert np.array_equal(got, want)
+
+
+def test_fp8_pool_fill_matches_oracle_encoding():
+    spec = wl.random_spec(4, head_size=64, group=4, kv_dtype="e4m3", max_len=60)
+    W = wl.make_workload(spec, 41, poison=True)
+    got = H.bits_of(H.gpu_pool(W).cpu())
+    want = ref.fp8_quantise(H.bits_of(W.pool_src), "f32", W.kv_scale)
+    assert np.array_equal(e4m3.is_nan_code(got), e4m3.is_nan_code(want))
+    ok = ~e4m3.is_nan_code(want)
+    assert np.array_equal(got[ok], want[ok])
+
+
+# ---------------------------------------------------------------- decode: the five workloads
+
+def _full_check(W, partition_size=0):
+    spec = W.spec
+    pool = H.gpu_pool(W)
+    out = H.gpu_step(W, pool, partition_size=partition_size)
+    got = H.widen_out(out, spec.q_dtype)
+    assert np.isfinite(got).all(), "NaN/inf output: a poisoned slot was read"
+    opool = H.oracle_pool_after_step(W)
+    assert np.array_equal(H.bits_of(pool.cpu()), opool), "pool after the write differs"
+    want = H.oracle_decode_full(W, opool)
+    return H.assert_close(got, want, spec, spec.name)
+
+
+def test_config1_tiny():
+    W = wl.make_workload(wl.SPECS[1], 1, poison=True, table_garbage=True)
+    _full_check(W)
+
+
+@pytest.mark.parametrize("n", [2, 3, 4])
+def test_full_size_config_all_outputs(n):
+    W = wl.make_workload(wl.SPECS[n], n, poison=True)
+    _full_check(W)
+
+
+def test_config5_long_fp8_sampled():
+    """Long-context fp8 workload at full size: every sequence, one KV head each,
+    checked against the oracle on the dequantised cache; the pool bytes of
+    those heads checked bit for bit."""
+    W = wl.make_workload(wl.SPECS[5], 5, poison=True)
+    spec = W.spec
+    pool = H.gpu_pool(W)
+    out = H.gpu_step(W, pool)
+    got_all = H.widen_out(out, spec.q_dtype)
+    assert np.isfinite(got_all).all()
+    g = spec.num_q_heads // spec.num_kv_heads
+    rng = np.random.default_rng(5)
+    for i in range(spec.num_seqs):
+        h = int(rng.integers(spec.num_kv_heads))
+        blocks, mini = H.mini_case(W, i, h)
+        opool, want = H.oracle_mini(W, mini)
+        gpool = H.bits_of(pool[torch.from_numpy(blocks).cuda()][:, :, :, h:h + 1].cpu())
+        assert np.array_equal(e4m3.is_nan_code(gpool), e4m3.is_nan_code(opool))
+        live = ~e4m3.is_nan_code(opool)
+        assert np.array_equal(gpool[live], opool[live])
+        H.assert_close(got_all[i, h * g:(h + 1) * g], want, spec, f"seq {i} kv head {h}")
+
+
+# ---------------------------------------------------------------- decode: sweeps and edges
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_shapes(seed):
+    spec = wl.random_spec(seed)
+    W = wl.make_workload(spec, 1000 + seed, poison=True, table_garbage=True)
+    if spec.kv_dtype == "e4m3":
+        pool = H.gpu_pool(W)
+        out = H.gpu_step(W, pool, partition_size=spec.partition_size)
+        got = H.widen_out(out, spec.q_dtype)
+        for i in range(spec.num_seqs):
+            for h in range(spec.num_kv_heads):
+                g = spec.num_q_heads // spec.num_kv_heads
+                _, mini = H.mini_case(W, i, h)
+                _, want = H.oracle_mini(W, mini)
+                H.assert_close(got[i, h * g:(h + 1) * g], want, spec, f"{spec.name} s{i} h{h}")
+    else:
+        _full_check(W, partition_size=spec.partition_size)
+
+
+EDGE_LENS = [0, 1, 2, 15, 16, 17, 31, 32, 33, 511, 512, 513, 1000]
+
+
+@pytest.mark.parametrize("kv,q", [("f16", "f16"), ("bf16", "bf16"), ("e4m3", "bf16"),
+                                  ("e4m3", "f16")])
+@pytest.mark.parametrize("head_size,group", [(64, 1), (128, 4), (128, 8), (64, 3)])
+@pytest.mark.parametrize("part", [16, 48, 0])
+def test_edge_context_lengths(kv, q, head_size, group, part):
+    spec = wl.Spec("edges", len(EDGE_LENS), 2 * group, 2, head_size, q, kv,
+                   ("fixed", EDGE_LENS), ("factor", 1.3))
+    W = wl.make_workload(spec, 77, poison=True, table_garbage=True)
+    pool = H.gpu_pool(W)
+    out = H.gpu_step(W, pool, partition_size=part)
+    got = H.widen_out(out, q)
+    assert np.isfinite(got).all()
+    assert np.array_equal(got[0], np.zeros_like(got[0])), "empty context must give zeros"
+    if kv != "e4m3":
+        want = H.oracle_decode_full(W, H.oracle_pool_after_step(W))
+        H.assert_close(got, want, spec, "edges")
+        # context length 1 returns v0 (the token written this step) exactly
+        v0 = ref.widen(H.bits_of(W.v_new[1]), kv)
+        for h in range(spec.num_q_heads):
+            assert np.array_equal(got[1, h], v0[h // group])
+    else:
+        for i in range(spec.num_seqs):
+            for h in range(spec.num_kv_heads):
+                _, mini = H.mini_case(W, i, h)
+                _, want = H.oracle_mini(W, mini)
+                H.assert_close(got[i, h * group:(h + 1) * group], want, spec, f"s{i} h{h}")
+
+
+def test_all_equal_keys_give_mean_of_v():
+    spec = wl.Spec("equal keys", 3, 8, 2, 128, "f16", "f16", ("fixed", [40, 300, 700]))
+    W = wl.make_workload(spec, 9)
+    # one key row for every token of every sequence
+    W.pool[:, :, 0] = W.pool[0, 0, 0]
+    W.k_new[:] = W.pool[0, 0, 0]
+    out = H.widen_out(H.gpu_step(W, H.gpu_pool(W)), "f16")
+    opool = H.oracle_pool_after_step(W)
+    for i, L in enumerate(W.context_lens.numpy()):
+        _, v = ref.gather_kv(opool, W.block_tables[i].numpy(), int(L), 16)
+        mean = ref.widen(v, "f16").mean(axis=0)
+        for h in range(8):
+            np.testing.assert_allclose(out[i, h], mean[h // 4], atol=2e-3, rtol=0)
+
+
+# ---------------------------------------------------------------- bitwise invariants on the GPU
+
+def _relabel(W, perm):
+    """The same workload with physical block b moved to perm[b]."""
+    pool = torch.empty_like(W.pool)
+    pool[torch.from_numpy(perm)] = W.pool
+    bt = W.block_tables.numpy().copy()
+    live = bt >= 0
+    bt[live] = perm[bt[live]]
+    slots = W.slot_mapping.numpy().copy()
+    ok = slots >= 0
+    slots[ok] = perm[slots[ok] // 16] * 16 + slots[ok] % 16
+    import dataclasses
+    return dataclasses.replace(W, pool=pool, block_tables=torch.from_numpy(bt.astype(np.int32)),
+                               slot_mapping=torch.from_numpy(slots))
+
+
+@pytest.mark.parametrize("n", [2, 4])
+def test_block_permutation_invariance_bitwise(n):
+    spec = wl.SPECS[n]
+    small = wl.Spec(spec.name, 12, spec.num_q_heads, spec.num_kv_heads, spec.head_size,
+                    spec.q_dtype, spec.kv_dtype,
+                    spec.lens if spec.lens[0] != "shared_prefix" else ("shared_prefix", 3, 4, 1024, 256))
+    W = wl.make_workload(small, 50 + n)
+    a = H.gpu_step(W, H.gpu_pool(W)).cpu()
+    perm = np.random.default_rng(n).permutation(W.num_blocks)
+    W2 = _relabel(W, perm)
+    b = H.gpu_step(W2, H.gpu_pool(W2)).cpu()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_shared_prefix_equals_private_copies_bitwise():
+    spec = wl.Spec("shared", 8, 32, 8, 128, "f16", "f16", ("shared_prefix", 2, 4, 1024, 256))
+    W = wl.make_workload(spec, 61)
+    a = H.gpu_step(W, H.gpu_pool(W)).cpu()
+    # give every sequence private copies of its prefix blocks
+    bt = W.block_tables.numpy().copy()
+    extra, pool = [], W.pool
+    nxt = W.num_blocks
+    copies = []
+    for i in range(spec.num_seqs):
+        for j in range(64):
+            copies.append(bt[i, j])
+            bt[i, j] = nxt
+            nxt += 1
+    pool = torch.cat([pool, pool[torch.tensor(copies)]], dim=0)
+    import dataclasses
+    W2 = dataclasses.replace(W, pool=pool, num_blocks=nxt,
+                             block_tables=torch.from_numpy(bt.astype(np.int32)))
+    b = H.gpu_step(W2, H.gpu_pool(W2)).cpu()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_deterministic_and_split_matches_unsplit():
+    W = wl.make_workload(wl.SPECS[3], 3)
+    pool = H.gpu_pool(W)
+    a = H.gpu_step(W, pool).cpu()
+    b = H.gpu_step(W, pool).cpu()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    whole = H.gpu_step(W, pool, partition_size=4096).cpu()      # one partition per sequence
+    err = (a.float() - whole.float()).abs().max().item()
+    assert err <= 1e-2, err
+
+
+def test_check_tables_counts_bad_indices():
+    W = wl.make_workload(wl.SPECS[1], 1, table_garbage=True)
+    bt, cl, sm = W.block_tables.cuda(), W.context_lens.cuda(), W.slot_mapping.cuda()
+    assert pa.pa_check_tables(bt, cl, sm, W.num_blocks) == [0, 0, 0]
+    bt2 = W.block_tables.clone()
+    bt2[3, 1] = W.num_blocks          # sequence 3 (17 tokens) uses two blocks
+    cl2 = W.context_lens.clone()
+    cl2[0] = 10 ** 6
+    sm2 = W.slot_mapping.clone()
+    sm2[2] = W.num_blocks * 16
+    counts = pa.pa_check_tables(bt2.cuda(), cl2.cuda(), sm2.cuda(), W.num_blocks)
+    assert counts == [1, 1, 1]
