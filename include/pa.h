@@ -177,7 +177,8 @@ pa_status pa_gather_kv(void* k_out, void* v_out, const void* k_cache, const void
  *
  * Counts into counts_dev (int32 [3], device, overwritten):
  *   [0] sequences with context_lens[i] < 0 or > max_blocks_per_seq*block_size;
- *   [1] table entries j < ceil(L_i / block_size) outside [0, num_blocks);
+ *   [1] table entries j < ceil(L_i / block_size) outside [0, num_blocks), over
+ *       the sequences whose length passed check [0];
  *   [2] slot_mapping entries >= num_blocks*block_size (negative = padding, fine).
  * slot_mapping may be NULL when n_tokens == 0.  If counts_host (int32 [3],
  * host) is non-NULL the call synchronises the stream, copies the counts there

@@ -147,10 +147,13 @@ __device__ __forceinline__ void load8(const uint8_t* p, float (&x)[8]) {
   }
 }
 
-// One CTA per new token.  16-bit caches copy 16-byte vectors; the E4M3 cache
-// quantises 8 elements per thread step and stores 8 bytes.
+// Grid (token, chunk): each thread moves one 16-byte vector of K or V (16-bit
+// caches) or quantises 8 elements into 8 bytes (E4M3 cache), so every load of
+// a token is in flight at once.
+constexpr int kWriteThreads = 256;
+
 template <int SRC, bool FP8>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kWriteThreads)
     reshape_and_cache_kernel(const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
                              uint8_t* __restrict__ kc, uint8_t* __restrict__ vc,
                              const int64_t* __restrict__ slots, int64_t src_stride_bytes,
@@ -160,39 +163,34 @@ __global__ void __launch_bounds__(128)
   if (s < 0 || s >= max_slot) return;  // padding, or a slot past the pool
   const uint8_t* ks = k + n * src_stride_bytes;
   const uint8_t* vs = v + n * src_stride_bytes;
+  const int i = blockIdx.y * kWriteThreads + threadIdx.x;
   if constexpr (!FP8) {
     const int64_t tok_stride = 2ll * hkv_d * 2;
-    uint8_t* kd = kc + s * tok_stride;
-    uint8_t* vd = vc + s * tok_stride;
     const int nvec = hkv_d * 2 / 16;
-    for (int i = threadIdx.x; i < 2 * nvec; i += blockDim.x) {
-      const bool isv = i >= nvec;
-      const int j = isv ? i - nvec : i;
-      const uint4 x = reinterpret_cast<const uint4*>(isv ? vs : ks)[j];
-      reinterpret_cast<uint4*>(isv ? vd : kd)[j] = x;
-    }
+    if (i >= 2 * nvec) return;
+    const bool isv = i >= nvec;
+    const int j = isv ? i - nvec : i;
+    const uint4 x = reinterpret_cast<const uint4*>(isv ? vs : ks)[j];
+    reinterpret_cast<uint4*>((isv ? vc : kc) + s * tok_stride)[j] = x;
   } else {
     constexpr int kSrcElt = (SRC == kSrcF32) ? 4 : 2;
     const int64_t tok_stride = 2ll * hkv_d;
-    uint8_t* kd = kc + s * tok_stride;
-    uint8_t* vd = vc + s * tok_stride;
     const int ngrp = hkv_d / 8;
-    for (int i = threadIdx.x; i < 2 * ngrp; i += blockDim.x) {
-      const bool isv = i >= ngrp;
-      const int j = isv ? i - ngrp : i;
-      float x[8];
-      load8<SRC>((isv ? vs : ks) + (size_t)j * 8 * kSrcElt, x);
-      uint32_t w[2];
+    if (i >= 2 * ngrp) return;
+    const bool isv = i >= ngrp;
+    const int j = isv ? i - ngrp : i;
+    float x[8];
+    load8<SRC>((isv ? vs : ks) + (size_t)j * 8 * kSrcElt, x);
+    uint32_t w[2];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint16_t a = f32x2_to_e4m3x2(__fdiv_rn(x[4 * h], kv_scale),
-                                           __fdiv_rn(x[4 * h + 1], kv_scale));
-        const uint16_t b = f32x2_to_e4m3x2(__fdiv_rn(x[4 * h + 2], kv_scale),
-                                           __fdiv_rn(x[4 * h + 3], kv_scale));
-        w[h] = (uint32_t)a | ((uint32_t)b << 16);
-      }
-      reinterpret_cast<uint2*>(isv ? vd : kd)[j] = make_uint2(w[0], w[1]);
+    for (int h = 0; h < 2; ++h) {
+      const uint16_t a = f32x2_to_e4m3x2(__fdiv_rn(x[4 * h], kv_scale),
+                                         __fdiv_rn(x[4 * h + 1], kv_scale));
+      const uint16_t b = f32x2_to_e4m3x2(__fdiv_rn(x[4 * h + 2], kv_scale),
+                                         __fdiv_rn(x[4 * h + 3], kv_scale));
+      w[h] = (uint32_t)a | ((uint32_t)b << 16);
     }
+    reinterpret_cast<uint2*>((isv ? vc : kc) + s * tok_stride)[j] = make_uint2(w[0], w[1]);
   }
 }
 
@@ -204,22 +202,23 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache
                                      int src_dtype, int kv_dtype, float kv_scale,
                                      cudaStream_t stream) {
   if (n_tokens == 0) return cudaSuccess;
-  const dim3 grid((unsigned)n_tokens);
+  const int units = (kv_dtype != 2) ? 2 * (hkv_d * 2 / 16) : 2 * (hkv_d / 8);
+  const dim3 grid((unsigned)n_tokens, (unsigned)((units + kWriteThreads - 1) / kWriteThreads));
   const auto* kk = static_cast<const uint8_t*>(k);
   const auto* vv = static_cast<const uint8_t*>(v);
   auto* kc = static_cast<uint8_t*>(k_cache);
   auto* vc = static_cast<uint8_t*>(v_cache);
   if (kv_dtype != 2) {
-    reshape_and_cache_kernel<kSrcF16, false><<<grid, 128, 0, stream>>>(
+    reshape_and_cache_kernel<kSrcF16, false><<<grid, kWriteThreads, 0, stream>>>(
         kk, vv, kc, vc, slot_mapping, src_stride_bytes, max_slot, hkv_d, kv_scale);
   } else if (src_dtype == 0) {
-    reshape_and_cache_kernel<kSrcF16, true><<<grid, 128, 0, stream>>>(
+    reshape_and_cache_kernel<kSrcF16, true><<<grid, kWriteThreads, 0, stream>>>(
         kk, vv, kc, vc, slot_mapping, src_stride_bytes, max_slot, hkv_d, kv_scale);
   } else if (src_dtype == 1) {
-    reshape_and_cache_kernel<kSrcBf16, true><<<grid, 128, 0, stream>>>(
+    reshape_and_cache_kernel<kSrcBf16, true><<<grid, kWriteThreads, 0, stream>>>(
         kk, vv, kc, vc, slot_mapping, src_stride_bytes, max_slot, hkv_d, kv_scale);
   } else {
-    reshape_and_cache_kernel<kSrcF32, true><<<grid, 128, 0, stream>>>(
+    reshape_and_cache_kernel<kSrcF32, true><<<grid, kWriteThreads, 0, stream>>>(
         kk, vv, kc, vc, slot_mapping, src_stride_bytes, max_slot, hkv_d, kv_scale);
   }
   return cudaGetLastError();
@@ -291,9 +290,11 @@ __global__ void check_tables_kernel(const int32_t* __restrict__ tables,
     const int seq = (int)(idx / max_blocks);
     const int j = (int)(idx - (int64_t)seq * max_blocks);
     const int64_t L = lens[seq];
-    if (j == 0 && (L < 0 || L > max_len)) atomicAdd(&counts[0], 1);
-    const int64_t Lc = L < 0 ? 0 : (L > max_len ? max_len : L);
-    const int64_t nb = (Lc + block_size - 1) / block_size;
+    if (L < 0 || L > max_len) {  // counted once; its table is not judged
+      if (j == 0) atomicAdd(&counts[0], 1);
+      continue;
+    }
+    const int64_t nb = (L + block_size - 1) / block_size;
     if (j < nb) {
       const int32_t e = tables[idx];
       if (e < 0 || e >= num_blocks) atomicAdd(&counts[1], 1);

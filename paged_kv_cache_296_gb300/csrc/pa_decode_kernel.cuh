@@ -64,9 +64,16 @@ struct DecodeCfg {
   static constexpr int kRowBytes = D * kElt;          // one token row of one head
   static constexpr int kTileBytes = 16 * kRowBytes;   // one block of K (or V) for one head
   static constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
-  static constexpr int kStages = (kStageBytes >= 8192) ? 6 : 12;
-  static constexpr int kSwizzle = (kRowBytes >= 128) ? 128 : 64;
   static constexpr int kConsumerWarps = 4;
+  // Block `it` goes to stage it % kStages and to consumer warp it % 4.  With
+  // kStages a multiple of 4, every stage has one consumer warp that waits on
+  // its phases strictly in order, so a parity wait never runs two phases ahead
+  // of its barrier (which would let it pass early).  Two or more stages per
+  // warp let the producer run ahead while a warp computes.
+  static constexpr int kStages = (kStageBytes >= 8192) ? 8 : 12;
+  static_assert(kStages % kConsumerWarps == 0 && kStages >= 2 * kConsumerWarps,
+                "each stage must belong to exactly one consumer warp");
+  static constexpr int kSwizzle = (kRowBytes >= 128) ? 128 : 64;
   static constexpr int kThreads = (kConsumerWarps + 1) * 32;
   static constexpr int kMTiles = D / 16;              // m-tiles of O^T, k-steps of S^T
   static constexpr int kRedStride = D + 4;            // floats per head row in the merge buffer
