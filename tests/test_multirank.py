@@ -1,0 +1,86 @@
+"""The N>1 bench path on CPU: replicas with gloo, world size 2.
+
+Each rank runs its own batch (weak scaling, no data-path collective); the only
+cross-rank step is the timing reduction (max over ranks) and the byte sum.
+"""
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, out_q):
+    import bench
+    from paged_kv_cache_296_gb300 import workloads as wl
+    torch.distributed.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}",
+                                         rank=rank, world_size=world)
+    dev = torch.device("cpu")
+    mx = bench.max_over_ranks(1.5 + rank, world, dev)
+    sm = bench.sum_over_ranks(10.0 * (rank + 1), world, dev)
+    W = wl.make_workload(wl.SPECS[2], 2 + 1000 * rank)     # the seed rule bench.py uses
+    out_q.put((rank, mx, sm, W.context_lens.tolist()))
+    bench.barrier(world)
+    torch.distributed.destroy_process_group()
+
+
+def test_replica_reductions_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=300) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    (_, mx0, sm0, lens0), (_, mx1, sm1, lens1) = res
+    assert mx0 == mx1 == 2.5          # the slowest rank sets the time
+    assert sm0 == sm1 == 30.0         # bytes add up over ranks
+    assert lens0 != lens1             # each replica has its own batch
+
+
+def _run_bench(args, env_extra):
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                          capture_output=True, text=True, env=env, timeout=600, cwd=ROOT)
+
+
+def test_reference_arm_prints_one_line():
+    r = _run_bench(["--impl", "reference", "--config", "1", "--steps", "2", "--warmup", "3",
+                    "--ref-seconds", "1"], {})
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["steps"] == 2 and d["warmup"] == 3
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    r = _run_bench(["--impl", "reference", "--config", "1", "--steps", "2", "--warmup", "3"],
+                   {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
+
+
+def test_bench_rejects_short_warmup():
+    r = _run_bench(["--impl", "reference", "--warmup", "2"], {})
+    assert r.returncode != 0
