@@ -14,5 +14,5 @@ from .binding import (  # noqa: F401
 
 def build(force=False):
     """Compile the CUDA library in-tree (nvcc, sm_103a) and return its path."""
-    from .build import build as _build
+    from .native_build import build as _build
     return _build(force=force)
