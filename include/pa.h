@@ -139,6 +139,44 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                     size_t workspace_bytes, void* stream);
 
 /*
+ * pa_decode_noalloc -- pa_decode for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this call: it exists for callers with no
+ * device allocator of their own (a plugin or extension that its host runtime
+ * hands only input and output buffers), or that must not allocate while they
+ * serve (cudaMalloc can synchronise the device and carves up a memory budget
+ * fixed in advance).  It computes exactly what pa_decode computes, with the
+ * same arguments minus the workspace.  The caller still passes every input
+ * and output.
+ *
+ * Scratch: the split-KV partials live in one array compiled into the library,
+ * PA_DECODE_NOALLOC_SCRATCH_BYTES (64 MiB) per device.  It is reserved on each
+ * device whose context loads it and is held until the process exits.  The call
+ * itself allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before capturing any stream on that device.
+ * Limit: if these sizes need more scratch than the array holds
+ * (pa_decode_workspace_size(...) > PA_DECODE_NOALLOC_SCRATCH_BYTES) the call
+ * returns PA_ERR_WORKSPACE and enqueues nothing; a larger partition_size needs
+ * less scratch.
+ * Sharing: every call on a device uses the same array, which keeps whatever
+ * the last call left there.  Nothing in it has to start at zero (each partial
+ * the merge reads is written earlier in the same call), but calls whose work
+ * overlaps on the GPU (different streams, no ordering between them) race on
+ * it.  Serialise them, for example by issuing them on one stream.
+ */
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            int num_seqs, int max_blocks_per_seq, int num_blocks,
+                            int num_q_heads, int num_kv_heads, int head_size, int block_size,
+                            float scale, pa_dtype q_dtype, pa_dtype kv_dtype, float kv_scale,
+                            int partition_size, void* stream);
+
+/*
  * pa_decode_workspace_size -- bytes of workspace pa_decode needs for these
  * arguments (0 when no sequence can span more than one partition).  Host only;
  * returns 0 and sets pa_last_error() for invalid arguments.

@@ -26,6 +26,8 @@ SIGNATURES = {
     "pa_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I, _I, _I, _I, _I, _I, _F, _P]),
     "pa_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _F, _I,
                        _P, _SZ, _P]),
+    "pa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
+                               _F, _I, _P]),
     "pa_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "pa_decode_partition_size": (_I, [_I, _I, _I, _I, _I]),
     "pa_gather_kv": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
@@ -169,6 +171,33 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, kv_sc
         B, mb, nb, hq, hkv, d, bs, float(scale), dtype_code(q.dtype), dtype_code(k_cache.dtype),
         float(kv_scale), int(partition_size), _ptr(workspace), wbytes, _stream(q))
     _check("pa_decode", st)
+
+
+#: Bytes of the library's fixed split-KV scratch used by pa_decode_noalloc.
+DECODE_NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale, kv_scale=1.0,
+                      partition_size=0):
+    """Paged decode with the library's own fixed scratch: no workspace, no allocation.
+
+    For callers that cannot allocate device memory.  Calls on one device share
+    that scratch, so calls that overlap on the GPU race; keep them on one stream.
+    """
+    nb, bs, hkv, d = _cache_geometry(k_cache, v_cache)
+    B, hq, dq = q.shape
+    if dq != d or out.shape != q.shape or not q.is_contiguous() or not out.is_contiguous():
+        raise ValueError("q and out must be contiguous [B, Hq, D] tensors")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 \
+            or not block_tables.is_contiguous() or not context_lens.is_contiguous():
+        raise ValueError("block_tables and context_lens must be contiguous int32 tensors")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables must be [B, max_blocks], context_lens [B]")
+    st = load().pa_decode_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        B, block_tables.shape[1], nb, hq, hkv, d, bs, float(scale), dtype_code(q.dtype),
+        dtype_code(k_cache.dtype), float(kv_scale), int(partition_size), _stream(q))
+    _check("pa_decode_noalloc", st)
 
 
 def pa_gather_kv(k_out, v_out, k_cache, v_cache, block_tables, context_lens, cu_seqlens):

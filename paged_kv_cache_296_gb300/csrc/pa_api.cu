@@ -108,6 +108,13 @@ pa_status check_pool(int num_blocks, int num_kv_heads) {
 
 }  // namespace
 
+namespace pa {
+int record_error_code(int status, const char* msg) {
+  g_last_error = msg;
+  return status;
+}
+}  // namespace pa
+
 extern "C" {
 
 const char* pa_last_error(void) { return g_last_error.c_str(); }

@@ -55,6 +55,10 @@ cudaError_t launch_check_tables(const int32_t* block_tables, const int32_t* cont
                                 int max_blocks_per_seq, int num_blocks, int block_size,
                                 int32_t* counts_dev, cudaStream_t stream);
 
+// Records `msg` for pa_last_error() on the calling thread and returns `status`.
+// (int-typed so this header needs no pa.h; the value is a pa_status.)
+int record_error_code(int status, const char* msg);
+
 // Address of this library's device status word on the current device.
 cudaError_t device_status_ptr(unsigned** ptr);
 
