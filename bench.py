@@ -1,8 +1,11 @@
 """Benchmark of the paged-KV-cache decode hot path on one GB300 (or N replicas).
 
-One step = pa_reshape_and_cache of the batch's new tokens + pa_decode over
-every sequence (attention kernel and, for split-KV, the merge kernel), on a
-seeded synthetic batch whose KV cache is already resident in HBM.
+One step = the write of each sequence's new token into the paged pool plus
+decode attention over every sequence, on a seeded synthetic batch whose KV
+cache is already resident in HBM.  By default the step is pa_decode_append
+(write, attention and split-KV merge in one launch); --path separate times
+pa_reshape_and_cache followed by pa_decode.  The other path is timed after
+the headline loop and reported under "other_path".
 
 Prints ONE JSON line (rank 0).  ``value`` is attended-KV GB/s of the whole job
 (sum over ranks of sum_i L_i*Hkv*D*2*elt bytes per step / step time, max
@@ -97,10 +100,11 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config_id):
-    """DRAM bytes per decode launch from the committed ncu summary, if it still
-    describes the current kernel source (else None)."""
-    path = os.path.join(PROFILE_DIR, f"paged_decode_kernel_config{config_id}.md")
+def profiled_traffic(config_id, step_path):
+    """DRAM bytes per decode call from the committed ncu summary of this step
+    path, if it still describes the current kernel source (else None)."""
+    name = "paged_decode_append" if step_path == "append" else "paged_decode_kernel"
+    path = os.path.join(PROFILE_DIR, f"{name}_config{config_id}.md")
     try:
         text = open(path, encoding="utf-8").read()
     except OSError:
@@ -250,42 +254,66 @@ def run_ours(args, world, rank, local):
     spec = wl.SPECS[args.config]
     W = wl.make_workload(spec, args.config + 1000 * rank, device=str(device))
     S = DecodeStep(W, device=device, partition_size=args.partition_size)
-    total_bytes, kv_bytes = step_bytes(W)
+    total_bytes, kv_bytes, new_bytes = step_bytes(W)
     stream = torch.cuda.current_stream(device)
+    step_fn = S.append if args.path == "append" else S.step
 
     for _ in range(args.warmup):
-        S.step()
+        step_fn()
     torch.cuda.synchronize(device)
     pa.pa_device_status(clear=True)
+
+    def timed(path, n, sampler=None):
+        """Time n steps of `path` on the stream: (ms per step, [ms per decode call], [ms per write])."""
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(device)
+        t0 = time.time()
+        start.record(stream)
+        if path == "append":
+            for i in range(n):
+                ev[i][1].record(stream)
+                S.append()
+                ev[i][2].record(stream)
+        else:
+            for i in range(n):
+                ev[i][0].record(stream)
+                S.write()
+                ev[i][1].record(stream)
+                S.decode()
+                ev[i][2].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+        t1 = time.time()
+        total = start.elapsed_time(end)
+        dec = [e[1].elapsed_time(e[2]) for e in ev]
+        wr = [e[0].elapsed_time(e[1]) for e in ev] if path != "append" else [0.0]
+        return total / n, dec, wr, t0, t1
 
     sampler = ClockSampler(device.index)
     sampler.start()
     time.sleep(0.3)  # let the sampler start before the timed region
     n = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize(device)
-    t_wall0 = time.time()
-    start.record(stream)
-    for i in range(n):
-        ev[i][0].record(stream)
-        S.write()
-        ev[i][1].record(stream)
-        S.decode()
-        ev[i][2].record(stream)
-    end.record(stream)
-    torch.cuda.synchronize(device)
-    barrier(world)
-    t_wall1 = time.time()
+    ms_local, decode_ms, write_ms, t_wall0, t_wall1 = timed(args.path, n)
     sampler.stop()
-    total_ms = start.elapsed_time(end)
-    decode_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    write_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    ms_step = max_over_ranks(total_ms / n, world, device)
+    ms_step = max_over_ranks(ms_local, world, device)
     status = pa.pa_device_status(clear=True)
     if status != 0:
         raise RuntimeError(f"device status {status:#x}: a kernel gave up waiting")
+
+    # The other way to run the same step, for comparison (not the headline).
+    alt = None
+    if not args.no_alt:
+        other = "separate" if args.path == "append" else "append"
+        fn = S.append if other == "append" else S.step
+        for _ in range(args.warmup):
+            fn()
+        a_ms, a_dec, a_wr, _, _ = timed(other, n)
+        alt = {"path": other, "us_per_step": round(max_over_ranks(a_ms, world, device) * 1e3, 2),
+               "us_decode_call": round(statistics.mean(a_dec) * 1e3, 2),
+               "us_write_call": round(statistics.mean(a_wr) * 1e3, 2)}
 
     # ---- e2e through the public API with host buffers
     e2e = None
@@ -299,7 +327,7 @@ def run_ours(args, world, rank, local):
         def e2e_step():
             for k, t in host.items():
                 getattr(S, k).copy_(t, non_blocking=True)
-            S.step()
+            step_fn()
             out_host.copy_(S.out, non_blocking=True)
 
         for _ in range(args.warmup):
@@ -330,9 +358,15 @@ def run_ours(args, world, rank, local):
     value = all_kv / (ms_step * 1e-3) / 1e9
     dec_ms = statistics.mean(decode_ms)
     peak, peak_kind = hbm_peak()
-    achieved = total_bytes / (dec_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(args.config)
-    launches = S.launches_per_step * n
+    if args.path == "append":
+        call_bytes = total_bytes + new_bytes
+        kernel = "pa_decode_append (token write + attention, then the split-KV merge)"
+    else:
+        call_bytes = total_bytes
+        kernel = "pa_decode (attention + split-KV merge)"
+    achieved = call_bytes / (dec_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(args.config, args.path)
+    launches = S.launches_per_step(args.path) * n
     uniq = unique_kv_bytes(W) if spec.lens[0] == "shared_prefix" else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -346,14 +380,16 @@ def run_ours(args, world, rank, local):
         "dtype": spec.kv_dtype if spec.kv_dtype == spec.q_dtype else f"{spec.q_dtype}+{spec.kv_dtype}",
         "data": "synthetic (seeded N(0,1) K/V/q; no model weights)",
         "config": config_block(spec, W, {
+            "step": args.path,
             "partition_tokens": S.partition_tokens,
             "l2": f"inputs larger than L2: {kv_bytes / 1e9:.3f} GB of KV read per step, no flush",
             "parallelism": f"replicas{world}" if world > 1 else "single GPU"}),
-        "roofline": {"bound": "hbm", "kernel": "pa_decode (attention kernel + split-KV merge)",
+        "roofline": {"bound": "hbm", "kernel": kernel,
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
-                     "algorithmic_bytes_per_launch": total_bytes,
+                     "algorithmic_bytes_per_launch": call_bytes,
                      "traffic": traffic},
+        "other_path": alt,
         "gpu_launches": launches,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -408,6 +444,10 @@ def main(argv=None):
     p.add_argument("--config", type=int, default=2, choices=sorted(wl.SPECS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--partition-size", type=int, default=0)
+    p.add_argument("--path", default="append", choices=["append", "separate"],
+                   help="append: pa_decode_append (one launch per step); separate: "
+                        "pa_reshape_and_cache then pa_decode")
+    p.add_argument("--no-alt", action="store_true", help="skip timing the other path")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--ref-seconds", type=float, default=60.0)
     p.add_argument("--no-e2e", action="store_true")

@@ -139,6 +139,36 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                     size_t workspace_bytes, void* stream);
 
 /*
+ * pa_decode_append -- one decode step in one launch: append each sequence's
+ * new token to the pool, then attend through the block table.
+ *
+ * The same result as pa_reshape_and_cache over the step's tokens followed by
+ * pa_decode (bit for bit: the same writes and the same attention arithmetic),
+ * for the decode case of "vLLM 部署深度指南", section 代码层面理解, where
+ * append_kv adds one token per running sequence and attention follows.
+ * Token i belongs to sequence i and is its last cached token (position
+ * context_lens[i] - 1, already counted in context_lens[i]); slot_mapping[i] is
+ * its slot (< 0: no write).  The CTA that attends over that position writes
+ * the token (head by head) before loading it.
+ *
+ * k_new, v_new  [num_seqs, num_kv_heads, head_size] of q_dtype; token i starts
+ *               at element i*src_token_stride (0 = contiguous); the stride in
+ *               bytes must be a multiple of 16.  A PA_E4M3 cache quantises them
+ *               with kv_scale exactly as pa_reshape_and_cache does.
+ * Every other argument is pa_decode's.  A slot that is not the one the block
+ * table gives position L - 1 leaves the result undefined (no access leaves
+ * the pool).
+ */
+pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                           const int64_t* slot_mapping, int64_t src_token_stride, void* k_cache,
+                           void* v_cache, const int32_t* block_tables,
+                           const int32_t* context_lens, int num_seqs, int max_blocks_per_seq,
+                           int num_blocks, int num_q_heads, int num_kv_heads, int head_size,
+                           int block_size, float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
+                           float kv_scale, int partition_size, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
  * pa_decode_noalloc -- pa_decode for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this call: it exists for callers with no

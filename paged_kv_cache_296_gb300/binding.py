@@ -26,6 +26,8 @@ SIGNATURES = {
     "pa_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I, _I, _I, _I, _I, _I, _F, _P]),
     "pa_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _F, _I,
                        _P, _SZ, _P]),
+    "pa_decode_append": (_I, [_P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                              _F, _I, _I, _F, _I, _P, _SZ, _P]),
     "pa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                                _F, _I, _P]),
     "pa_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
@@ -171,6 +173,36 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, kv_sc
         B, mb, nb, hq, hkv, d, bs, float(scale), dtype_code(q.dtype), dtype_code(k_cache.dtype),
         float(kv_scale), int(partition_size), _ptr(workspace), wbytes, _stream(q))
     _check("pa_decode", st)
+
+
+def pa_decode_append(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                     context_lens, scale, kv_scale=1.0, partition_size=0, workspace=None):
+    """Write each sequence's new token (``k_new``/``v_new`` ``[B, Hkv, D]``) and decode, in one launch."""
+    nb, bs, hkv, d = _cache_geometry(k_cache, v_cache)
+    B, hq, dq = q.shape
+    if dq != d or out.shape != q.shape or not q.is_contiguous() or not out.is_contiguous():
+        raise ValueError("q and out must be contiguous [B, Hq, D] tensors")
+    if k_new.shape != (B, hkv, d) or v_new.shape != k_new.shape or k_new.stride() != v_new.stride() \
+            or k_new.stride(1) != d or k_new.stride(2) != 1 or k_new.dtype != q.dtype \
+            or v_new.dtype != q.dtype:
+        raise ValueError("k_new and v_new must be [B, Hkv, D] of q's dtype with unit inner strides")
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_contiguous() \
+            or slot_mapping.shape != (B,):
+        raise ValueError("slot_mapping must be a contiguous int64 [B] tensor")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 \
+            or not block_tables.is_contiguous() or not context_lens.is_contiguous():
+        raise ValueError("block_tables and context_lens must be contiguous int32 tensors")
+    mb = block_tables.shape[1]
+    need = pa_decode_workspace_size(B, hq, d, mb, bs, partition_size)
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().pa_decode_append(
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), k_new.stride(0),
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), B, mb, nb, hq, hkv,
+        d, bs, float(scale), dtype_code(q.dtype), dtype_code(k_cache.dtype), float(kv_scale),
+        int(partition_size), _ptr(workspace), wbytes, _stream(q))
+    _check("pa_decode_append", st)
 
 
 #: Bytes of the library's fixed split-KV scratch used by pa_decode_noalloc.

@@ -106,6 +106,118 @@ pa_status check_pool(int num_blocks, int num_kv_heads) {
   return PA_OK;
 }
 
+// Shared by pa_decode and pa_decode_append (`fn` names the caller in messages;
+// `k_new` == NULL means no fused write).
+pa_status decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
+                      const void* v_cache, const int32_t* block_tables,
+                      const int32_t* context_lens, int num_seqs, int max_blocks_per_seq,
+                      int num_blocks, int num_q_heads, int num_kv_heads, int head_size,
+                      int block_size, float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
+                      float kv_scale, int partition_size, void* workspace,
+                      size_t workspace_bytes, void* stream, const void* k_new,
+                      const void* v_new, const int64_t* slot_mapping, int64_t src_token_stride) {
+  pa_status st;
+  if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs must be >= 0 (got %d)", num_seqs);
+  if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "num_seqs %d exceeds 65535", num_seqs);
+  if (max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be > 0 (got %d)", max_blocks_per_seq);
+  if ((st = check_block_size(block_size)) != PA_OK) return st;
+  if ((st = check_head_size(head_size)) != PA_OK) return st;
+  if ((st = check_pool(num_blocks, num_kv_heads)) != PA_OK) return st;
+  if (num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+                num_q_heads, num_kv_heads);
+  if (num_q_heads / num_kv_heads > kMaxGroup)
+    return fail(PA_ERR_UNSUPPORTED, "query heads per KV head %d exceeds %d",
+                num_q_heads / num_kv_heads, kMaxGroup);
+  if (num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads exceeds 65535");
+  if (q_dtype != PA_F16 && q_dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "q dtype must be PA_F16 or PA_BF16");
+  if (kv_dtype != q_dtype && kv_dtype != PA_E4M3)
+    return fail(PA_ERR_UNSUPPORTED, "cache dtype must equal the q dtype or be PA_E4M3");
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return fail(PA_ERR_INVALID_ARG, "scale must be finite");
+  if (kv_dtype == PA_E4M3 && (!(kv_scale > 0.f) || kv_scale == INFINITY))
+    return fail(PA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an E4M3 cache");
+  const int part = partition_tokens(max_blocks_per_seq, partition_size);
+  if (part <= 0)
+    return fail(PA_ERR_INVALID_ARG, "partition_size must be 0 or a positive multiple of 16 (got %d)",
+                partition_size);
+  const int np = num_partitions(max_blocks_per_seq, part);
+  if (np > 65535) return fail(PA_ERR_UNSUPPORTED, "too many partitions (%d)", np);
+  const WorkspaceLayout ws = workspace_layout(num_seqs, num_q_heads, head_size, np);
+  if (num_seqs == 0) return ok();
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return fail(PA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "out, q, k_cache and v_cache must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return fail(PA_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
+  const int64_t hkv_d = (int64_t)num_kv_heads * head_size;
+  const int64_t src_stride = src_token_stride == 0 ? hkv_d : src_token_stride;
+  if (k_new) {
+    if (!v_new || !slot_mapping) return fail(PA_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned16(k_new) || !aligned16(v_new))
+      return fail(PA_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(slot_mapping) & 7u)
+      return fail(PA_ERR_INVALID_ARG, "slot_mapping must be 8-byte aligned");
+    if (src_stride < hkv_d || (src_stride * 2) % 16 != 0)
+      return fail(PA_ERR_INVALID_ARG,
+                  "src_token_stride must be >= num_kv_heads*head_size and a multiple of 16 bytes");
+  }
+  if (ws.total > 0) {
+    if (!workspace || workspace_bytes < ws.total)
+      return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", ws.total,
+                  workspace ? workspace_bytes : (size_t)0);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+      return fail(PA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  }
+
+  pa::DecodeArgs a;
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.num_seqs = num_seqs;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_size = head_size;
+  a.q_dtype = (int)q_dtype;
+  a.kv_dtype = (int)kv_dtype;
+  a.scale = scale;
+  a.kv_scale = kv_dtype == PA_E4M3 ? kv_scale : 1.0f;
+  a.partition_tokens = part;
+  a.num_partitions = np;
+  auto* wsb = static_cast<uint8_t*>(workspace);
+  a.part_m = ws.total ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
+  a.part_l = ws.total ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
+  a.part_o = ws.total ? reinterpret_cast<float*>(wsb + ws.o_off) : nullptr;
+  a.append = k_new != nullptr;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.slot_mapping = slot_mapping;
+  a.src_stride_bytes = src_stride * 2;
+  cudaError_t e = pa::device_status_ptr(&a.status);
+  if (e != cudaSuccess) return cuda_fail(e, "status word");
+
+  const char* why = "launch failed";
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (kv_dtype == PA_E4M3) {
+    e = pa::launch_decode_e4m3(a, s, &why);
+  } else if (kv_dtype == PA_BF16) {
+    e = pa::launch_decode_bf16(a, s, &why);
+  } else {
+    e = pa::launch_decode_f16(a, s, &why);
+  }
+  if (e == cudaErrorInvalidValue) return fail(PA_ERR_CUDA, "%s: %s", fn, why);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+
 }  // namespace
 
 namespace pa {
@@ -207,89 +319,27 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                     int head_size, int block_size, float scale, pa_dtype q_dtype,
                     pa_dtype kv_dtype, float kv_scale, int partition_size, void* workspace,
                     size_t workspace_bytes, void* stream) {
-  pa_status st;
-  if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs must be >= 0 (got %d)", num_seqs);
-  if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "num_seqs %d exceeds 65535", num_seqs);
-  if (max_blocks_per_seq <= 0)
-    return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be > 0 (got %d)", max_blocks_per_seq);
-  if ((st = check_block_size(block_size)) != PA_OK) return st;
-  if ((st = check_head_size(head_size)) != PA_OK) return st;
-  if ((st = check_pool(num_blocks, num_kv_heads)) != PA_OK) return st;
-  if (num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
-    return fail(PA_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)",
-                num_q_heads, num_kv_heads);
-  if (num_q_heads / num_kv_heads > kMaxGroup)
-    return fail(PA_ERR_UNSUPPORTED, "query heads per KV head %d exceeds %d",
-                num_q_heads / num_kv_heads, kMaxGroup);
-  if (num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads exceeds 65535");
-  if (q_dtype != PA_F16 && q_dtype != PA_BF16)
-    return fail(PA_ERR_UNSUPPORTED, "q dtype must be PA_F16 or PA_BF16");
-  if (kv_dtype != q_dtype && kv_dtype != PA_E4M3)
-    return fail(PA_ERR_UNSUPPORTED, "cache dtype must equal the q dtype or be PA_E4M3");
-  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
-    return fail(PA_ERR_INVALID_ARG, "scale must be finite");
-  if (kv_dtype == PA_E4M3 && (!(kv_scale > 0.f) || kv_scale == INFINITY))
-    return fail(PA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an E4M3 cache");
-  const int part = partition_tokens(max_blocks_per_seq, partition_size);
-  if (part <= 0)
-    return fail(PA_ERR_INVALID_ARG, "partition_size must be 0 or a positive multiple of 16 (got %d)",
-                partition_size);
-  const int np = num_partitions(max_blocks_per_seq, part);
-  if (np > 65535) return fail(PA_ERR_UNSUPPORTED, "too many partitions (%d)", np);
-  const WorkspaceLayout ws = workspace_layout(num_seqs, num_q_heads, head_size, np);
-  if (num_seqs == 0) return ok();
-  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
-    return fail(PA_ERR_INVALID_ARG, "null pointer argument");
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
-    return fail(PA_ERR_INVALID_ARG, "out, q, k_cache and v_cache must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
-    return fail(PA_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
-  if (ws.total > 0) {
-    if (!workspace || workspace_bytes < ws.total)
-      return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", ws.total,
-                  workspace ? workspace_bytes : (size_t)0);
-    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
-      return fail(PA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-  }
+  return decode_impl("pa_decode", out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                     max_blocks_per_seq, num_blocks, num_q_heads, num_kv_heads, head_size,
+                     block_size, scale, q_dtype, kv_dtype, kv_scale, partition_size, workspace,
+                     workspace_bytes, stream, nullptr, nullptr, nullptr, 0);
+}
 
-  pa::DecodeArgs a;
-  a.out = out;
-  a.q = q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.block_tables = block_tables;
-  a.context_lens = context_lens;
-  a.num_seqs = num_seqs;
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.num_blocks = num_blocks;
-  a.num_q_heads = num_q_heads;
-  a.num_kv_heads = num_kv_heads;
-  a.head_size = head_size;
-  a.q_dtype = (int)q_dtype;
-  a.kv_dtype = (int)kv_dtype;
-  a.scale = scale;
-  a.kv_scale = kv_dtype == PA_E4M3 ? kv_scale : 1.0f;
-  a.partition_tokens = part;
-  a.num_partitions = np;
-  auto* wsb = static_cast<uint8_t*>(workspace);
-  a.part_m = ws.total ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
-  a.part_l = ws.total ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
-  a.part_o = ws.total ? reinterpret_cast<float*>(wsb + ws.o_off) : nullptr;
-  cudaError_t e = pa::device_status_ptr(&a.status);
-  if (e != cudaSuccess) return cuda_fail(e, "pa_decode status word");
-
-  const char* why = "launch failed";
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (kv_dtype == PA_E4M3) {
-    e = pa::launch_decode_e4m3(a, s, &why);
-  } else if (kv_dtype == PA_BF16) {
-    e = pa::launch_decode_bf16(a, s, &why);
-  } else {
-    e = pa::launch_decode_f16(a, s, &why);
-  }
-  if (e == cudaErrorInvalidValue) return fail(PA_ERR_CUDA, "pa_decode: %s", why);
-  if (e != cudaSuccess) return cuda_fail(e, "pa_decode launch");
-  return ok();
+pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                           const int64_t* slot_mapping, int64_t src_token_stride, void* k_cache,
+                           void* v_cache, const int32_t* block_tables,
+                           const int32_t* context_lens, int num_seqs, int max_blocks_per_seq,
+                           int num_blocks, int num_q_heads, int num_kv_heads, int head_size,
+                           int block_size, float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
+                           float kv_scale, int partition_size, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (num_seqs > 0 && (!k_new || !v_new || !slot_mapping))
+    return fail(PA_ERR_INVALID_ARG, "pa_decode_append: k_new, v_new and slot_mapping are required");
+  return decode_impl("pa_decode_append", out, q, k_cache, v_cache, block_tables, context_lens,
+                     num_seqs, max_blocks_per_seq, num_blocks, num_q_heads, num_kv_heads,
+                     head_size, block_size, scale, q_dtype, kv_dtype, kv_scale, partition_size,
+                     workspace, workspace_bytes, stream, k_new, v_new, slot_mapping,
+                     src_token_stride);
 }
 
 pa_status pa_gather_kv(void* k_out, void* v_out, const void* k_cache, const void* v_cache,

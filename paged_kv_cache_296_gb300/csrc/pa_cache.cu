@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include "pa_internal.h"
+#include "pa_ptx.cuh"
 
 namespace pa {
 
@@ -116,12 +117,6 @@ namespace {
 
 constexpr int kSrcF16 = 0, kSrcBf16 = 1, kSrcF32 = 3;
 
-__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
-  // cvt packs its first source into the upper byte: pass (hi, lo).
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
 
 template <int SRC>
 __device__ __forceinline__ void load8(const uint8_t* p, float (&x)[8]) {
@@ -158,6 +153,9 @@ __global__ void __launch_bounds__(kWriteThreads)
                              uint8_t* __restrict__ kc, uint8_t* __restrict__ vc,
                              const int64_t* __restrict__ slots, int64_t src_stride_bytes,
                              int64_t max_slot, int hkv_d, float kv_scale) {
+  // The decode kernel that follows may begin launching now; it waits for this
+  // grid to complete before it reads the pool.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t n = blockIdx.x;
   const int64_t s = slots[n];
   if (s < 0 || s >= max_slot) return;  // padding, or a slot past the pool

@@ -56,7 +56,16 @@ struct DecodeParams {
   int num_partitions;           // P = partitions of the longest possible sequence
   float scale_log2;             // scale * log2(e) (* kv_scale for E4M3)
   float out_scale;              // kv_scale for E4M3, else 1
+  float kv_scale;               // E4M3 write scale (fused write only)
+  // Fused write of each sequence's new token (the last one, position L - 1).
+  const uint8_t* k_new;         // [B, Hkv, D] of the q dtype, token stride src_stride_bytes
+  const uint8_t* v_new;
+  const int64_t* slot_mapping;  // [B]
+  int64_t src_stride_bytes;
+  uint8_t* k_cache;             // writable pool views
+  uint8_t* v_cache;
 };
+
 
 template <int D, int KV>
 struct DecodeCfg {
@@ -116,7 +125,7 @@ __device__ __forceinline__ uint32_t token_mask(int tok, int valid) {
   return (tok < valid ? 0x0000FFFFu : 0u) | (tok + 1 < valid ? 0xFFFF0000u : 0u);
 }
 
-template <int D, int KV, int QT>
+template <int D, int KV, int QT, bool kAppend>
 __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
@@ -167,6 +176,66 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
     if (lane == 0) {
       tma_prefetch_desc(&tmap_k);
       tma_prefetch_desc(&tmap_v);
+    }
+    // The pool may have just been written by the preceding kernel (the step's
+    // reshape_and_cache): wait for it before the first access to it.  Nothing
+    // read before this point (q, tables, lengths) is written there.
+    griddep_wait();
+    if constexpr (kAppend) {
+      // append_kv for this sequence's new token, head kvh: the CTA holding the
+      // partition with position L - 1 writes it, then makes the write visible
+      // to its own TMA loads (generic -> async proxy) before issuing them.
+      if (L > 0 && part == nparts_seq - 1) {
+        const int64_t slot = p.slot_mapping[seq];
+        if (slot >= 0 && slot < (int64_t)p.num_blocks * 16) {
+          constexpr int kSrcElt = 2;  // the new token comes in the q dtype
+          const size_t src = (size_t)seq * p.src_stride_bytes + (size_t)kvh * D * kSrcElt;
+          const size_t dst = (size_t)slot * (2ull * p.num_kv_heads * C::kRowBytes) +
+                             (size_t)kvh * C::kRowBytes;
+          if constexpr (!kFp8) {
+            constexpr int kVec = D * 2 / 16;  // 16-byte vectors per row
+            if (lane < 2 * kVec) {
+              const bool isv = lane >= kVec;
+              const int j = isv ? lane - kVec : lane;
+              const uint4 x = reinterpret_cast<const uint4*>((isv ? p.v_new : p.k_new) + src)[j];
+              reinterpret_cast<uint4*>((isv ? p.v_cache : p.k_cache) + dst)[j] = x;
+            }
+          } else {
+            constexpr int kGrp = D / 8;  // 8 elements -> 8 bytes per lane
+            if (lane < 2 * kGrp) {
+              const bool isv = lane >= kGrp;
+              const int j = isv ? lane - kGrp : lane;
+              const uint4 u = reinterpret_cast<const uint4*>((isv ? p.v_new : p.k_new) + src)[j];
+              const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+              float x[8];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                if constexpr (QT == kKvF16) {
+                  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+                  x[2 * i] = f.x;
+                  x[2 * i + 1] = f.y;
+                } else {
+                  x[2 * i] = __uint_as_float(w[i] << 16);
+                  x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                }
+              }
+              uint32_t q8[2];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint16_t a = f32x2_to_e4m3x2(__fdiv_rn(x[4 * h], p.kv_scale),
+                                                   __fdiv_rn(x[4 * h + 1], p.kv_scale));
+                const uint16_t b = f32x2_to_e4m3x2(__fdiv_rn(x[4 * h + 2], p.kv_scale),
+                                                   __fdiv_rn(x[4 * h + 3], p.kv_scale));
+                q8[h] = (uint32_t)a | ((uint32_t)b << 16);
+              }
+              reinterpret_cast<uint2*>((isv ? p.v_cache : p.k_cache) + dst)[j] =
+                  make_uint2(q8[0], q8[1]);
+            }
+          }
+          fence_proxy_async_global();
+        }
+      }
+      __syncwarp();
     }
     const int32_t* tbl =
         p.block_tables + (size_t)seq * p.max_blocks_per_seq + (size_t)part * p.partition_blocks;
@@ -277,8 +346,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
       }
 
       // ---- online softmax on the fragment: c0/c1 token g, c2/c3 token g+8
-      float s0 = sacc[0] * p.scale_log2, s1 = sacc[1] * p.scale_log2;
-      float s2 = sacc[2] * p.scale_log2, s3 = sacc[3] * p.scale_log2;
+      // Every rounding step below is spelled out (_rn intrinsics), so no
+      // instantiation of this kernel contracts them into FMAs differently:
+      // all variants produce the same bits.
+      float s0 = __fmul_rn(sacc[0], p.scale_log2), s1 = __fmul_rn(sacc[1], p.scale_log2);
+      float s2 = __fmul_rn(sacc[2], p.scale_log2), s3 = __fmul_rn(sacc[3], p.scale_log2);
       if (valid < 16) {
         if (g >= valid) s0 = s1 = -INFINITY;
         if (g + 8 >= valid) s2 = s3 = -INFINITY;
@@ -290,11 +362,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
         bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
       }
       const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-      const float al0 = ex2_approx(m0 - mn0), al1 = ex2_approx(m1 - mn1);
+      const float al0 = ex2_approx(__fsub_rn(m0, mn0)), al1 = ex2_approx(__fsub_rn(m1, mn1));
       m0 = mn0;
       m1 = mn1;
-      const float p0 = ex2_approx(s0 - mn0), p1 = ex2_approx(s1 - mn1);
-      const float p2 = ex2_approx(s2 - mn0), p3 = ex2_approx(s3 - mn1);
+      const float p0 = ex2_approx(__fsub_rn(s0, mn0)), p1 = ex2_approx(__fsub_rn(s1, mn1));
+      const float p2 = ex2_approx(__fsub_rn(s2, mn0)), p3 = ex2_approx(__fsub_rn(s3, mn1));
       uint32_t P01, P23;
       float r0, r1, r2, r3;  // the rounded probabilities the MMA will use
       if constexpr (kBf16Mma) {
@@ -309,12 +381,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
         const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&P23));
         r0 = f01.x; r1 = f01.y; r2 = f23.x; r3 = f23.y;
       }
-      l0 = l0 * al0 + (r0 + r2);
-      l1 = l1 * al1 + (r1 + r3);
+      l0 = __fmaf_rn(l0, al0, __fadd_rn(r0, r2));
+      l1 = __fmaf_rn(l1, al1, __fadd_rn(r1, r3));
       if (__any_sync(0xffffffffu, (al0 != 1.f) || (al1 != 1.f))) {
 #pragma unroll
         for (int i = 0; i < C::kMTiles; ++i) {
-          o[i][0] *= al0; o[i][1] *= al1; o[i][2] *= al0; o[i][3] *= al1;
+          o[i][0] = __fmul_rn(o[i][0], al0); o[i][1] = __fmul_rn(o[i][1], al1);
+          o[i][2] = __fmul_rn(o[i][2], al0); o[i][3] = __fmul_rn(o[i][3], al1);
         }
       }
       // P^T as the B operand: k = tokens (2t, 2t+1 | 2t+8, 2t+9), n = head g.
@@ -379,6 +452,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
           mma_f16(o[mt], a, pb0, pb1);
         }
       }
+      // Release the stage: this warp's reads of it (generic proxy) are ordered
+      // before the TMA refill (async proxy) by the proxy fence, then the warp's
+      // lanes by __syncwarp, then the producer by the mbarrier.
+      fence_proxy_async_shared();
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
@@ -392,6 +469,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
 
   // ---------------------------------------------------------------- merge warps
   __syncthreads();  // the ring is idle: reuse it for the per-warp states
+  // All loads are done: the split-KV merge kernel may start launching; it
+  // waits for this grid to finish before reading the partials.
+  griddep_launch_dependents();
   float* red_o = reinterpret_cast<float*>(smem);                       // [4][8][D+4]
   float* red_m = red_o + C::kConsumerWarps * 8 * C::kRedStride;          // [4][8]
   float* red_l = red_m + C::kConsumerWarps * 8;                          // [4][8]
@@ -432,14 +512,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < C::kConsumerWarps; ++w) {
-        const float wt = ex2_approx(red_m[w * 8 + h] - M);
-        num += wt * red_o[(w * 8 + h) * C::kRedStride + d];
-        den += wt * red_l[w * 8 + h];
+        const float wt = ex2_approx(__fsub_rn(red_m[w * 8 + h], M));
+        num = __fmaf_rn(wt, red_o[(w * 8 + h) * C::kRedStride + d], num);
+        den = __fmaf_rn(wt, red_l[w * 8 + h], den);
       }
     }
     const int qh = kvh * p.group + h;
     if (direct) {
-      const float v = (den > 0.f) ? num / den * p.out_scale : 0.f;
+      const float v = (den > 0.f) ? __fmul_rn(__fdiv_rn(num, den), p.out_scale) : 0.f;
       store_out<QT>(p.out, ((size_t)seq * p.num_q_heads + qh) * D + d, v);
     } else {
       const size_t pi = ((size_t)seq * p.num_q_heads + qh) * p.num_partitions + part;
@@ -452,57 +532,81 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
   }
 }
 
-// Log-sum-exp merge of split-KV partials: one warp per (sequence, query head).
+// Log-sum-exp merge of split-KV partials: one CTA of kMergeThreads per
+// (sequence, query head).  The threads form kMergeThreads / D groups; group r
+// takes partitions r, r + groups, ... and thread d of a group accumulates
+// head_size element d, so every partial's O row is read once, coalesced, with
+// several independent loads in flight per thread.  The groups' sums are added
+// in a fixed order, so the result does not depend on timing.
+constexpr int kMergeThreads = 256;
+
 template <int D, int QT>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kMergeThreads)
     paged_decode_merge_kernel(const DecodeParams p) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int idx = blockIdx.x * 4 + warp;
-  if (idx >= p.num_seqs * p.num_q_heads) return;
+  constexpr int kGroups = kMergeThreads / D;
+  __shared__ float red_acc[kGroups][D];
+  __shared__ float red_den[kGroups];
+  __shared__ float red_max[kMergeThreads / 32];
+
+  const int idx = blockIdx.x;  // sequence * num_q_heads + query head
   const int seq = idx / p.num_q_heads;
   const int L = p.context_lens[seq];
   const int part_tokens = p.partition_blocks * 16;
   const int np = (L + part_tokens - 1) / part_tokens;
   if (np <= 1) return;  // written directly by the attention kernel
   const size_t base = (size_t)idx * p.num_partitions;
+  const int tid = threadIdx.x;
+  griddep_wait();  // the partials come from the attention kernel just before
 
   float M = -INFINITY;
-  for (int i = lane; i < np; i += 32) M = fmaxf(M, p.part_m[base + i]);
+  for (int i = tid; i < np; i += kMergeThreads) M = fmaxf(M, p.part_m[base + i]);
 #pragma unroll
   for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+  if ((tid & 31) == 0) red_max[tid >> 5] = M;
+  __syncthreads();
+  M = red_max[0];
+#pragma unroll
+  for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red_max[w]);
 
-  constexpr int kPer = D / 32;  // elements of head_size per lane
-  float acc[kPer];
+  const int r = tid / D;
+  const int d = tid - r * D;
+  float acc = 0.f, den = 0.f;
+  int i = r;
+  for (; i + 3 * kGroups < np; i += 4 * kGroups) {
+    float mv[4], lv[4], ov[4];
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-  float den = 0.f;
-  for (int b0 = 0; b0 < np; b0 += 32) {
-    const int i = b0 + lane;
-    float wt = 0.f, lv = 0.f;
-    if (i < np) {
-      wt = ex2_approx(p.part_m[base + i] - M);
-      lv = p.part_l[base + i];
+    for (int u = 0; u < 4; ++u) {
+      const size_t pi = base + i + u * kGroups;
+      mv[u] = p.part_m[pi];
+      lv[u] = p.part_l[pi];
+      ov[u] = p.part_o[pi * D + d];
     }
-    float dl = wt * lv;
 #pragma unroll
-    for (int x = 16; x > 0; x >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, x);
-    den += dl;
-    const int cnt = min(32, np - b0);
-    for (int j = 0; j < cnt; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, wt, j);
-      const float* src = p.part_o + (base + b0 + j) * D + lane * kPer;
-      if constexpr (kPer == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] += wj * v.x; acc[1] += wj * v.y; acc[2] += wj * v.z; acc[3] += wj * v.w;
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] += wj * v.x; acc[1] += wj * v.y;
-      }
+    for (int u = 0; u < 4; ++u) {
+      const float w = ex2_approx(__fsub_rn(mv[u], M));
+      den = __fmaf_rn(w, lv[u], den);
+      acc = __fmaf_rn(w, ov[u], acc);
     }
   }
-  const float inv = (den > 0.f) ? p.out_scale / den : 0.f;
+  for (; i < np; i += kGroups) {
+    const size_t pi = base + i;
+    const float w = ex2_approx(__fsub_rn(p.part_m[pi], M));
+    den = __fmaf_rn(w, p.part_l[pi], den);
+    acc = __fmaf_rn(w, p.part_o[pi * D + d], acc);
+  }
+  red_acc[r][d] = acc;
+  if (d == 0) red_den[r] = den;
+  __syncthreads();
+  if (r == 0) {
+    float a = red_acc[0][d], dn = red_den[0];
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) store_out<QT>(p.out, (size_t)idx * D + lane * kPer + e, acc[e] * inv);
+    for (int g = 1; g < kGroups; ++g) {
+      a = __fadd_rn(a, red_acc[g][d]);
+      dn = __fadd_rn(dn, red_den[g]);
+    }
+    const float v = (dn > 0.f) ? __fmul_rn(__fdiv_rn(a, dn), p.out_scale) : 0.f;
+    store_out<QT>(p.out, (size_t)idx * D + d, v);
+  }
 }
 
 }  // namespace pa

@@ -11,6 +11,47 @@
 
 namespace pa {
 
+template <int D, int KV, int QT, bool kAppend>
+cudaError_t launch_decode_kernel(const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const DecodeParams& p, const DecodeArgs& a, cudaStream_t stream) {
+  using C = DecodeCfg<D, KV>;
+  // Opt in to more than 48 KB of dynamic shared memory, once per device.
+  static std::atomic<unsigned long long> attr_done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(paged_decode_kernel<D, KV, QT, kAppend>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  // Both kernels are launched with programmatic stream serialisation: each may
+  // start while the kernel before it drains, and waits (griddepcontrol.wait)
+  // before touching anything that kernel writes.
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.num_kv_heads, (unsigned)a.num_partitions, (unsigned)a.num_seqs);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, KV, QT, kAppend>, tk, tv, p);
+  if (e != cudaSuccess) return e;
+  if (a.num_partitions > 1) {
+    cudaLaunchConfig_t mcfg = cfg;
+    mcfg.gridDim = dim3((unsigned)((long long)a.num_seqs * a.num_q_heads));
+    mcfg.blockDim = dim3(kMergeThreads);
+    mcfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&mcfg, paged_decode_merge_kernel<D, QT>, p);
+  }
+  return e;
+}
+
 template <int D, int KV, int QT>
 cudaError_t launch_decode_instance(const DecodeArgs& a, cudaStream_t stream, const char** why) {
   using C = DecodeCfg<D, KV>;
@@ -41,30 +82,15 @@ cudaError_t launch_decode_instance(const DecodeArgs& a, cudaStream_t stream, con
   const double kvs = (KV == kKvE4m3) ? (double)a.kv_scale : 1.0;
   p.scale_log2 = (float)((double)a.scale * log2e * kvs);
   p.out_scale = (float)kvs;
-
-  // Opt in to more than 48 KB of dynamic shared memory, once per device.
-  static std::atomic<unsigned long long> attr_done{0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(attr_done.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(paged_decode_kernel<D, KV, QT>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done.fetch_or(bit, std::memory_order_acq_rel);
-  }
-
-  const dim3 grid((unsigned)a.num_kv_heads, (unsigned)a.num_partitions, (unsigned)a.num_seqs);
-  paged_decode_kernel<D, KV, QT><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (a.num_partitions > 1) {
-    const long long warps = (long long)a.num_seqs * a.num_q_heads;
-    paged_decode_merge_kernel<D, QT><<<(unsigned)((warps + 3) / 4), 128, 0, stream>>>(p);
-    e = cudaGetLastError();
-  }
-  return e;
+  p.kv_scale = a.kv_scale;
+  p.k_new = static_cast<const uint8_t*>(a.k_new);
+  p.v_new = static_cast<const uint8_t*>(a.v_new);
+  p.slot_mapping = a.slot_mapping;
+  p.src_stride_bytes = a.src_stride_bytes;
+  p.k_cache = static_cast<uint8_t*>(const_cast<void*>(a.k_cache));
+  p.v_cache = static_cast<uint8_t*>(const_cast<void*>(a.v_cache));
+  if (a.append) return launch_decode_kernel<D, KV, QT, true>(tk, tv, p, a, stream);
+  return launch_decode_kernel<D, KV, QT, false>(tk, tv, p, a, stream);
 }
 
 }  // namespace pa

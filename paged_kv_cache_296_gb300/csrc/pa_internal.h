@@ -32,6 +32,12 @@ struct DecodeArgs {
   float* part_l;
   float* part_o;
   unsigned* status;
+  // pa_decode_append: the step's new token per sequence, written by the kernel.
+  bool append;
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slot_mapping;
+  int64_t src_stride_bytes;
 };
 
 // Per-dtype decode launchers (one translation unit each, compiled in parallel).

@@ -76,6 +76,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Block until every grid this one depends on (the preceding kernel on the
+// stream, when launched with programmatic stream serialisation) has finished
+// and its memory writes are visible.  A no-op for an ordinary launch.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next kernel on the stream start launching (it still waits in
+// griddep_wait() for this grid to finish before reading its results).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -99,6 +114,22 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
       "r"(c3)
       : "memory");
+}
+
+// Order this thread's earlier generic-proxy global writes before later
+// async-proxy (TMA) accesses; with a barrier after it, other threads' TMA
+// loads issued after the barrier observe the writes.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses (ld.shared,
+// ldmatrix) before later async-proxy (TMA) writes to the same bytes.  A
+// consumer must execute it before releasing a stage that TMA will refill: the
+// mbarrier hand-off alone orders the threads but not the two proxies, and
+// without it a refill can land while the stage is still being read.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- shared-memory fragments
@@ -164,6 +195,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
   uint32_t y;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(y) : "h"(x));
   return y;
+}
+
+// Two floats to two E4M3 bytes (lo -> low byte), round to nearest even,
+// saturating to +-448; cvt packs its first source into the upper byte.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

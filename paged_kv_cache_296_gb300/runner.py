@@ -56,12 +56,24 @@ class DecodeStep:
         self.kv_scale = W.kv_scale
         self.scale = W.scale
 
-    @property
-    def launches_per_step(self):
-        """Kernels one step enqueues: the write, the attention and (split-KV) the merge."""
-        lens = self.W.context_lens
-        split = bool((lens > self.partition_tokens).any())
-        return 2 + (1 if split else 0)
+    def launches_per_step(self, path="append"):
+        """Kernels one step enqueues.
+
+        "append": one (token write + attention), plus the merge kernel when a
+        sequence can span more than one partition.  "separate": the write
+        kernel, then the same.
+        """
+        max_tokens = self.W.max_blocks_per_seq * BLOCK_SIZE
+        n = 1 + (1 if max_tokens > self.partition_tokens else 0)
+        return n + (1 if path == "separate" else 0)
+
+    def append(self):
+        """The whole step in one call: pa_decode_append."""
+        pa.pa_decode_append(self.out, self.q, self.k_new, self.v_new, self.slot_mapping,
+                            self.k_cache, self.v_cache, self.block_tables, self.context_lens,
+                            self.scale, kv_scale=self.kv_scale,
+                            partition_size=self.partition_size, workspace=self.workspace)
+        return self.out
 
     def write(self):
         pa.pa_reshape_and_cache(self.k_new, self.v_new, self.k_cache, self.v_cache,
@@ -79,16 +91,19 @@ class DecodeStep:
 
 
 def step_bytes(W):
-    """Algorithmic bytes of one decode: attended K/V + q + out (and K/V alone).
+    """Algorithmic bytes of one step: (attended K/V + q + out, attended K/V, new-token bytes).
 
     Attended K/V counts every token of every sequence once per KV head:
-    ``sum_i L_i * Hkv * D * 2 * elt``.
+    ``sum_i L_i * Hkv * D * 2 * elt``.  The new-token bytes are the write's:
+    k_new/v_new read in the q dtype plus their cache rows written.
     """
     spec = W.spec
     elt = 1 if spec.kv_dtype == "e4m3" else 2
     kv = int(W.context_lens.to(torch.int64).sum()) * spec.num_kv_heads * spec.head_size * 2 * elt
     qo = 2 * W.q.numel() * W.q.element_size()
-    return kv + qo, kv
+    n_new = int((W.slot_mapping >= 0).sum())
+    new = n_new * spec.num_kv_heads * spec.head_size * 2 * (W.q.element_size() + elt)
+    return kv + qo, kv, new
 
 
 def unique_kv_bytes(W):

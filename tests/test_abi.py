@@ -99,7 +99,8 @@ def test_workspace_size(lib):
     # 128 blocks = 2048 tokens = 4 partitions of 512
     rows = 64 * 32 * 4
     al = lambda x: (x + 255) // 256 * 256
-    assert lib.pa_decode_workspace_size(64, 32, 128, 128, 16, 0) == 2 * al(rows * 4) + al(rows * 128 * 4)
+    assert lib.pa_decode_workspace_size(64, 32, 128, 128, 16, 0) == \
+        2 * al(rows * 4) + al(rows * 128 * 4)
     assert lib.pa_decode_workspace_size(64, 32, 128, 128, 16, 256) == \
         2 * al(rows * 2 * 4) + al(rows * 2 * 128 * 4)
     assert lib.pa_decode_workspace_size(64, 32, 128, 128, 15, 0) == 0      # invalid block size
@@ -161,3 +162,16 @@ def test_binding_fails_loudly_without_library(tmp_path):
             mod.load(str(tmp_path / "nope.so"))
     finally:
         mod._lib = saved
+
+
+def test_decode_append_requires_token_buffers(lib):
+    args = decode_args()
+    # pa_decode_append(out, q, k_new, v_new, slot_mapping, src_stride, k_cache, v_cache, ...)
+    a = [args[0], args[1], NULL, FAKE, FAKE, 0] + args[2:]
+    assert lib.pa_decode_append(*a) == 1
+    a = [args[0], args[1], FAKE, FAKE, FAKE, 100] + args[2:]     # stride < Hkv*D
+    assert lib.pa_decode_append(*a) == 1
+    a = [args[0], args[1], MISALIGNED, FAKE, FAKE, 0] + args[2:]
+    assert lib.pa_decode_append(*a) == 1
+    a = [args[0], args[1], FAKE, FAKE, ctypes.c_void_p(0x10004), 0] + args[2:]
+    assert lib.pa_decode_append(*a) == 1
