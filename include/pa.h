@@ -122,8 +122,8 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void
  *               ceil(L / 16) are never read.
  * context_lens  int32 [num_seqs], 0 <= L <= max_blocks_per_seq * 16.
  * num_blocks    number of blocks in the pool (bounds the loads).
- * partition_size  tokens per split-KV partition: 0 = library choice, else a
- *               multiple of 16.  Sequences longer than one partition are
+ * partition_size  tokens per split-KV partition: 0 = library choice (see
+ *               pa_decode_partition_size), else a multiple of 16.  Sequences longer than one partition are
  *               processed as partitions whose fp32 partial results are merged
  *               by log-sum-exp (a second kernel on the same stream).
  * workspace     device scratch of at least pa_decode_workspace_size(...) bytes
@@ -211,12 +211,16 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const
  * arguments (0 when no sequence can span more than one partition).  Host only;
  * returns 0 and sets pa_last_error() for invalid arguments.
  */
-size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_size,
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
                                 int max_blocks_per_seq, int block_size, int partition_size);
 
 /*
  * pa_decode_partition_size -- the partition size pa_decode uses when given
- * partition_size (0 = the library's choice).  Host only; -1 on invalid input.
+ * partition_size.  0 asks for the library's choice, made from the batch shape
+ * alone: no split when num_seqs*num_kv_heads >= 512 (partitions still capped
+ * at 8192 tokens), otherwise about 512/(num_seqs*num_kv_heads) partitions of
+ * the longest possible sequence, a power of two in [512, 8192] tokens.
+ * Host only; -1 on invalid input.
  */
 int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_blocks_per_seq,
                              int block_size, int partition_size);

@@ -30,7 +30,7 @@ SIGNATURES = {
                               _F, _I, _I, _F, _I, _P, _SZ, _P]),
     "pa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                                _F, _I, _P]),
-    "pa_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "pa_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "pa_decode_partition_size": (_I, [_I, _I, _I, _I, _I]),
     "pa_gather_kv": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
     "pa_check_tables": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P]),
@@ -128,9 +128,9 @@ def pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, kv_scale=1.0):
     _check("pa_reshape_and_cache", st)
 
 
-def pa_decode_workspace_size(num_seqs, num_q_heads, head_size, max_blocks_per_seq,
+def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size, max_blocks_per_seq,
                              block_size=16, partition_size=0):
-    return int(load().pa_decode_workspace_size(num_seqs, num_q_heads, head_size,
+    return int(load().pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size,
                                                max_blocks_per_seq, block_size, partition_size))
 
 
@@ -164,7 +164,7 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, kv_sc
     if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
         raise ValueError("block_tables must be [B, max_blocks], context_lens [B]")
     mb = block_tables.shape[1]
-    need = pa_decode_workspace_size(B, hq, d, mb, bs, partition_size)
+    need = pa_decode_workspace_size(B, hq, hkv, d, mb, bs, partition_size)
     if workspace is None:
         workspace = alloc_workspace(need, q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -193,7 +193,7 @@ def pa_decode_append(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block
             or not block_tables.is_contiguous() or not context_lens.is_contiguous():
         raise ValueError("block_tables and context_lens must be contiguous int32 tensors")
     mb = block_tables.shape[1]
-    need = pa_decode_workspace_size(B, hq, d, mb, bs, partition_size)
+    need = pa_decode_workspace_size(B, hq, hkv, d, mb, bs, partition_size)
     if workspace is None:
         workspace = alloc_workspace(need, q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()

@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdint>
+#include <algorithm>
 #include <string>
 
 #include <cuda_runtime.h>
@@ -18,7 +19,9 @@ namespace {
 thread_local std::string g_last_error;
 
 constexpr int kBlockSize = 16;
-constexpr int kDefaultPartitionTokens = 512;
+constexpr int kMinPartitionTokens = 512;
+constexpr int kMaxPartitionTokens = 8192;
+constexpr long long kTargetCtas = 512;
 constexpr int kMaxGroup = 8;
 
 pa_status fail(pa_status st, const char* fmt, ...) {
@@ -55,10 +58,31 @@ int elt_bytes(pa_dtype d) {
   return 0;
 }
 
-// Partition size actually used, or -1 when the request is invalid.
-int partition_tokens(int max_blocks_per_seq, int requested) {
+// Split-KV partition size (tokens) actually used, or -1 when the request is
+// invalid.  A request of 0 picks one from the batch shape alone (no device
+// query, so the host-side sizing calls agree with pa_decode everywhere):
+//   * with >= kTargetCtas (sequence, KV head) pairs there are enough CTAs
+//     already: no split, except that no partition exceeds kMaxPartitionTokens
+//     (bounds the slowest CTA);
+//   * otherwise split the longest possible sequence into about
+//     kTargetCtas / pairs partitions, as a power of two within
+//     [kMinPartitionTokens, kMaxPartitionTokens].
+// Measured on GB300 (512 to 32768-token partitions): fewer, longer partitions
+// win as long as about 2.5+ CTAs per SM remain; a lone fp8 CTA streams only
+// ~14 GB/s, so a handful of long sequences must still be split.
+int partition_tokens(int num_seqs, int num_kv_heads, int max_blocks_per_seq, int requested) {
   if (requested < 0 || requested % kBlockSize != 0) return -1;
-  return requested == 0 ? kDefaultPartitionTokens : requested;
+  if (requested > 0) return requested;
+  const long long max_tokens = (long long)max_blocks_per_seq * kBlockSize;
+  const long long pairs = std::max(1LL, (long long)num_seqs * std::max(1, num_kv_heads));
+  if (pairs >= kTargetCtas) {
+    return (int)std::max<long long>(kBlockSize, std::min<long long>(max_tokens, kMaxPartitionTokens));
+  }
+  const long long parts = (kTargetCtas + pairs - 1) / pairs;
+  const long long want = (max_tokens + parts - 1) / parts;
+  long long part = kMinPartitionTokens;
+  while (part < want && part < kMaxPartitionTokens) part *= 2;
+  return (int)part;
 }
 
 int num_partitions(int max_blocks_per_seq, int part_tokens) {
@@ -139,7 +163,7 @@ pa_status decode_impl(const char* fn, void* out, const void* q, const void* k_ca
     return fail(PA_ERR_INVALID_ARG, "scale must be finite");
   if (kv_dtype == PA_E4M3 && (!(kv_scale > 0.f) || kv_scale == INFINITY))
     return fail(PA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an E4M3 cache");
-  const int part = partition_tokens(max_blocks_per_seq, partition_size);
+  const int part = partition_tokens(num_seqs, num_kv_heads, max_blocks_per_seq, partition_size);
   if (part <= 0)
     return fail(PA_ERR_INVALID_ARG, "partition_size must be 0 or a positive multiple of 16 (got %d)",
                 partition_size);
@@ -289,14 +313,14 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void
   return ok();
 }
 
-size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_size,
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
                                 int max_blocks_per_seq, int block_size, int partition_size) {
-  if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || block_size != kBlockSize ||
-      (head_size != 64 && head_size != 128)) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 ||
+      block_size != kBlockSize || (head_size != 64 && head_size != 128)) {
     fail(PA_ERR_INVALID_ARG, "invalid arguments to pa_decode_workspace_size");
     return 0;
   }
-  const int part = partition_tokens(max_blocks_per_seq, partition_size);
+  const int part = partition_tokens(num_seqs, num_kv_heads, max_blocks_per_seq, partition_size);
   if (part <= 0) {
     fail(PA_ERR_INVALID_ARG, "partition_size must be 0 or a positive multiple of 16");
     return 0;
@@ -307,10 +331,8 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int head_size,
 
 int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_blocks_per_seq,
                              int block_size, int partition_size) {
-  (void)num_seqs;
-  (void)num_kv_heads;
   if (block_size != kBlockSize || max_blocks_per_seq <= 0) return -1;
-  return partition_tokens(max_blocks_per_seq, partition_size);
+  return partition_tokens(num_seqs, num_kv_heads, max_blocks_per_seq, partition_size);
 }
 
 pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,

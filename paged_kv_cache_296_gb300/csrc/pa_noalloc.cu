@@ -57,7 +57,7 @@ extern "C" pa_status pa_decode_noalloc(void* out, const void* q, const void* k_c
                                        int num_kv_heads, int head_size, int block_size,
                                        float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
                                        float kv_scale, int partition_size, void* stream) {
-  const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, head_size,
+  const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size,
                                                max_blocks_per_seq, block_size, partition_size);
   if (need > kScratchBytes) {
     return record_error(PA_ERR_WORKSPACE,

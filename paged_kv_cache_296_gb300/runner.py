@@ -51,8 +51,8 @@ class DecodeStep:
         self.partition_tokens = pa.pa_decode_partition_size(
             B, spec.num_kv_heads, W.max_blocks_per_seq, BLOCK_SIZE, partition_size)
         self.workspace = pa.alloc_workspace(
-            pa.pa_decode_workspace_size(B, hq, d, W.max_blocks_per_seq, BLOCK_SIZE,
-                                        partition_size), self.device)
+            pa.pa_decode_workspace_size(B, hq, spec.num_kv_heads, d, W.max_blocks_per_seq,
+                                        BLOCK_SIZE, partition_size), self.device)
         self.kv_scale = W.kv_scale
         self.scale = W.scale
 

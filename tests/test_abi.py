@@ -70,7 +70,7 @@ def decode_args(**over):
     (dict(kvd=pa.PA_E4M3, kvs=float("inf")), 1),
     (dict(scale=float("nan")), 1),
     (dict(part=24), 1),                  # not a multiple of 16
-    (dict(mb=100), 3),                   # 1600 tokens > one 512-token partition: needs workspace
+    (dict(mb=100, part=512), 3),         # 1600 tokens > one 512-token partition: needs workspace
     (dict(nb=0), 1),
     (dict(B=-1), 1),
     (dict(B=70000), 2),
@@ -82,7 +82,7 @@ def test_decode_rejects_bad_arguments(lib, over, status):
 
 
 def test_decode_workspace_must_be_aligned(lib):
-    need = lib.pa_decode_workspace_size(4, 8, 128, 100, 16, 0)
+    need = lib.pa_decode_workspace_size(4, 8, 2, 128, 100, 16, 0)
     st = lib.pa_decode(*decode_args(mb=100, ws=ctypes.c_void_p(0x10010), wsb=need))
     assert st == 1
 
@@ -93,18 +93,27 @@ def test_decode_zero_sequences_is_a_no_op(lib):
 
 
 def test_workspace_size(lib):
-    # one partition: nothing to merge, no workspace
-    assert lib.pa_decode_workspace_size(64, 32, 128, 32, 16, 0) == 0
-    assert lib.pa_decode_workspace_size(64, 32, 128, 32, 16, 512) == 0
-    # 128 blocks = 2048 tokens = 4 partitions of 512
-    rows = 64 * 32 * 4
     al = lambda x: (x + 255) // 256 * 256
-    assert lib.pa_decode_workspace_size(64, 32, 128, 128, 16, 0) == \
+    # 64 x 32 (sequence, KV head) pairs: enough CTAs, no split below 8192 tokens, no workspace
+    assert lib.pa_decode_workspace_size(64, 32, 32, 128, 128, 16, 0) == 0
+    assert pa.pa_decode_partition_size(64, 32, 128) == 2048
+    # 8 x 8 pairs, 2048 blocks (32768 tokens): 512/64 = 8 partitions of 4096 tokens
+    assert pa.pa_decode_partition_size(8, 8, 2048) == 4096
+    rows = 8 * 64 * 8
+    assert lib.pa_decode_workspace_size(8, 64, 8, 128, 2048, 16, 0) == \
         2 * al(rows * 4) + al(rows * 128 * 4)
-    assert lib.pa_decode_workspace_size(64, 32, 128, 128, 16, 256) == \
+    # explicit sizes: 128 blocks = 2048 tokens = 4 partitions of 512
+    rows = 64 * 32 * 4
+    assert lib.pa_decode_workspace_size(64, 32, 32, 128, 128, 16, 512) == \
+        2 * al(rows * 4) + al(rows * 128 * 4)
+    assert lib.pa_decode_workspace_size(64, 32, 32, 128, 128, 16, 256) == \
         2 * al(rows * 2 * 4) + al(rows * 2 * 128 * 4)
-    assert lib.pa_decode_workspace_size(64, 32, 128, 128, 15, 0) == 0      # invalid block size
-    assert pa.pa_decode_partition_size(64, 8, 128) == 512
+    assert lib.pa_decode_workspace_size(64, 32, 32, 128, 128, 15, 0) == 0   # invalid block size
+    # the library's choice: never below 512 tokens, powers of two, capped at 8192
+    assert pa.pa_decode_partition_size(4, 4, 2) == 512
+    assert pa.pa_decode_partition_size(1, 1, 100000) == 4096       # 1.6M tokens in ~512 parts
+    assert pa.pa_decode_partition_size(1, 1, 1000000) == 8192      # capped
+    assert pa.pa_decode_partition_size(1024, 8, 4096) == 8192     # 65536 tokens, many pairs
     assert pa.pa_decode_partition_size(64, 8, 128, partition_size=48) == 48
     assert pa.pa_decode_partition_size(64, 8, 128, partition_size=40) == -1
 

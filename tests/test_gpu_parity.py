@@ -315,8 +315,8 @@ def test_run_to_run_bitwise_deterministic(n):
 def test_deterministic_and_split_matches_unsplit():
     W = wl.make_workload(wl.SPECS[3], 3)
     pool = H.gpu_pool(W)
-    a = H.gpu_step(W, pool).cpu()
-    b = H.gpu_step(W, pool).cpu()
+    a = H.gpu_step(W, pool, partition_size=512).cpu()             # up to 8 partitions
+    b = H.gpu_step(W, pool, partition_size=512).cpu()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     whole = H.gpu_step(W, pool, partition_size=4096).cpu()      # one partition per sequence
     err = (a.float() - whole.float()).abs().max().item()

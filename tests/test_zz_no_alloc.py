@@ -29,17 +29,17 @@ def test_rejects_sizes_beyond_the_fixed_scratch():
     lib = pa.load()
     fake = ctypes.c_void_p(0x10000)
     # 4096 sequences x 64 heads x 64 partitions of 512 tokens: ~8.7 GB of partials.
-    need = lib.pa_decode_workspace_size(4096, 64, 128, 2048, 16, 0)
+    need = lib.pa_decode_workspace_size(4096, 64, 8, 128, 2048, 16, 512)
     assert need > pa.DECODE_NOALLOC_SCRATCH_BYTES
     st = lib.pa_decode_noalloc(fake, fake, fake, fake, fake, fake, 4096, 2048, 100000, 64, 8, 128,
-                               16, 0.088, pa.PA_BF16, pa.PA_E4M3, 0.01, 0, ctypes.c_void_p(0))
+                               16, 0.088, pa.PA_BF16, pa.PA_E4M3, 0.01, 512, ctypes.c_void_p(0))
     assert st == 3
     assert "scratch" in pa.pa_last_error()
 
 
-def _compare_once(W, atol):
+def _compare_once(W, atol, partition_size=0):
     """Run pa_decode (caller workspace) and pa_decode_noalloc on the same device state."""
-    S = DecodeStep(W, device="cuda")
+    S = DecodeStep(W, device="cuda", partition_size=partition_size)
     assert S.workspace is not None, "the batch must use split-KV scratch"
     S.write()
     S.decode()
@@ -65,5 +65,5 @@ def test_noalloc_matches_pa_decode_on_two_calls_in_a_row():
     # Call 2: fp16 MHA batch with a different partition count; it starts from
     # whatever call 1 left in the shared scratch.
     mha = wl.Spec("mha fp16", 16, 32, 32, 128, "f16", "f16", ("uniform", 128, 2048))
-    _compare_once(wl.make_workload(mha, 502, device="cuda"), H.ATOL["f16"])
+    _compare_once(wl.make_workload(mha, 502, device="cuda"), H.ATOL["f16"], partition_size=256)
     assert pa.pa_device_status(clear=True) == 0
