@@ -216,10 +216,13 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
 
 /*
  * pa_decode_partition_size -- the partition size pa_decode uses when given
- * partition_size.  0 asks for the library's choice, made from the batch shape
- * alone: no split when num_seqs*num_kv_heads >= 512 (partitions still capped
- * at 8192 tokens), otherwise about 512/(num_seqs*num_kv_heads) partitions of
- * the longest possible sequence, a power of two in [512, 8192] tokens.
+ * partition_size.  A positive request is used as given.  0 asks for the
+ * library's choice, made from the batch shape: with num_seqs*num_kv_heads >=
+ * 512 no split (partitions capped at 8192 tokens; a sequence no longer than
+ * 512 tokens is never split either); otherwise a balanced split, returned as
+ * 0: the decode kernel reads the context lengths and takes the smallest
+ * partition size (>= 512 tokens) whose partitions over all sequences and KV
+ * heads run in one wave of resident CTAs on this GPU.
  * Host only; -1 on invalid input.
  */
 int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_blocks_per_seq,

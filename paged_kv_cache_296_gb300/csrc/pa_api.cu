@@ -21,7 +21,7 @@ thread_local std::string g_last_error;
 constexpr int kBlockSize = 16;
 constexpr int kMinPartitionTokens = 512;
 constexpr int kMaxPartitionTokens = 8192;
-constexpr long long kTargetCtas = 512;
+constexpr long long kTargetPairs = 512;
 constexpr int kMaxGroup = 8;
 
 pa_status fail(pa_status st, const char* fmt, ...) {
@@ -58,53 +58,58 @@ int elt_bytes(pa_dtype d) {
   return 0;
 }
 
-// Split-KV partition size (tokens) actually used, or -1 when the request is
-// invalid.  A request of 0 picks one from the batch shape alone (no device
-// query, so the host-side sizing calls agree with pa_decode everywhere):
-//   * with >= kTargetCtas (sequence, KV head) pairs there are enough CTAs
+// Split-KV partition size (tokens), 0 for a balanced split, or -1 when the
+// request is invalid.  A request of 0 decides from the batch shape alone (no
+// device query, so the host-side sizing calls agree with pa_decode everywhere):
+//   * with >= kTargetPairs (sequence, KV head) pairs there are enough CTAs
 //     already: no split, except that no partition exceeds kMaxPartitionTokens
 //     (bounds the slowest CTA);
-//   * otherwise split the longest possible sequence into about
-//     kTargetCtas / pairs partitions, as a power of two within
-//     [kMinPartitionTokens, kMaxPartitionTokens].
-// Measured on GB300 (512 to 32768-token partitions): fewer, longer partitions
-// win as long as about 2.5+ CTAs per SM remain; a lone fp8 CTA streams only
-// ~14 GB/s, so a handful of long sequences must still be split.
+//   * otherwise a balanced split (returned as 0): the decode kernel reads the
+//     actual context lengths and picks the smallest partition size, at least
+//     kMinPartitionTokens, whose partitions over all sequences and KV heads
+//     fit in one wave of resident CTAs, so every SM streams from the start to
+//     the end and the longest CTA is as short as that allows.
+// Measured on GB300: a CTA streams about its ring (64 KB) per loaded memory
+// latency (~3.5 us), so a batch of a few long sequences must be split, and a
+// split that spills into a second wave leaves a long tail.
 int partition_tokens(int num_seqs, int num_kv_heads, int max_blocks_per_seq, int requested) {
   if (requested < 0 || requested % kBlockSize != 0) return -1;
   if (requested > 0) return requested;
   const long long max_tokens = (long long)max_blocks_per_seq * kBlockSize;
   const long long pairs = std::max(1LL, (long long)num_seqs * std::max(1, num_kv_heads));
-  if (pairs >= kTargetCtas) {
+  if (pairs >= kTargetPairs) {
     return (int)std::max<long long>(kBlockSize, std::min<long long>(max_tokens, kMaxPartitionTokens));
   }
-  const long long parts = (kTargetCtas + pairs - 1) / pairs;
-  const long long want = (max_tokens + parts - 1) / parts;
-  long long part = kMinPartitionTokens;
-  while (part < want && part < kMaxPartitionTokens) part *= 2;
-  return (int)part;
+  if (max_tokens <= kMinPartitionTokens) return (int)std::max<long long>(kBlockSize, max_tokens);
+  return 0;
 }
 
+// Partitions of the grid (per sequence and KV head) for a partition size from
+// partition_tokens(); for a balanced split, enough for its smallest size.
 int num_partitions(int max_blocks_per_seq, int part_tokens) {
   const long long max_tokens = (long long)max_blocks_per_seq * kBlockSize;
-  const long long p = (max_tokens + part_tokens - 1) / part_tokens;
+  const long long unit = part_tokens > 0 ? part_tokens : kMinPartitionTokens;
+  const long long p = (max_tokens + unit - 1) / unit;
   return (int)(p < 1 ? 1 : p);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Split-KV workspace: partial m, l, O per (sequence, query head, partition),
+// then 256 bytes where a balanced split records its partition size.
 struct WorkspaceLayout {
-  size_t m_off, l_off, o_off, total;
+  size_t m_off, l_off, o_off, plan_off, total;
 };
 
 WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_size, int nparts) {
-  WorkspaceLayout w{0, 0, 0, 0};
+  WorkspaceLayout w{0, 0, 0, 0, 0};
   if (nparts <= 1) return w;
   const size_t rows = (size_t)num_seqs * num_q_heads * nparts;
   w.m_off = 0;
   w.l_off = align256(rows * sizeof(float));
   w.o_off = w.l_off + align256(rows * sizeof(float));
-  w.total = w.o_off + align256(rows * head_size * sizeof(float));
+  w.plan_off = w.o_off + align256(rows * head_size * sizeof(float));
+  w.total = w.plan_off + 256;
   return w;
 }
 
@@ -164,7 +169,7 @@ pa_status decode_impl(const char* fn, void* out, const void* q, const void* k_ca
   if (kv_dtype == PA_E4M3 && (!(kv_scale > 0.f) || kv_scale == INFINITY))
     return fail(PA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an E4M3 cache");
   const int part = partition_tokens(num_seqs, num_kv_heads, max_blocks_per_seq, partition_size);
-  if (part <= 0)
+  if (part < 0)
     return fail(PA_ERR_INVALID_ARG, "partition_size must be 0 or a positive multiple of 16 (got %d)",
                 partition_size);
   const int np = num_partitions(max_blocks_per_seq, part);
@@ -215,11 +220,13 @@ pa_status decode_impl(const char* fn, void* out, const void* q, const void* k_ca
   a.scale = scale;
   a.kv_scale = kv_dtype == PA_E4M3 ? kv_scale : 1.0f;
   a.partition_tokens = part;
+  a.min_partition_tokens = (int)kMinPartitionTokens;
   a.num_partitions = np;
   auto* wsb = static_cast<uint8_t*>(workspace);
   a.part_m = ws.total ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
   a.part_l = ws.total ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
   a.part_o = ws.total ? reinterpret_cast<float*>(wsb + ws.o_off) : nullptr;
+  a.plan = ws.total ? reinterpret_cast<int*>(wsb + ws.plan_off) : nullptr;
   a.append = k_new != nullptr;
   a.k_new = k_new;
   a.v_new = v_new;
@@ -321,7 +328,7 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
     return 0;
   }
   const int part = partition_tokens(num_seqs, num_kv_heads, max_blocks_per_seq, partition_size);
-  if (part <= 0) {
+  if (part < 0) {
     fail(PA_ERR_INVALID_ARG, "partition_size must be 0 or a positive multiple of 16");
     return 0;
   }

@@ -52,7 +52,13 @@ struct DecodeParams {
   int num_q_heads;
   int num_kv_heads;
   int group;                    // G = Hq / Hkv, 1..8
-  int partition_blocks;         // partition size in 16-token blocks
+  int partition_blocks;         // partition size in 16-token blocks; 0 = balanced (below)
+  // Balanced split: the partition size is chosen in the kernel from the actual
+  // context lengths, as the smallest one (>= min_partition_blocks) whose
+  // partitions over all sequences and KV heads fit in `slots` resident CTAs.
+  int min_partition_blocks;
+  int slots;
+  int* plan;                    // balanced: the chosen size, for the merge kernel
   int num_partitions;           // P = partitions of the longest possible sequence
   float scale_log2;             // scale * log2(e) (* kv_scale for E4M3)
   float out_scale;              // kv_scale for E4M3, else 1
@@ -78,8 +84,10 @@ struct DecodeCfg {
   // kStages a multiple of 4, every stage has one consumer warp that waits on
   // its phases strictly in order, so a parity wait never runs two phases ahead
   // of its barrier (which would let it pass early).  Two or more stages per
-  // warp let the producer run ahead while a warp computes.
-  static constexpr int kStages = (kStageBytes >= 8192) ? 8 : 12;
+  // warp let the producer run ahead while a warp computes.  A CTA streams
+  // about (ring bytes) / (loaded memory latency, ~3.5 us on GB300), so the
+  // ring is 64 KB whatever the stage size.
+  static constexpr int kStages = (kStageBytes >= 8192) ? 8 : 16;
   static_assert(kStages % kConsumerWarps == 0 && kStages >= 2 * kConsumerWarps,
                 "each stage must belong to exactly one consumer warp");
   static constexpr int kSwizzle = (kRowBytes >= 128) ? 128 : 64;
@@ -125,6 +133,111 @@ __device__ __forceinline__ uint32_t token_mask(int tok, int valid) {
   return (tok < valid ? 0x0000FFFFu : 0u) | (tok + 1 < valid ? 0xFFFF0000u : 0u);
 }
 
+// Balanced split (partition_blocks == 0).  The grid is one dimension of
+// `slots` CTAs (one wave on this GPU, or the number of (sequence, KV head)
+// pairs if that is larger).  Every CTA computes the same plan from the actual
+// context lengths:
+//   pb = the smallest partition size in blocks, >= min_partition_blocks, with
+//        num_kv_heads * sum_i max(1, ceil(ceil(L_i / 16) / pb)) <= slots;
+// then takes work item blockIdx.x of the list ordered by (sequence, partition,
+// KV head) -- each sequence has at least one item, so empty sequences still
+// get their zero output.  Items past the list's end exit at once.
+struct BalancedItem {
+  int pb, seq, part, kvh;
+  bool valid;
+};
+
+template <int kThreads>
+__device__ __forceinline__ BalancedItem balanced_plan(const DecodeParams& p, int* red, int* pick) {
+  constexpr int kWarps = kThreads / 32;
+  constexpr int kPer = 4;  // sequences per thread, contiguous (the mode has < 512 sequences)
+  int nb[kPer];
+  int total = 0, maxnb = 0;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = threadIdx.x * kPer + k;
+    const int L = i < p.num_seqs ? p.context_lens[i] : -1;
+    nb[k] = L > 0 ? (L + 15) >> 4 : (L == 0 ? 0 : -1);  // -1: no such sequence
+    total += max(nb[k], 0);
+    maxnb = max(maxnb, nb[k]);
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  auto block_reduce = [&](int v, bool is_max) {
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) {
+      const int o = __shfl_xor_sync(0xffffffffu, v, x);
+      v = is_max ? max(v, o) : v + o;
+    }
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    int r = red[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) r = is_max ? max(r, red[w]) : r + red[w];
+    return r;
+  };
+  auto parts_of = [&](int pbv, int k) { return nb[k] < 0 ? 0 : max(1, (nb[k] + pbv - 1) / pbv); };
+  total = block_reduce(total, false);
+  maxnb = block_reduce(maxnb, true);
+  const long long want = ((long long)total * p.num_kv_heads + p.slots - 1) / p.slots;
+  int lo = max(p.min_partition_blocks, (int)(want < (1ll << 30) ? want : (1ll << 30)));
+  int hi = max(lo, maxnb);  // count(maxnb) = pairs <= slots
+  while (lo < hi) {
+    const int mid = lo + (hi - lo) / 2;
+    int c = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) c += parts_of(mid, k);
+    if ((long long)block_reduce(c, false) * p.num_kv_heads <= p.slots) {
+      hi = mid;
+    } else {
+      lo = mid + 1;
+    }
+  }
+  const int pb = lo;
+  // Exclusive prefix of partitions over sequences (threads hold consecutive
+  // sequences), then find the item's sequence and partition.
+  int mine = 0;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) mine += parts_of(pb, k);
+  int incl = mine;
+#pragma unroll
+  for (int x = 1; x < 32; x <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, x);
+    if (lane >= x) incl += o;
+  }
+  __syncthreads();
+  if (lane == 31) red[warp] = incl;
+  if (threadIdx.x == 0) pick[0] = -1;
+  __syncthreads();
+  int before = incl - mine;
+  for (int w = 0; w < warp; ++w) before += red[w];
+  int all = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) all += red[w];
+  const int q = blockIdx.x / p.num_kv_heads;  // the item's (sequence, partition) index
+  if (q >= before && q < before + mine) {
+    int acc = before;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int n = parts_of(pb, k);
+      if (q < acc + n) {
+        pick[0] = threadIdx.x * kPer + k;
+        pick[1] = q - acc;
+        break;
+      }
+      acc += n;
+    }
+  }
+  __syncthreads();
+  BalancedItem it;
+  it.pb = pb;
+  it.valid = q < all && pick[0] >= 0;
+  it.seq = it.valid ? pick[0] : 0;
+  it.part = it.valid ? pick[1] : 0;
+  it.kvh = blockIdx.x % p.num_kv_heads;
+  return it;
+}
+
 template <int D, int KV, int QT, bool kAppend>
 __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -140,11 +253,21 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kRingBytes);
   uint64_t* empty_bar = full_bar + C::kStages;
 
-  const int kvh = blockIdx.x;
-  const int part = blockIdx.y;
-  const int seq = blockIdx.z;
+  int kvh = blockIdx.x, part = blockIdx.y, seq = blockIdx.z;
+  int pb = p.partition_blocks;
+  if (pb == 0) {
+    __shared__ int red[C::kThreads / 32];
+    __shared__ int pick[2];
+    const BalancedItem item = balanced_plan<C::kThreads>(p, red, pick);
+    if (threadIdx.x == 0 && blockIdx.x == 0) *p.plan = item.pb;
+    if (!item.valid) return;
+    pb = item.pb;
+    kvh = item.kvh;
+    part = item.part;
+    seq = item.seq;
+  }
   const int L = p.context_lens[seq];
-  const int part_tokens = p.partition_blocks * 16;
+  const int part_tokens = pb * 16;
   const int tok0 = part * part_tokens;
   if (part > 0 && tok0 >= L) return;  // past the end of this sequence
   const int ntok = min(L - tok0, part_tokens);
@@ -238,7 +361,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
       __syncwarp();
     }
     const int32_t* tbl =
-        p.block_tables + (size_t)seq * p.max_blocks_per_seq + (size_t)part * p.partition_blocks;
+        p.block_tables + (size_t)seq * p.max_blocks_per_seq + (size_t)part * pb;
     const int oob_row = p.num_blocks * 16;  // first token row past the pool: TMA fills zeros
     bool ok = true;
     int issued = 0;
@@ -551,12 +674,14 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int idx = blockIdx.x;  // sequence * num_q_heads + query head
   const int seq = idx / p.num_q_heads;
   const int L = p.context_lens[seq];
-  const int part_tokens = p.partition_blocks * 16;
+  // A balanced split never cuts a sequence shorter than its minimum partition.
+  if (p.partition_blocks == 0 && L <= p.min_partition_blocks * 16) return;
+  griddep_wait();  // the partials (and a balanced split's size) come from the attention kernel
+  const int part_tokens = (p.partition_blocks ? p.partition_blocks : *p.plan) * 16;
   const int np = (L + part_tokens - 1) / part_tokens;
   if (np <= 1) return;  // written directly by the attention kernel
   const size_t base = (size_t)idx * p.num_partitions;
   const int tid = threadIdx.x;
-  griddep_wait();  // the partials come from the attention kernel just before
 
   float M = -INFINITY;
   for (int i = tid; i < np; i += kMergeThreads) M = fmaxf(M, p.part_m[base + i]);

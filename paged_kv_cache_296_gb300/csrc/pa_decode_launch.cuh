@@ -2,6 +2,7 @@
 // split-KV merge.  Included by the per-dtype translation units.
 #pragma once
 
+#include <algorithm>
 #include <atomic>
 
 #include <cuda_runtime.h>
@@ -27,6 +28,25 @@ cudaError_t launch_decode_kernel(const CUtensorMap& tk, const CUtensorMap& tv,
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit, std::memory_order_acq_rel);
   }
+  // Resident CTAs of this kernel on the whole GPU (the balanced split fits its
+  // partitions into one such wave), once per device.
+  if (p.partition_blocks == 0) {
+    static std::atomic<int> slots_cache[64];
+    int slots = slots_cache[dev & 63].load(std::memory_order_acquire);
+    if (slots == 0) {
+      int per_sm = 0, sms = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &per_sm, paged_decode_kernel<D, KV, QT, kAppend>, C::kThreads, C::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      slots = std::max(1, per_sm * sms);
+      slots_cache[dev & 63].store(slots, std::memory_order_release);
+    }
+    // One CTA per work item; at least one item per (sequence, KV head).
+    const_cast<DecodeParams&>(p).slots =
+        std::max(slots, a.num_seqs * a.num_kv_heads);
+  }
   // Both kernels are launched with programmatic stream serialisation: each may
   // start while the kernel before it drains, and waits (griddepcontrol.wait)
   // before touching anything that kernel writes.
@@ -34,7 +54,9 @@ cudaError_t launch_decode_kernel(const CUtensorMap& tk, const CUtensorMap& tv,
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.num_kv_heads, (unsigned)a.num_partitions, (unsigned)a.num_seqs);
+  cfg.gridDim = p.partition_blocks == 0
+                    ? dim3((unsigned)p.slots)
+                    : dim3((unsigned)a.num_kv_heads, (unsigned)a.num_partitions, (unsigned)a.num_seqs);
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
@@ -77,6 +99,9 @@ cudaError_t launch_decode_instance(const DecodeArgs& a, cudaStream_t stream, con
   p.num_kv_heads = a.num_kv_heads;
   p.group = a.num_q_heads / a.num_kv_heads;
   p.partition_blocks = a.partition_tokens / 16;
+  p.min_partition_blocks = a.min_partition_tokens / 16;
+  p.slots = 0;
+  p.plan = a.plan;
   p.num_partitions = a.num_partitions;
   const double log2e = 1.4426950408889634;
   const double kvs = (KV == kKvE4m3) ? (double)a.kv_scale : 1.0;

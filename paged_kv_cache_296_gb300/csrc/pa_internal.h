@@ -26,8 +26,10 @@ struct DecodeArgs {
   int kv_dtype;  // 0 f16, 1 bf16, 2 e4m3
   float scale;
   float kv_scale;
-  int partition_tokens;
-  int num_partitions;
+  int partition_tokens;      // 0: balanced split chosen in the kernel (>= min_partition_tokens)
+  int min_partition_tokens;
+  int num_partitions;        // grid partitions: an upper bound in the balanced mode
+  int* plan;                 // balanced mode: where the kernel records its choice
   float* part_m;
   float* part_l;
   float* part_o;

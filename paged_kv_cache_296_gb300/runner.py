@@ -64,7 +64,8 @@ class DecodeStep:
         kernel, then the same.
         """
         max_tokens = self.W.max_blocks_per_seq * BLOCK_SIZE
-        n = 1 + (1 if max_tokens > self.partition_tokens else 0)
+        split = self.partition_tokens == 0 or max_tokens > self.partition_tokens   # 0: balanced
+        n = 1 + (1 if split else 0)
         return n + (1 if path == "separate" else 0)
 
     def append(self):

@@ -94,26 +94,27 @@ def test_decode_zero_sequences_is_a_no_op(lib):
 
 def test_workspace_size(lib):
     al = lambda x: (x + 255) // 256 * 256
+    plan = 256                              # where a balanced split records its size
     # 64 x 32 (sequence, KV head) pairs: enough CTAs, no split below 8192 tokens, no workspace
     assert lib.pa_decode_workspace_size(64, 32, 32, 128, 128, 16, 0) == 0
     assert pa.pa_decode_partition_size(64, 32, 128) == 2048
-    # 8 x 8 pairs, 2048 blocks (32768 tokens): 512/64 = 8 partitions of 4096 tokens
-    assert pa.pa_decode_partition_size(8, 8, 2048) == 4096
-    rows = 8 * 64 * 8
+    # 8 x 8 pairs: a balanced split (0), chosen on the device; the workspace
+    # covers its smallest partition, 512 tokens: 32768 / 512 = 64 partitions
+    assert pa.pa_decode_partition_size(8, 8, 2048) == 0
+    rows = 8 * 64 * 64
     assert lib.pa_decode_workspace_size(8, 64, 8, 128, 2048, 16, 0) == \
-        2 * al(rows * 4) + al(rows * 128 * 4)
+        2 * al(rows * 4) + al(rows * 128 * 4) + plan
     # explicit sizes: 128 blocks = 2048 tokens = 4 partitions of 512
     rows = 64 * 32 * 4
     assert lib.pa_decode_workspace_size(64, 32, 32, 128, 128, 16, 512) == \
-        2 * al(rows * 4) + al(rows * 128 * 4)
+        2 * al(rows * 4) + al(rows * 128 * 4) + plan
     assert lib.pa_decode_workspace_size(64, 32, 32, 128, 128, 16, 256) == \
-        2 * al(rows * 2 * 4) + al(rows * 2 * 128 * 4)
+        2 * al(rows * 2 * 4) + al(rows * 2 * 128 * 4) + plan
     assert lib.pa_decode_workspace_size(64, 32, 32, 128, 128, 15, 0) == 0   # invalid block size
-    # the library's choice: never below 512 tokens, powers of two, capped at 8192
-    assert pa.pa_decode_partition_size(4, 4, 2) == 512
-    assert pa.pa_decode_partition_size(1, 1, 100000) == 4096       # 1.6M tokens in ~512 parts
-    assert pa.pa_decode_partition_size(1, 1, 1000000) == 8192      # capped
-    assert pa.pa_decode_partition_size(1024, 8, 4096) == 8192     # 65536 tokens, many pairs
+    # the library's choice
+    assert pa.pa_decode_partition_size(4, 4, 2) == 32            # short: one partition
+    assert pa.pa_decode_partition_size(1, 1, 100000) == 0        # few pairs: balanced split
+    assert pa.pa_decode_partition_size(1024, 8, 4096) == 8192    # many pairs, 65536 tokens: capped
     assert pa.pa_decode_partition_size(64, 8, 128, partition_size=48) == 48
     assert pa.pa_decode_partition_size(64, 8, 128, partition_size=40) == -1
 
