@@ -331,15 +331,15 @@ def run_ours(args, world, rank, local):
     # ---- e2e through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        host = {k: getattr(S, k).cpu().pin_memory() for k in
-                ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")}
+        # the step's inputs live packed in one pinned host buffer (q, new k/v,
+        # slot mapping, block tables, lengths): one host-to-device copy per step
+        host_in, dev_in = S.stage_inputs()
         out_host = torch.empty(S.out.shape, dtype=S.out.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        h2d = host_in.numel()
         d2h = out_host.numel() * out_host.element_size()
 
         def e2e_step():
-            for k, t in host.items():
-                getattr(S, k).copy_(t, non_blocking=True)
+            dev_in.copy_(host_in, non_blocking=True)
             step_fn()
             out_host.copy_(S.out, non_blocking=True)
 

@@ -56,6 +56,33 @@ class DecodeStep:
         self.kv_scale = W.kv_scale
         self.scale = W.scale
 
+    #: The step's per-call inputs, in the order they are packed by :meth:`stage_inputs`.
+    STEP_INPUTS = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+
+    def stage_inputs(self):
+        """Pack the per-step inputs into one device buffer and a pinned host twin.
+
+        Each input becomes a view into a single device byte buffer (sections
+        256-byte aligned), so a caller that keeps its step inputs in the
+        pinned twin moves all of them with one host-to-device copy.  Returns
+        ``(host, device)``, both uint8 of the same size; the host buffer
+        already holds the current inputs.
+        """
+        align = lambda n: (n + 255) // 256 * 256
+        tensors = [getattr(self, k) for k in self.STEP_INPUTS]
+        sizes = [t.numel() * t.element_size() for t in tensors]
+        total = sum(align(n) for n in sizes)
+        dev = torch.empty(total, dtype=torch.uint8, device=self.device)
+        host = torch.empty(total, dtype=torch.uint8).pin_memory()
+        off = 0
+        for name, t, n in zip(self.STEP_INPUTS, tensors, sizes):
+            view = dev[off:off + n].view(t.dtype).view(t.shape)
+            view.copy_(t)
+            host[off:off + n].copy_(view.view(torch.uint8).reshape(-1).cpu())
+            setattr(self, name, view)
+            off += align(n)
+        return host, dev
+
     def launches_per_step(self, path="append"):
         """Kernels one step enqueues.
 
