@@ -72,7 +72,7 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 bool encode_kv_tensor_map(void* desc, const void* base, int num_blocks, int num_kv_heads,
-                          int head_size, int elt_bytes, const char** why) {
+                          int head_size, int elt_bytes, int box_heads, const char** why) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     *why = "cuTensorMapEncodeTiled is not available from the driver";
@@ -89,7 +89,8 @@ bool encode_kv_tensor_map(void* desc, const void* base, int num_blocks, int num_
     // 128B swizzle span: dims (elements of a half, halves, kv heads, token rows).
     const cuuint64_t dims[4] = {128ull / elt_bytes, row / 128, (cuuint64_t)num_kv_heads, ntok};
     const cuuint64_t strides[3] = {128ull, row, token_stride};
-    const cuuint32_t box[4] = {128u / elt_bytes, (cuuint32_t)(row / 128), 1u, 16u};
+    const cuuint32_t box[4] = {128u / elt_bytes, (cuuint32_t)(row / 128), (cuuint32_t)box_heads,
+                               16u};
     const cuuint32_t es[4] = {1u, 1u, 1u, 1u};
     r = fn(static_cast<CUtensorMap*>(desc), dt, 4, const_cast<void*>(base), dims, strides, box,
            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -97,7 +98,7 @@ bool encode_kv_tensor_map(void* desc, const void* base, int num_blocks, int num_
   } else {
     const cuuint64_t dims[3] = {(cuuint64_t)head_size, (cuuint64_t)num_kv_heads, ntok};
     const cuuint64_t strides[2] = {row, token_stride};
-    const cuuint32_t box[3] = {(cuuint32_t)head_size, 1u, 16u};
+    const cuuint32_t box[3] = {(cuuint32_t)head_size, (cuuint32_t)box_heads, 16u};
     const cuuint32_t es[3] = {1u, 1u, 1u};
     r = fn(static_cast<CUtensorMap*>(desc), dt, 3, const_cast<void*>(base), dims, strides, box,
            es, CU_TENSOR_MAP_INTERLEAVE_NONE,

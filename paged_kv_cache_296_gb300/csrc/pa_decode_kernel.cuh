@@ -1,4 +1,4 @@
-// Paged decode attention: one CTA per (kv_head, KV partition, sequence).
+// Paged decode attention: one CTA per (KV head group, KV partition, sequence).
 //
 // What it computes ("vLLM GitHub 项目…" section 二; "vLLM 部署深度指南" sections
 // PagedAttention 方案 and 代码层面理解): for every sequence i and query head h,
@@ -6,21 +6,27 @@
 // where K_i / V_i are the sequence's first L_i tokens, found block by block
 // through its block table (logical block j // 16 -> physical block, offset
 // j % 16) in the pool [num_blocks, 16, 2, Hkv, D].  Query head h reads KV head
-// h / G (G = Hq / Hkv), so each CTA serves the G query heads of one KV head and
-// reads every K/V byte of that head once.
+// h / G (G = Hq / Hkv), so each CTA serves the G query heads of its KV heads
+// and reads every K/V byte of those heads once.  A CTA takes H adjacent KV
+// heads (H = 1 for 16-bit caches, whose rows are 256 bytes; H = 2 for E4M3,
+// so each token's K (and V) bytes of the group are one 256-byte run in the
+// pool: measured on GB300, streaming that pattern in 128-byte runs tops out
+// near 6.1 TB/s, in 256-byte runs near 6.7 TB/s).
 //
-// Layout of the work inside a CTA (160 threads):
-//   * warp 4 (producer): one lane reads the partition's block-table entries
-//     and issues one TMA load per 16-token block for K and one for V into a
-//     ring of shared-memory stages, each guarded by a "full" and an "empty"
-//     mbarrier.  Tiles land 128B-swizzled, so fragment loads are bank-conflict
-//     free.
-//   * warps 0-3 (consumers): warp w takes blocks w, w+4, ...  For each block it
+// Layout of the work inside a CTA (4H consumer warps + 1 producer warp):
+//   * the producer warp: one lane reads the partition's block-table entries
+//     and issues one TMA load per 16-token block for K and one for V (all H
+//     heads) into a ring of shared-memory stages, each guarded by a "full"
+//     and an "empty" mbarrier.  Tiles land 128B-swizzled, so fragment loads
+//     are bank-conflict free.
+//   * consumers: warps 4j .. 4j+3 serve the group's head j; warp 4j + w takes
+//     blocks w, w+4, ... and releases each stage once all H heads are done
+//     with it (the empty barrier counts H arrivals).  For each block it
 //     computes S^T = K . Q^T with m16n8k16 tensor-core MMAs (tokens as M = 16,
 //     the G <= 8 query heads as N = 8, head_size as K), runs the online softmax
 //     on the fragment, turns P^T into the B operand with movmatrix, and
 //     accumulates O^T += V^T . P^T (head_size as M).  All accumulation is fp32.
-//   * at the end the four warps' (m, l, O) states are merged through shared
+//   * at the end each head's four warps' (m, l, O) states are merged through shared
 //     memory; the CTA writes the normalised output (one partition) or an fp32
 //     partial (m, l, O) that the merge kernel combines by log-sum-exp.
 //
@@ -51,6 +57,7 @@ struct DecodeParams {
   int num_blocks;
   int num_q_heads;
   int num_kv_heads;
+  int kv_groups;                // CTAs per (sequence, partition): ceil(num_kv_heads / H)
   int group;                    // G = Hq / Hkv, 1..8
   int partition_blocks;         // partition size in 16-token blocks; 0 = balanced (below)
   // Balanced split: the partition size is chosen in the kernel from the actual
@@ -76,22 +83,25 @@ struct DecodeParams {
 template <int D, int KV>
 struct DecodeCfg {
   static constexpr int kElt = (KV == kKvE4m3) ? 1 : 2;
+  static constexpr int kHeads = (KV == kKvE4m3) ? 2 : 1;  // KV heads per CTA (H)
   static constexpr int kRowBytes = D * kElt;          // one token row of one head
-  static constexpr int kTileBytes = 16 * kRowBytes;   // one block of K (or V) for one head
+  static constexpr int kTileBytes = 16 * kHeads * kRowBytes;  // one block of K (or V), H heads
   static constexpr int kStageBytes = 2 * kTileBytes;  // K tile then V tile
-  static constexpr int kConsumerWarps = 4;
-  // Block `it` goes to stage it % kStages and to consumer warp it % 4.  With
-  // kStages a multiple of 4, every stage has one consumer warp that waits on
-  // its phases strictly in order, so a parity wait never runs two phases ahead
-  // of its barrier (which would let it pass early).  Two or more stages per
-  // warp let the producer run ahead while a warp computes.  A CTA streams
-  // about (ring bytes) / (loaded memory latency, ~3.5 us on GB300), so the
-  // ring is 64 KB whatever the stage size.
+  static constexpr int kWarpsPerHead = 4;
+  static constexpr int kConsumerWarps = kWarpsPerHead * kHeads;
+  // Block `it` goes to stage it % kStages and to warp it % 4 of every head.
+  // With kStages a multiple of 4, every stage has one consumer warp per head
+  // that waits on its phases strictly in order, so a parity wait never runs
+  // two phases ahead of its barrier (which would let it pass early).  Two or
+  // more stages per warp let the producer run ahead while a warp computes.  A
+  // CTA streams about (ring bytes) / (loaded memory latency, ~3.5 us on
+  // GB300), so the ring is 64 KB whatever the stage size.
   static constexpr int kStages = (kStageBytes >= 8192) ? 8 : 16;
-  static_assert(kStages % kConsumerWarps == 0 && kStages >= 2 * kConsumerWarps,
-                "each stage must belong to exactly one consumer warp");
+  static_assert(kStages % kWarpsPerHead == 0 && kStages >= 2 * kWarpsPerHead,
+                "each stage must belong to exactly one consumer warp per head");
   static constexpr int kSwizzle = (kRowBytes >= 128) ? 128 : 64;
   static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+  static constexpr int kMinCtasPerSm = (kHeads == 1) ? 4 : 2;  // register budget
   static constexpr int kMTiles = D / 16;              // m-tiles of O^T, k-steps of S^T
   static constexpr int kRedStride = D + 4;            // floats per head row in the merge buffer
   static constexpr int kRingBytes = kStages * kStageBytes;
@@ -134,112 +144,130 @@ __device__ __forceinline__ uint32_t token_mask(int tok, int valid) {
 }
 
 // Balanced split (partition_blocks == 0).  The grid is one dimension of
-// `slots` CTAs (one wave on this GPU, or the number of (sequence, KV head)
-// pairs if that is larger).  Every CTA computes the same plan from the actual
-// context lengths:
+// `slots` CTAs (one wave on this GPU, or the number of (sequence, KV head
+// group) pairs if that is larger).  Every CTA computes the same plan from the
+// actual context lengths:
 //   pb = the smallest partition size in blocks, >= min_partition_blocks, with
-//        num_kv_heads * sum_i max(1, ceil(ceil(L_i / 16) / pb)) <= slots;
+//        kv_groups * sum_i max(1, ceil(ceil(L_i / 16) / pb)) <= slots;
 // then takes work item blockIdx.x of the list ordered by (sequence, partition,
-// KV head) -- each sequence has at least one item, so empty sequences still
-// get their zero output.  Items past the list's end exit at once.
+// KV head group) -- each sequence has at least one item, so empty sequences
+// still get their zero output.  Items past the list's end exit at once.
+//
+// The plan is on every CTA's critical path, so it is a k-ary search: in each
+// round the CTA's warps test kWarps evenly spaced sizes at once (the count is
+// monotone in pb) and keep the interval where the test flips, one barrier per
+// round.  The interval starts narrow: with T blocks over V sequences,
+// count(pb) <= T / pb + V, so every pb >= kv_groups * T / (slots - kv_groups * V)
+// fits, while none below kv_groups * T / slots does; for a few long sequences
+// that is a window of a few dozen sizes, two or three rounds.
+constexpr int kMaxBalancedSeqs = 512;  // the host only picks the mode below this
+
 struct BalancedItem {
-  int pb, seq, part, kvh;
+  int pb, seq, part, kvg;
   bool valid;
 };
 
+struct BalancedScratch {
+  int nb[kMaxBalancedSeqs];  // blocks per sequence; -1: negative length (no item)
+  int fits[2][32];           // per round parity, per warp
+  int chunk[kMaxBalancedSeqs / 32];
+  int pick[2];
+};
+
 template <int kThreads>
-__device__ __forceinline__ BalancedItem balanced_plan(const DecodeParams& p, int* red, int* pick) {
+__device__ __forceinline__ BalancedItem balanced_plan(const DecodeParams& p, BalancedScratch& sc) {
   constexpr int kWarps = kThreads / 32;
-  constexpr int kPer = 4;  // sequences per thread, contiguous (the mode has < 512 sequences)
-  int nb[kPer];
-  int total = 0, maxnb = 0;
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int i = threadIdx.x * kPer + k;
-    const int L = i < p.num_seqs ? p.context_lens[i] : -1;
-    nb[k] = L > 0 ? (L + 15) >> 4 : (L == 0 ? 0 : -1);  // -1: no such sequence
-    total += max(nb[k], 0);
-    maxnb = max(maxnb, nb[k]);
-  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  auto block_reduce = [&](int v, bool is_max) {
+  const int B = p.num_seqs;
+  for (int i = threadIdx.x; i < B; i += kThreads) {
+    const int L = p.context_lens[i];
+    sc.nb[i] = L > 0 ? (L + 15) >> 4 : (L == 0 ? 0 : -1);
+  }
+  if (threadIdx.x == 0) sc.pick[0] = -1;
+  __syncthreads();
+  auto parts_of = [](int n, int pbv) { return n < 0 ? 0 : max(1, (n + pbv - 1) / pbv); };
+  // Every warp reduces the totals itself: no barrier needed.
+  int total = 0, maxnb = 0, nvalid = 0;
+  for (int i = lane; i < B; i += 32) {
+    const int n = sc.nb[i];
+    total += max(n, 0);
+    maxnb = max(maxnb, n);
+    nvalid += n >= 0 ? 1 : 0;
+  }
 #pragma unroll
-    for (int x = 16; x > 0; x >>= 1) {
-      const int o = __shfl_xor_sync(0xffffffffu, v, x);
-      v = is_max ? max(v, o) : v + o;
-    }
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    int r = red[0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) r = is_max ? max(r, red[w]) : r + red[w];
-    return r;
-  };
-  auto parts_of = [&](int pbv, int k) { return nb[k] < 0 ? 0 : max(1, (nb[k] + pbv - 1) / pbv); };
-  total = block_reduce(total, false);
-  maxnb = block_reduce(maxnb, true);
-  const long long want = ((long long)total * p.num_kv_heads + p.slots - 1) / p.slots;
+  for (int x = 16; x > 0; x >>= 1) {
+    total += __shfl_xor_sync(0xffffffffu, total, x);
+    maxnb = max(maxnb, __shfl_xor_sync(0xffffffffu, maxnb, x));
+    nvalid += __shfl_xor_sync(0xffffffffu, nvalid, x);
+  }
+  const long long tg = (long long)total * p.kv_groups;
+  const long long want = (tg + p.slots - 1) / p.slots;
   int lo = max(p.min_partition_blocks, (int)(want < (1ll << 30) ? want : (1ll << 30)));
-  int hi = max(lo, maxnb);  // count(maxnb) = pairs <= slots
-  while (lo < hi) {
-    const int mid = lo + (hi - lo) / 2;
-    int c = 0;
+  // Every sequence in one partition (pb = maxnb) fits, as kv_groups * B <= slots.
+  long long ub = maxnb;
+  const long long spare = (long long)p.slots - (long long)nvalid * p.kv_groups;
+  if (spare > 0) ub = min(ub, (tg + spare - 1) / spare);
+  int hi = max(lo, (int)ub);
+  for (int round = 0; lo < hi; ++round) {
+    const long long span = hi - lo;
+    const int c = lo + (int)(span * (warp + 1) / kWarps);  // the last warp tests hi
+    int cnt = 0;
+    for (int i = lane; i < B; i += 32) cnt += parts_of(sc.nb[i], c);
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) c += parts_of(mid, k);
-    if ((long long)block_reduce(c, false) * p.num_kv_heads <= p.slots) {
-      hi = mid;
-    } else {
-      lo = mid + 1;
-    }
+    for (int x = 16; x > 0; x >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, x);
+    int* fits = sc.fits[round & 1];  // alternate so the next round's writes race no reads
+    if (lane == 0) fits[warp] = ((long long)cnt * p.kv_groups <= p.slots) ? 1 : 0;
+    __syncthreads();
+    int w = kWarps - 1;
+#pragma unroll
+    for (int k = kWarps - 2; k >= 0; --k) w = fits[k] ? k : w;
+    hi = lo + (int)(span * (w + 1) / kWarps);
+    lo = (w == 0) ? lo : lo + (int)(span * w / kWarps) + 1;
   }
   const int pb = lo;
-  // Exclusive prefix of partitions over sequences (threads hold consecutive
-  // sequences), then find the item's sequence and partition.
-  int mine = 0;
+  // The item's (sequence, partition): prefix sums of partitions over
+  // sequences, by chunks of 32 sequences per warp.
+  const int nchunks = (B + 31) / 32;
+  for (int ch = warp; ch < nchunks; ch += kWarps) {
+    const int i = ch * 32 + lane;
+    int v = i < B ? parts_of(sc.nb[i], pb) : 0;
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) mine += parts_of(pb, k);
-  int incl = mine;
-#pragma unroll
-  for (int x = 1; x < 32; x <<= 1) {
-    const int o = __shfl_up_sync(0xffffffffu, incl, x);
-    if (lane >= x) incl += o;
+    for (int x = 16; x > 0; x >>= 1) v += __shfl_xor_sync(0xffffffffu, v, x);
+    if (lane == 0) sc.chunk[ch] = v;
   }
   __syncthreads();
-  if (lane == 31) red[warp] = incl;
-  if (threadIdx.x == 0) pick[0] = -1;
-  __syncthreads();
-  int before = incl - mine;
-  for (int w = 0; w < warp; ++w) before += red[w];
+  const int q = blockIdx.x / p.kv_groups;  // the item's (sequence, partition) index
   int all = 0;
+  for (int ch = 0; ch < nchunks; ++ch) all += sc.chunk[ch];
+  for (int ch = warp; ch < nchunks; ch += kWarps) {
+    int before = 0;
+    for (int k = 0; k < ch; ++k) before += sc.chunk[k];
+    const int i = ch * 32 + lane;
+    const int mine = i < B ? parts_of(sc.nb[i], pb) : 0;
+    int incl = mine;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) all += red[w];
-  const int q = blockIdx.x / p.num_kv_heads;  // the item's (sequence, partition) index
-  if (q >= before && q < before + mine) {
-    int acc = before;
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int n = parts_of(pb, k);
-      if (q < acc + n) {
-        pick[0] = threadIdx.x * kPer + k;
-        pick[1] = q - acc;
-        break;
-      }
-      acc += n;
+    for (int x = 1; x < 32; x <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, x);
+      if (lane >= x) incl += o;
+    }
+    const int excl = before + incl - mine;
+    if (q >= excl && q < excl + mine) {
+      sc.pick[0] = i;
+      sc.pick[1] = q - excl;
     }
   }
   __syncthreads();
   BalancedItem it;
   it.pb = pb;
-  it.valid = q < all && pick[0] >= 0;
-  it.seq = it.valid ? pick[0] : 0;
-  it.part = it.valid ? pick[1] : 0;
-  it.kvh = blockIdx.x % p.num_kv_heads;
+  it.valid = q < all && sc.pick[0] >= 0;
+  it.seq = it.valid ? sc.pick[0] : 0;
+  it.part = it.valid ? sc.pick[1] : 0;
+  it.kvg = blockIdx.x % p.kv_groups;
   return it;
 }
 
 template <int D, int KV, int QT, bool kAppend>
-__global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
+__global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, DecodeCfg<D, KV>::kMinCtasPerSm)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
   using C = DecodeCfg<D, KV>;
@@ -253,16 +281,24 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kRingBytes);
   uint64_t* empty_bar = full_bar + C::kStages;
 
-  int kvh = blockIdx.x, part = blockIdx.y, seq = blockIdx.z;
+  // Launched with programmatic stream serialisation, this grid may start while
+  // the kernel before it on the stream is still running; that kernel may have
+  // written any input (q, tables, lengths, the pool), so every thread waits
+  // for it before its first global read.  (The tensor maps are parameters.)
+  if (threadIdx.x == C::kConsumerWarps * 32) {
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+  }
+  griddep_wait();
+  int kvg = blockIdx.x, part = blockIdx.y, seq = blockIdx.z;
   int pb = p.partition_blocks;
   if (pb == 0) {
-    __shared__ int red[C::kThreads / 32];
-    __shared__ int pick[2];
-    const BalancedItem item = balanced_plan<C::kThreads>(p, red, pick);
+    __shared__ BalancedScratch plan_scratch;
+    const BalancedItem item = balanced_plan<C::kThreads>(p, plan_scratch);
     if (threadIdx.x == 0 && blockIdx.x == 0) *p.plan = item.pb;
     if (!item.valid) return;
     pb = item.pb;
-    kvh = item.kvh;
+    kvg = item.kvg;
     part = item.part;
     seq = item.seq;
   }
@@ -273,6 +309,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
   const int ntok = min(L - tok0, part_tokens);
   const int nblk = ntok > 0 ? (ntok + 15) >> 4 : 0;
   const int nparts_seq = (L + part_tokens - 1) / part_tokens;  // 0 when L == 0
+  const int kv0 = kvg * C::kHeads;  // the group's first KV head
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -280,7 +317,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], C::kHeads);
     }
     mbar_fence_init();
   }
@@ -296,21 +333,19 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
 
   if (warp == C::kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmap_k);
-      tma_prefetch_desc(&tmap_v);
-    }
-    // The pool may have just been written by the preceding kernel (the step's
-    // reshape_and_cache): wait for it before the first access to it.  Nothing
-    // read before this point (q, tables, lengths) is written there.
-    griddep_wait();
+    const int32_t* tbl =
+        p.block_tables + (size_t)seq * p.max_blocks_per_seq + (size_t)part * pb;
+    int mine = (lane < nblk) ? __ldg(tbl + lane) : 0;
     if constexpr (kAppend) {
-      // append_kv for this sequence's new token, head kvh: the CTA holding the
-      // partition with position L - 1 writes it, then makes the write visible
-      // to its own TMA loads (generic -> async proxy) before issuing them.
-      if (L > 0 && part == nparts_seq - 1) {
-        const int64_t slot = p.slot_mapping[seq];
-        if (slot >= 0 && slot < (int64_t)p.num_blocks * 16) {
+      // append_kv for this sequence's new token, the group's heads: the CTA
+      // holding the partition with position L - 1 writes it, then makes the
+      // write visible to its own TMA loads (generic -> async proxy) before
+      // issuing them.
+      const int64_t slot = (L > 0 && part == nparts_seq - 1) ? p.slot_mapping[seq] : -1;
+#pragma unroll
+      for (int hh = 0; hh < C::kHeads; ++hh) {
+        const int kvh = kv0 + hh;
+        if (kvh < p.num_kv_heads && slot >= 0 && slot < (int64_t)p.num_blocks * 16) {
           constexpr int kSrcElt = 2;  // the new token comes in the q dtype
           const size_t src = (size_t)seq * p.src_stride_bytes + (size_t)kvh * D * kSrcElt;
           const size_t dst = (size_t)slot * (2ull * p.num_kv_heads * C::kRowBytes) +
@@ -360,13 +395,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
       }
       __syncwarp();
     }
-    const int32_t* tbl =
-        p.block_tables + (size_t)seq * p.max_blocks_per_seq + (size_t)part * pb;
     const int oob_row = p.num_blocks * 16;  // first token row past the pool: TMA fills zeros
+    const uint64_t kv_policy = l2_evict_first_policy();  // the KV stream is read once
     bool ok = true;
     int issued = 0;
     for (int base = 0; base < nblk; base += 32) {
-      const int mine = (base + lane < nblk) ? __ldg(tbl + base + lane) : 0;
+      if (base > 0) mine = (base + lane < nblk) ? __ldg(tbl + base + lane) : 0;
       const int cnt = min(32, nblk - base);
       for (int j = 0; j < cnt; ++j) {
         const int blk = __shfl_sync(0xffffffffu, mine, j);
@@ -381,11 +415,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
             uint8_t* ks = smem + s * C::kStageBytes;
             mbar_arrive_expect_tx(&full_bar[s], C::kStageBytes);
             if constexpr (C::kRowBytes > 128) {
-              tma_load_4d(ks, &tmap_k, &full_bar[s], 0, 0, kvh, row);
-              tma_load_4d(ks + C::kTileBytes, &tmap_v, &full_bar[s], 0, 0, kvh, row);
+              tma_load_4d(ks, &tmap_k, &full_bar[s], 0, 0, kv0, row, kv_policy);
+              tma_load_4d(ks + C::kTileBytes, &tmap_v, &full_bar[s], 0, 0, kv0, row, kv_policy);
             } else {
-              tma_load_3d(ks, &tmap_k, &full_bar[s], 0, kvh, row);
-              tma_load_3d(ks + C::kTileBytes, &tmap_v, &full_bar[s], 0, kvh, row);
+              tma_load_3d(ks, &tmap_k, &full_bar[s], 0, kv0, row, kv_policy);
+              tma_load_3d(ks + C::kTileBytes, &tmap_v, &full_bar[s], 0, kv0, row, kv_policy);
             }
             ++issued;
           }
@@ -402,8 +436,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
     }
   } else {
     // ------------------------------------------------------------ consumers
+    // Warp 4j + w serves head j of the group; a head past the last KV head
+    // (odd count) sees zero-filled tiles and writes nothing.
+    const int hsel = warp / C::kWarpsPerHead;
+    const int kvh = kv0 + hsel;
     const int head0 = kvh * p.group;
-    const bool head_live = g < p.group;
+    const bool head_live = kvh < p.num_kv_heads && g < p.group;
+    // Byte offset of token `tok`'s row of this warp's head inside a tile.
+    auto row_of = [&](int tok) { return (uint32_t)((tok * C::kHeads + hsel) * C::kRowBytes); };
     const size_t qrow = ((size_t)seq * p.num_q_heads + head0 + (head_live ? g : 0)) * D;
     // B operand (Q^T): 2 registers per k-step.
     uint32_t qb[C::kMTiles][2];
@@ -424,7 +464,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
       }
     }
 
-    for (int it = warp; it < nblk; it += C::kConsumerWarps) {
+    for (int it = warp % C::kWarpsPerHead; it < nblk; it += C::kWarpsPerHead) {
       const int s = it % C::kStages;
       const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
       if (!mbar_wait_bounded(&full_bar[s], ph, p.status)) break;
@@ -439,7 +479,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
 #pragma unroll
         for (int ks = 0; ks < C::kMTiles; ++ks) {
           uint32_t a[4];
-          ldsm_x4(a, kbase + swz<C::kSwizzle>(tok * C::kRowBytes + (ks * 2 + (lane >> 4)) * 16));
+          ldsm_x4(a, kbase + swz<C::kSwizzle>(row_of(tok) + (ks * 2 + (lane >> 4)) * 16));
           if constexpr (kBf16Mma) {
             mma_bf16(sacc, a, qb[ks][0], qb[ks][1]);
           } else {
@@ -451,9 +491,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
         uint32_t wa[C::kMTiles], wb[C::kMTiles];
 #pragma unroll
         for (int i = 0; i < kCpl; ++i) {
-          const uint4 xa = lds128(kbase + swz<C::kSwizzle>(g * C::kRowBytes + (kCpl * t + i) * 16));
-          const uint4 xb =
-              lds128(kbase + swz<C::kSwizzle>((g + 8) * C::kRowBytes + (kCpl * t + i) * 16));
+          const uint4 xa = lds128(kbase + swz<C::kSwizzle>(row_of(g) + (kCpl * t + i) * 16));
+          const uint4 xb = lds128(kbase + swz<C::kSwizzle>(row_of(g + 8) + (kCpl * t + i) * 16));
           wa[4 * i + 0] = xa.x; wa[4 * i + 1] = xa.y; wa[4 * i + 2] = xa.z; wa[4 * i + 3] = xa.w;
           wb[4 * i + 0] = xb.x; wb[4 * i + 1] = xb.y; wb[4 * i + 2] = xb.z; wb[4 * i + 3] = xb.w;
         }
@@ -525,7 +564,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
 #pragma unroll
         for (int mt = 0; mt < C::kMTiles; ++mt) {
           uint32_t a[4];
-          ldsm_x4_trans(a, vbase + swz<C::kSwizzle>(tok * C::kRowBytes + (mt * 2 + (mi & 1)) * 16));
+          ldsm_x4_trans(a, vbase + swz<C::kSwizzle>(row_of(tok) + (mt * 2 + (mi & 1)) * 16));
           if (valid < 16) {
             a[0] &= mlo; a[1] &= mlo; a[2] &= mhi; a[3] &= mhi;
           }
@@ -542,20 +581,20 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
         uint32_t va[D / 32], vb[D / 32], vc[D / 32], vd[D / 32];
         if constexpr (D == 128) {
           const uint32_t col = g * 16;
-          const uint4 x0 = lds128(vbase + swz<C::kSwizzle>((2 * t) * C::kRowBytes + col));
-          const uint4 x1 = lds128(vbase + swz<C::kSwizzle>((2 * t + 1) * C::kRowBytes + col));
-          const uint4 x2 = lds128(vbase + swz<C::kSwizzle>((2 * t + 8) * C::kRowBytes + col));
-          const uint4 x3 = lds128(vbase + swz<C::kSwizzle>((2 * t + 9) * C::kRowBytes + col));
+          const uint4 x0 = lds128(vbase + swz<C::kSwizzle>(row_of(2 * t) + col));
+          const uint4 x1 = lds128(vbase + swz<C::kSwizzle>(row_of(2 * t + 1) + col));
+          const uint4 x2 = lds128(vbase + swz<C::kSwizzle>(row_of(2 * t + 8) + col));
+          const uint4 x3 = lds128(vbase + swz<C::kSwizzle>(row_of(2 * t + 9) + col));
           va[0] = x0.x; va[1] = x0.y; va[2] = x0.z; va[3] = x0.w;
           vb[0] = x1.x; vb[1] = x1.y; vb[2] = x1.z; vb[3] = x1.w;
           vc[0] = x2.x; vc[1] = x2.y; vc[2] = x2.z; vc[3] = x2.w;
           vd[0] = x3.x; vd[1] = x3.y; vd[2] = x3.z; vd[3] = x3.w;
         } else {
           const uint32_t col = g * 8;
-          const uint2 x0 = lds64(vbase + swz<C::kSwizzle>((2 * t) * C::kRowBytes + col));
-          const uint2 x1 = lds64(vbase + swz<C::kSwizzle>((2 * t + 1) * C::kRowBytes + col));
-          const uint2 x2 = lds64(vbase + swz<C::kSwizzle>((2 * t + 8) * C::kRowBytes + col));
-          const uint2 x3 = lds64(vbase + swz<C::kSwizzle>((2 * t + 9) * C::kRowBytes + col));
+          const uint2 x0 = lds64(vbase + swz<C::kSwizzle>(row_of(2 * t) + col));
+          const uint2 x1 = lds64(vbase + swz<C::kSwizzle>(row_of(2 * t + 1) + col));
+          const uint2 x2 = lds64(vbase + swz<C::kSwizzle>(row_of(2 * t + 8) + col));
+          const uint2 x3 = lds64(vbase + swz<C::kSwizzle>(row_of(2 * t + 9) + col));
           va[0] = x0.x; va[1] = x0.y; vb[0] = x1.x; vb[1] = x1.y;
           vc[0] = x2.x; vc[1] = x2.y; vd[0] = x3.x; vd[1] = x3.y;
         }
@@ -595,9 +634,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
   // All loads are done: the split-KV merge kernel may start launching; it
   // waits for this grid to finish before reading the partials.
   griddep_launch_dependents();
-  float* red_o = reinterpret_cast<float*>(smem);                       // [4][8][D+4]
-  float* red_m = red_o + C::kConsumerWarps * 8 * C::kRedStride;          // [4][8]
-  float* red_l = red_m + C::kConsumerWarps * 8;                          // [4][8]
+  float* red_o = reinterpret_cast<float*>(smem);                       // [warps][8][D+4]
+  float* red_m = red_o + C::kConsumerWarps * 8 * C::kRedStride;          // [warps][8]
+  float* red_l = red_m + C::kConsumerWarps * 8;                          // [warps][8]
   if (warp < C::kConsumerWarps) {
     float* mine = red_o + warp * 8 * C::kRedStride;
 #pragma unroll
@@ -624,29 +663,54 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
   }
   __syncthreads();
 
+  // Combine each head's four warp states, four head_size elements per thread
+  // and step (float4 reads of the buffer, 8- or 16-byte global stores).
   const bool direct = nparts_seq <= 1;
-  for (int idx = threadIdx.x; idx < p.group * D; idx += C::kThreads) {
-    const int h = idx / D;
-    const int d = idx - h * D;
+  constexpr int kQuads = D / 4;
+  const int per_head = p.group * kQuads;
+  for (int idx = threadIdx.x; idx < C::kHeads * per_head; idx += C::kThreads) {
+    const int hs = idx / per_head;  // head of the group
+    const int rem = idx - hs * per_head;
+    const int h = rem / kQuads;
+    const int d = (rem - h * kQuads) * 4;
+    const int kvh = kv0 + hs;
+    if (kvh >= p.num_kv_heads) break;  // later idx are past it too
+    const int w0 = hs * C::kWarpsPerHead;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < C::kConsumerWarps; ++w) M = fmaxf(M, red_m[w * 8 + h]);
-    float num = 0.f, den = 0.f;
+    for (int w = w0; w < w0 + C::kWarpsPerHead; ++w) M = fmaxf(M, red_m[w * 8 + h]);
+    float num[4] = {0.f, 0.f, 0.f, 0.f}, den = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < C::kConsumerWarps; ++w) {
+      for (int w = w0; w < w0 + C::kWarpsPerHead; ++w) {
         const float wt = ex2_approx(__fsub_rn(red_m[w * 8 + h], M));
-        num = __fmaf_rn(wt, red_o[(w * 8 + h) * C::kRedStride + d], num);
+        const float4 ov = *reinterpret_cast<const float4*>(&red_o[(w * 8 + h) * C::kRedStride + d]);
+        num[0] = __fmaf_rn(wt, ov.x, num[0]);
+        num[1] = __fmaf_rn(wt, ov.y, num[1]);
+        num[2] = __fmaf_rn(wt, ov.z, num[2]);
+        num[3] = __fmaf_rn(wt, ov.w, num[3]);
         den = __fmaf_rn(wt, red_l[w * 8 + h], den);
       }
     }
     const int qh = kvh * p.group + h;
     if (direct) {
-      const float v = (den > 0.f) ? __fmul_rn(__fdiv_rn(num, den), p.out_scale) : 0.f;
-      store_out<QT>(p.out, ((size_t)seq * p.num_q_heads + qh) * D + d, v);
+      float v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        v[k] = (den > 0.f) ? __fmul_rn(__fdiv_rn(num[k], den), p.out_scale) : 0.f;
+      uint2 pk;
+      if constexpr (QT == kKvF16) {
+        pk.x = pack_f16x2(v[0], v[1]);
+        pk.y = pack_f16x2(v[2], v[3]);
+      } else {
+        pk.x = pack_bf16x2(v[0], v[1]);
+        pk.y = pack_bf16x2(v[2], v[3]);
+      }
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) +
+                                ((size_t)seq * p.num_q_heads + qh) * D + d) = pk;
     } else {
       const size_t pi = ((size_t)seq * p.num_q_heads + qh) * p.num_partitions + part;
-      p.part_o[pi * D + d] = num;
+      *reinterpret_cast<float4*>(p.part_o + pi * D + d) = make_float4(num[0], num[1], num[2], num[3]);
       if (d == 0) {
         p.part_m[pi] = M;
         p.part_l[pi] = den;
@@ -658,9 +722,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, 4)
 // Log-sum-exp merge of split-KV partials: one CTA of kMergeThreads per
 // (sequence, query head).  The threads form kMergeThreads / D groups; group r
 // takes partitions r, r + groups, ... and thread d of a group accumulates
-// head_size element d, so every partial's O row is read once, coalesced, with
-// several independent loads in flight per thread.  The groups' sums are added
-// in a fixed order, so the result does not depend on timing.
+// head_size element d with a running maximum (one pass: m, l and O of four
+// partitions are loaded together, then folded in), so every partial's O row
+// is read once, coalesced.  The groups' states are combined in a fixed order,
+// so the result does not depend on timing.
 constexpr int kMergeThreads = 256;
 
 template <int D, int QT>
@@ -669,12 +734,14 @@ __global__ void __launch_bounds__(kMergeThreads)
   constexpr int kGroups = kMergeThreads / D;
   __shared__ float red_acc[kGroups][D];
   __shared__ float red_den[kGroups];
-  __shared__ float red_max[kMergeThreads / 32];
+  __shared__ float red_max[kGroups];
 
   const int idx = blockIdx.x;  // sequence * num_q_heads + query head
   const int seq = idx / p.num_q_heads;
   const int L = p.context_lens[seq];
-  // A balanced split never cuts a sequence shorter than its minimum partition.
+  // The kernel before this one is always the same call's attention kernel,
+  // which writes no lengths: they may be read before the wait.  A balanced
+  // split never cuts a sequence shorter than its minimum partition.
   if (p.partition_blocks == 0 && L <= p.min_partition_blocks * 16) return;
   griddep_wait();  // the partials (and a balanced split's size) come from the attention kernel
   const int part_tokens = (p.partition_blocks ? p.partition_blocks : *p.plan) * 16;
@@ -682,20 +749,24 @@ __global__ void __launch_bounds__(kMergeThreads)
   if (np <= 1) return;  // written directly by the attention kernel
   const size_t base = (size_t)idx * p.num_partitions;
   const int tid = threadIdx.x;
-
-  float M = -INFINITY;
-  for (int i = tid; i < np; i += kMergeThreads) M = fmaxf(M, p.part_m[base + i]);
-#pragma unroll
-  for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
-  if ((tid & 31) == 0) red_max[tid >> 5] = M;
-  __syncthreads();
-  M = red_max[0];
-#pragma unroll
-  for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red_max[w]);
-
   const int r = tid / D;
   const int d = tid - r * D;
-  float acc = 0.f, den = 0.f;
+
+  // Fold partials into (M, den, acc) with M the running maximum (log2 domain).
+  float M = -INFINITY, acc = 0.f, den = 0.f;
+  auto fold = [&](float mx, int n, const float* mv, const float* lv, const float* ov) {
+    const float Mn = fmaxf(M, mx);
+    if (Mn == -INFINITY) return;  // nothing seen yet
+    const float sc = ex2_approx(__fsub_rn(M, Mn));  // 0 when M is still -inf
+    acc = __fmul_rn(acc, sc);
+    den = __fmul_rn(den, sc);
+    for (int u = 0; u < n; ++u) {
+      const float w = ex2_approx(__fsub_rn(mv[u], Mn));
+      den = __fmaf_rn(w, lv[u], den);
+      acc = __fmaf_rn(w, ov[u], acc);
+    }
+    M = Mn;
+  };
   int i = r;
   for (; i + 3 * kGroups < np; i += 4 * kGroups) {
     float mv[4], lv[4], ov[4];
@@ -706,28 +777,31 @@ __global__ void __launch_bounds__(kMergeThreads)
       lv[u] = p.part_l[pi];
       ov[u] = p.part_o[pi * D + d];
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float w = ex2_approx(__fsub_rn(mv[u], M));
-      den = __fmaf_rn(w, lv[u], den);
-      acc = __fmaf_rn(w, ov[u], acc);
-    }
+    fold(fmaxf(fmaxf(mv[0], mv[1]), fmaxf(mv[2], mv[3])), 4, mv, lv, ov);
   }
   for (; i < np; i += kGroups) {
     const size_t pi = base + i;
-    const float w = ex2_approx(__fsub_rn(p.part_m[pi], M));
-    den = __fmaf_rn(w, p.part_l[pi], den);
-    acc = __fmaf_rn(w, p.part_o[pi * D + d], acc);
+    const float mv = p.part_m[pi], lv = p.part_l[pi], ov = p.part_o[pi * D + d];
+    fold(mv, 1, &mv, &lv, &ov);
   }
   red_acc[r][d] = acc;
-  if (d == 0) red_den[r] = den;
+  if (d == 0) {
+    red_den[r] = den;
+    red_max[r] = M;
+  }
   __syncthreads();
   if (r == 0) {
-    float a = red_acc[0][d], dn = red_den[0];
+    float Mall = red_max[0];
 #pragma unroll
-    for (int g = 1; g < kGroups; ++g) {
-      a = __fadd_rn(a, red_acc[g][d]);
-      dn = __fadd_rn(dn, red_den[g]);
+    for (int g = 1; g < kGroups; ++g) Mall = fmaxf(Mall, red_max[g]);
+    float a = 0.f, dn = 0.f;
+    if (Mall != -INFINITY) {
+#pragma unroll
+      for (int g = 0; g < kGroups; ++g) {
+        const float w = ex2_approx(__fsub_rn(red_max[g], Mall));
+        a = __fmaf_rn(w, red_acc[g][d], a);
+        dn = __fmaf_rn(w, red_den[g], dn);
+      }
     }
     const float v = (dn > 0.f) ? __fmul_rn(__fdiv_rn(a, dn), p.out_scale) : 0.f;
     store_out<QT>(p.out, (size_t)idx * D + d, v);

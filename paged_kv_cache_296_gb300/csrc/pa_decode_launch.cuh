@@ -43,9 +43,8 @@ cudaError_t launch_decode_kernel(const CUtensorMap& tk, const CUtensorMap& tv,
       slots = std::max(1, per_sm * sms);
       slots_cache[dev & 63].store(slots, std::memory_order_release);
     }
-    // One CTA per work item; at least one item per (sequence, KV head).
-    const_cast<DecodeParams&>(p).slots =
-        std::max(slots, a.num_seqs * a.num_kv_heads);
+    // One CTA per work item; at least one item per (sequence, KV head group).
+    const_cast<DecodeParams&>(p).slots = std::max(slots, a.num_seqs * p.kv_groups);
   }
   // Both kernels are launched with programmatic stream serialisation: each may
   // start while the kernel before it drains, and waits (griddepcontrol.wait)
@@ -56,7 +55,7 @@ cudaError_t launch_decode_kernel(const CUtensorMap& tk, const CUtensorMap& tv,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = p.partition_blocks == 0
                     ? dim3((unsigned)p.slots)
-                    : dim3((unsigned)a.num_kv_heads, (unsigned)a.num_partitions, (unsigned)a.num_seqs);
+                    : dim3((unsigned)p.kv_groups, (unsigned)a.num_partitions, (unsigned)a.num_seqs);
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
@@ -79,8 +78,10 @@ cudaError_t launch_decode_instance(const DecodeArgs& a, cudaStream_t stream, con
   using C = DecodeCfg<D, KV>;
   alignas(64) CUtensorMap tk;
   alignas(64) CUtensorMap tv;
-  if (!encode_kv_tensor_map(&tk, a.k_cache, a.num_blocks, a.num_kv_heads, D, C::kElt, why) ||
-      !encode_kv_tensor_map(&tv, a.v_cache, a.num_blocks, a.num_kv_heads, D, C::kElt, why)) {
+  if (!encode_kv_tensor_map(&tk, a.k_cache, a.num_blocks, a.num_kv_heads, D, C::kElt, C::kHeads,
+                            why) ||
+      !encode_kv_tensor_map(&tv, a.v_cache, a.num_blocks, a.num_kv_heads, D, C::kElt, C::kHeads,
+                            why)) {
     return cudaErrorInvalidValue;
   }
   DecodeParams p;
@@ -97,6 +98,7 @@ cudaError_t launch_decode_instance(const DecodeArgs& a, cudaStream_t stream, con
   p.num_blocks = a.num_blocks;
   p.num_q_heads = a.num_q_heads;
   p.num_kv_heads = a.num_kv_heads;
+  p.kv_groups = (a.num_kv_heads + C::kHeads - 1) / C::kHeads;
   p.group = a.num_q_heads / a.num_kv_heads;
   p.partition_blocks = a.partition_tokens / 16;
   p.min_partition_blocks = a.min_partition_tokens / 16;

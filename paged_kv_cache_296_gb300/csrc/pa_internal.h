@@ -71,9 +71,10 @@ int record_error_code(int status, const char* msg);
 cudaError_t device_status_ptr(unsigned** ptr);
 
 // Encodes a TMA descriptor for one view (K or V) of the pool, as used by the
-// decode kernel: rows of head_size elements per (token, kv head), 16 token
-// rows per box, 128B (or 64B) swizzle.  `desc` points to a CUtensorMap.
+// decode kernel: rows of head_size elements per (token, kv head); a box is 16
+// tokens x `box_heads` adjacent KV heads (heads past the last read as zeros),
+// 128B (or 64B) swizzle.  `desc` points to a CUtensorMap.
 bool encode_kv_tensor_map(void* desc, const void* base, int num_blocks, int num_kv_heads,
-                          int head_size, int elt_bytes, const char** why);
+                          int head_size, int elt_bytes, int box_heads, const char** why);
 
 }  // namespace pa

@@ -417,3 +417,42 @@ def test_workspace_garbage_does_not_matter():
         outs.append(S.out.clone())
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+@pytest.mark.parametrize("hkv,group,path,part", [(1, 8, "separate", 0), (3, 2, "append", 0),
+                                                 (5, 1, "separate", 64), (3, 4, "append", 512),
+                                                 (1, 4, "append", 16)])
+def test_fp8_odd_kv_head_counts(hkv, group, path, part):
+    """E4M3 CTAs take KV heads in pairs; with an odd count the last pair's second
+    head does not exist.  Every real head must match the oracle, the pool must
+    hold exactly the oracle's bytes, and nothing past ``out`` may be written."""
+    lens = [1, 17, 300, 1500, 40, 0]
+    spec = wl.Spec("fp8, odd KV head count", len(lens), hkv * group, hkv, 128, "bf16", "e4m3",
+                   ("fixed", lens), ("factor", 1.3))
+    W = wl.make_workload(spec, 40 + hkv + group, poison=True, table_garbage=True)
+    from paged_kv_cache_296_gb300.runner import DecodeStep
+    S = DecodeStep(W, device="cuda", partition_size=part)
+    n = S.out.numel()
+    canary = torch.full((n + 4096,), -7.0, dtype=S.out.dtype, device="cuda")
+    out = canary[:n].view(S.out.shape)
+    if path == "append":
+        pa.pa_decode_append(out, S.q, S.k_new, S.v_new, S.slot_mapping, S.k_cache, S.v_cache,
+                            S.block_tables, S.context_lens, S.scale, kv_scale=S.kv_scale,
+                            partition_size=part, workspace=S.workspace)
+    else:
+        S.write()
+        pa.pa_decode(out, S.q, S.k_cache, S.v_cache, S.block_tables, S.context_lens, S.scale,
+                     kv_scale=S.kv_scale, partition_size=part, workspace=S.workspace)
+    assert bool((canary[n:] == -7.0).all()), "a write landed past the output"
+    got = H.widen_out(out, spec.q_dtype)
+    assert np.isfinite(got).all()
+    assert np.array_equal(got[-1], np.zeros_like(got[-1])), "empty context must give zeros"
+    for i in range(spec.num_seqs):
+        for h in range(hkv):
+            blocks, mini = H.mini_case(W, i, h)
+            opool, want = H.oracle_mini(W, mini)
+            if len(blocks):
+                gpool = H.bits_of(S.pool[torch.from_numpy(blocks).cuda()][:, :, :, h:h + 1].cpu())
+                live = ~e4m3.is_nan_code(opool)
+                assert np.array_equal(gpool[live], opool[live])
+            H.assert_close(got[i, h * group:(h + 1) * group], want, spec, f"s{i} h{h}")

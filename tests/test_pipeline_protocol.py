@@ -1,14 +1,15 @@
 """A CPU model of the decode kernel's shared-memory ring protocol (no GPU).
 
 The decode kernel's producer fills stage ``it % S`` for block ``it`` and
-signals a "full" mbarrier; consumer warp ``it % W`` waits on that barrier by
-phase parity, reads the stage and arrives on its "empty" barrier, which the
+signals a "full" mbarrier; for each of the CTA's H KV heads, consumer warp
+``it % W`` of that head waits on the barrier by phase parity, reads the stage
+and arrives on its "empty" barrier (H arrivals complete a phase), which the
 producer waits on (parity) before refilling.  A parity wait only tells two
 consecutive phases apart, so a waiter must never be two phases ahead of its
 barrier.  This model runs the protocol under random interleavings with the
 mbarrier rules written out and checks that every consumer reads the block it
 expects.  It pins the rule the kernel's static_assert encodes: the stage count
-must be a multiple of the consumer-warp count (6 stages over 4 warps breaks).
+must be a multiple of the per-head warp count (6 stages over 4 warps breaks).
 """
 
 import random
@@ -47,14 +48,15 @@ class Barrier:
             self.pending = self.count
 
 
-def run_protocol(nblk, stages, warps, seed):
+def run_protocol(nblk, stages, warps, seed, heads=1):
     rnd = random.Random(seed)
     full = [Barrier(1) for _ in range(stages)]
-    empty = [Barrier(1) for _ in range(stages)]
+    empty = [Barrier(heads) for _ in range(stages)]
     holds = [None] * stages          # block whose bytes have landed in the stage
     in_flight = []                   # (stage, block) copies not yet landed
     produced = 0
-    next_block = {w: w for w in range(warps)}
+    consumers = [(h, w) for h in range(heads) for w in range(warps)]
+    next_block = {c: c[1] for c in consumers}
     for _ in range(10 ** 6):
         moves = []
         if produced < nblk:
@@ -63,10 +65,10 @@ def run_protocol(nblk, stages, warps, seed):
                 moves.append(("produce",))
         if in_flight:
             moves.append(("land",))
-        for w in range(warps):
-            it = next_block[w]
+        for c in consumers:
+            it = next_block[c]
             if it < nblk and full[it % stages].phase_done((it // stages) & 1):
-                moves.append(("consume", w))
+                moves.append(("consume", c))
         if not moves:
             break
         m = rnd.choice(moves)
@@ -87,18 +89,20 @@ def run_protocol(nblk, stages, warps, seed):
             empty[s].arrive()
             next_block[w] += warps
     assert produced == nblk and not in_flight
-    assert all(next_block[w] >= nblk for w in range(warps))
+    assert all(next_block[c] >= nblk for c in consumers)
 
 
-@pytest.mark.parametrize("stages", [8, 12])
-def test_kernel_stage_counts_are_safe(stages):
-    # The kernel uses 8 stages (16-bit caches, head_size 128) or 12, with 4 consumer warps.
+@pytest.mark.parametrize("stages,heads", [(8, 1), (16, 1), (8, 2), (16, 2)])
+def test_kernel_stage_counts_are_safe(stages, heads):
+    # The kernel uses 8 or 16 stages, 4 consumer warps per KV head, and one
+    # (16-bit caches) or two (E4M3) KV heads per CTA.
     for nblk in (1, 2, 3, 5, 8, 13, 32, 64):
-        for seed in range(200):
-            run_protocol(nblk, stages, 4, seed)
+        for seed in range(100):
+            run_protocol(nblk, stages, 4, seed, heads)
 
 
-def test_stage_count_not_a_multiple_of_warps_breaks():
+@pytest.mark.parametrize("heads", [1, 2])
+def test_stage_count_not_a_multiple_of_warps_breaks(heads):
     with pytest.raises(AssertionError):
         for seed in range(300):
-            run_protocol(8, 6, 4, seed)
+            run_protocol(8, 6, 4, seed, heads)
