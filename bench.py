@@ -263,18 +263,49 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(device)
     pa.pa_device_status(clear=True)
 
+    def steps_per_graph(n):
+        return max(d for d in range(1, min(n, 20) + 1) if n % d == 0)
+
+    def make_runner(fn, n):
+        """A callable that runs n steps of fn.  With graphs (the default) the
+        steps are captured once, a few per CUDA graph (so the kernels of
+        consecutive steps keep their programmatic-launch overlap), and the
+        graph is replayed: every replay runs every kernel of those steps again,
+        without the Python and launch overhead of issuing them one by one."""
+        if args.no_graph:
+            def run():
+                for _ in range(n):
+                    fn()
+            return run
+        spg = steps_per_graph(n)
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize(device)
+        with torch.cuda.graph(g):
+            for _ in range(spg):
+                fn()
+        g.replay()  # one untimed replay
+        torch.cuda.synchronize(device)
+        graphs.append(g)
+
+        def run():
+            for _ in range(n // spg):
+                g.replay()
+        return run
+
+    graphs = []  # kept alive until the end of the run
+
     def timed(path, n):
         """Time n steps of `path`: CUDA events only at the ends of the region
         (an event between kernels would cost time and break their
         programmatic-launch overlap).  Returns (ms per step, t0, t1)."""
         fn = S.append if path == "append" else S.step
+        run = make_runner(fn, n)
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize(device)
         t0 = time.time()
         start.record(stream)
-        for _ in range(n):
-            fn()
+        run()
         end.record(stream)
         torch.cuda.synchronize(device)
         barrier(world)
@@ -346,11 +377,11 @@ def run_ours(args, world, rank, local):
         for _ in range(args.warmup):
             e2e_step()
         torch.cuda.synchronize(device)
+        run_e2e = make_runner(e2e_step, n)
         s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         s2.record(stream)
-        for _ in range(n):
-            e2e_step()
+        run_e2e()
         e2.record(stream)
         torch.cuda.synchronize(device)
         barrier(world)
@@ -394,6 +425,8 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded N(0,1) K/V/q; no model weights)",
         "config": config_block(spec, W, {
             "step": args.path,
+            "launch": "stream" if args.no_graph else
+                      f"CUDA graph replay, {steps_per_graph(n)} steps per graph",
             "partition_tokens": S.partition_tokens,
             "l2": f"inputs larger than L2: {kv_bytes / 1e9:.3f} GB of KV read per step, no flush",
             "parallelism": f"replicas{world}" if world > 1 else "single GPU"}),
@@ -464,6 +497,8 @@ def main(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--ref-seconds", type=float, default=60.0)
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-graph", action="store_true",
+                   help="issue every call from Python instead of replaying captured steps")
     p.add_argument("--no-cpu-baseline", action="store_true")
     args = p.parse_args(argv)
     if args.warmup < 3:

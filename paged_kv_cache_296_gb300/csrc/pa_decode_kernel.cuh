@@ -153,17 +153,20 @@ __device__ __forceinline__ uint32_t token_mask(int tok, int valid) {
 // KV head group) -- each sequence has at least one item, so empty sequences
 // still get their zero output.  Items past the list's end exit at once.
 //
-// The plan is on every CTA's critical path, so it is a k-ary search: in each
-// round the CTA's warps test kWarps evenly spaced sizes at once (the count is
-// monotone in pb) and keep the interval where the test flips, one barrier per
-// round.  The interval starts narrow: with T blocks over V sequences,
-// count(pb) <= T / pb + V, so every pb >= kv_groups * T / (slots - kv_groups * V)
-// fits, while none below kv_groups * T / slots does; for a few long sequences
-// that is a window of a few dozen sizes, two or three rounds.
+// The plan is on every CTA's critical path, so it is a k-ary search: each
+// round tests evenly spaced sizes at once (the count is monotone in pb) and
+// keeps the interval where the test flips.  The interval starts narrow: with
+// T blocks over V sequences, count(pb) <= T / pb + V, so every
+// pb >= kv_groups * T / (slots - kv_groups * V) fits, while none below
+// kv_groups * T / slots does; for a few long sequences that is a window of a
+// few dozen sizes.  Up to 32 sequences, one warp does it all (a lane per
+// sequence and a lane per tested size, 32 sizes a round, no barrier inside);
+// beyond that the CTA's warps each test one size per round.
 constexpr int kMaxBalancedSeqs = 512;  // the host only picks the mode below this
 
 struct BalancedItem {
   int pb, seq, part, kvg;
+  int len;  // the sequence's context length (-1: not known here)
   bool valid;
 };
 
@@ -171,11 +174,87 @@ struct BalancedScratch {
   int nb[kMaxBalancedSeqs];  // blocks per sequence; -1: negative length (no item)
   int fits[2][32];           // per round parity, per warp
   int chunk[kMaxBalancedSeqs / 32];
-  int pick[2];
+  int pick[5];
 };
+
+__device__ __forceinline__ int parts_of(int n, int pbv) {
+  return n < 0 ? 0 : max(1, (n + pbv - 1) / pbv);
+}
+
+// Up to 32 sequences: warp 0 computes the plan, every thread reads it.
+__device__ __forceinline__ BalancedItem balanced_plan_small(const DecodeParams& p,
+                                                           BalancedScratch& sc) {
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) {
+    const int B = p.num_seqs;
+    const int L = lane < B ? p.context_lens[lane] : -1;
+    const int n = L > 0 ? (L + 15) >> 4 : (L == 0 ? 0 : -1);  // -1: no item
+    int total = max(n, 0), maxnb = n, nvalid = n >= 0 ? 1 : 0;
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) {
+      total += __shfl_xor_sync(0xffffffffu, total, x);
+      maxnb = max(maxnb, __shfl_xor_sync(0xffffffffu, maxnb, x));
+      nvalid += __shfl_xor_sync(0xffffffffu, nvalid, x);
+    }
+    // The window's ends in float, widened so rounding cannot cut the answer
+    // off: below lo nothing fits, from hi on everything does.
+    const float tg = (float)total * (float)p.kv_groups;
+    const float want = tg / (float)p.slots * 0.999f;
+    int lo = max(p.min_partition_blocks, (int)fminf(want, 1.0e9f));
+    int ub = maxnb;
+    const int spare = p.slots - nvalid * p.kv_groups;
+    if (spare > 0) ub = min(ub, (int)fminf(tg / (float)spare * 1.001f + 2.f, 1.0e9f));
+    int hi = max(lo, ub);
+    while (lo < hi) {
+      const int span = hi - lo;
+      const int c = lo + (int)((long long)span * (lane + 1) / 32);  // lane 31 tests hi
+      int cnt = 0;
+      for (int i = 0; i < B; ++i) cnt += parts_of(__shfl_sync(0xffffffffu, n, i), c);
+      const unsigned fit =
+          __ballot_sync(0xffffffffu, (long long)cnt * p.kv_groups <= p.slots);
+      const int w = __ffs(fit) - 1;  // lane 31 (hi) always fits
+      const int cw = __shfl_sync(0xffffffffu, c, w);
+      const int cprev = __shfl_sync(0xffffffffu, c, w > 0 ? w - 1 : 0);
+      hi = cw;
+      lo = w > 0 ? cprev + 1 : lo;
+    }
+    const int pb = lo;
+    const int mine = parts_of(n, pb);
+    int incl = mine;
+#pragma unroll
+    for (int x = 1; x < 32; x <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, x);
+      if (lane >= x) incl += o;
+    }
+    const int all = __shfl_sync(0xffffffffu, incl, 31);
+    const int q = blockIdx.x / p.kv_groups;
+    const int excl = incl - mine;
+    const unsigned hit = __ballot_sync(0xffffffffu, q >= excl && q < excl + mine);
+    if (lane == 0) {
+      sc.pick[0] = hit ? __ffs(hit) - 1 : -1;
+      sc.pick[2] = pb;
+      sc.pick[3] = all;
+    }
+    if (hit && lane == __ffs(hit) - 1) {
+      sc.pick[1] = q - excl;
+      sc.pick[4] = L;
+    }
+  }
+  __syncthreads();
+  BalancedItem it;
+  it.pb = sc.pick[2];
+  const int q = blockIdx.x / p.kv_groups;
+  it.valid = q < sc.pick[3] && sc.pick[0] >= 0;
+  it.seq = it.valid ? sc.pick[0] : 0;
+  it.part = it.valid ? sc.pick[1] : 0;
+  it.kvg = blockIdx.x % p.kv_groups;
+  it.len = it.valid ? sc.pick[4] : -1;
+  return it;
+}
 
 template <int kThreads>
 __device__ __forceinline__ BalancedItem balanced_plan(const DecodeParams& p, BalancedScratch& sc) {
+  if (p.num_seqs <= 32) return balanced_plan_small(p, sc);
   constexpr int kWarps = kThreads / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int B = p.num_seqs;
@@ -185,7 +264,6 @@ __device__ __forceinline__ BalancedItem balanced_plan(const DecodeParams& p, Bal
   }
   if (threadIdx.x == 0) sc.pick[0] = -1;
   __syncthreads();
-  auto parts_of = [](int n, int pbv) { return n < 0 ? 0 : max(1, (n + pbv - 1) / pbv); };
   // Every warp reduces the totals itself: no barrier needed.
   int total = 0, maxnb = 0, nvalid = 0;
   for (int i = lane; i < B; i += 32) {
@@ -263,6 +341,7 @@ __device__ __forceinline__ BalancedItem balanced_plan(const DecodeParams& p, Bal
   it.seq = it.valid ? sc.pick[0] : 0;
   it.part = it.valid ? sc.pick[1] : 0;
   it.kvg = blockIdx.x % p.kv_groups;
+  it.len = -1;
   return it;
 }
 
@@ -292,6 +371,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, DecodeCfg<D, KV>::
   griddep_wait();
   int kvg = blockIdx.x, part = blockIdx.y, seq = blockIdx.z;
   int pb = p.partition_blocks;
+  int L = -1;
   if (pb == 0) {
     __shared__ BalancedScratch plan_scratch;
     const BalancedItem item = balanced_plan<C::kThreads>(p, plan_scratch);
@@ -301,8 +381,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, DecodeCfg<D, KV>::
     kvg = item.kvg;
     part = item.part;
     seq = item.seq;
+    L = item.len;
   }
-  const int L = p.context_lens[seq];
+  if (L < 0) L = p.context_lens[seq];
   const int part_tokens = pb * 16;
   const int tok0 = part * part_tokens;
   if (part > 0 && tok0 >= L) return;  // past the end of this sequence

@@ -456,3 +456,22 @@ def test_fp8_odd_kv_head_counts(hkv, group, path, part):
                 live = ~e4m3.is_nan_code(opool)
                 assert np.array_equal(gpool[live], opool[live])
             H.assert_close(got[i, h * group:(h + 1) * group], want, spec, f"s{i} h{h}")
+
+
+@pytest.mark.parametrize("num_seqs", [1, 31, 32, 33, 100])
+def test_balanced_split_batch_sizes(num_seqs):
+    """Few (sequence, KV head) pairs: the kernel plans a balanced split from the
+    lengths (one warp up to 32 sequences, all warps above).  Every output must
+    match the oracle, including empty and one-token sequences."""
+    rng = np.random.default_rng(num_seqs)
+    lens = [int(x) for x in np.exp(rng.uniform(0, np.log(6000), num_seqs))]
+    if num_seqs == 1:
+        lens = [5000]
+    else:
+        lens[0], lens[1] = 0, 1
+        lens[-1] = 5000
+    spec = wl.Spec("balanced split", num_seqs, 8, 2, 64, "f16", "f16", ("fixed", lens),
+                   ("factor", 1.2))
+    W = wl.make_workload(spec, 500 + num_seqs, poison=True, table_garbage=True)
+    assert pa.pa_decode_partition_size(num_seqs, 2, W.max_blocks_per_seq) == 0  # balanced
+    _full_check(W)
