@@ -44,7 +44,8 @@ from paged_kv_cache_296_gb300 import workloads as wl  # noqa: E402
 METRIC = "paged-decode attended-KV GB/s (fraction of GB300 HBM peak); µs per decode step"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-KERNEL_SOURCES = ["pa_decode_kernel.cuh", "pa_ptx.cuh", "pa_decode_launch.cuh", "pa_api.cu"]
+KERNEL_SOURCES = ["pa_decode_kernel.cuh", "pa_ptx.cuh", "pa_decode_launch.cuh", "pa_api.cu",
+                  "pa_cache.cu"]
 
 
 # ---------------------------------------------------------------- helpers
