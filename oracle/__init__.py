@@ -21,7 +21,8 @@ Sources (four web pages on vLLM's PagedAttention):
 Modules:
   e4m3             -- OCP E4M3 encode (round-to-nearest-even, saturating) / decode.
   paged_attention  -- reshape_and_cache, block-table gather, paged decode,
-                      contiguous attention, split-KV partials and their merge.
+                      causal paged prefill, contiguous attention, split-KV
+                      partials and their merge.
 
 Every function is pinned by ``tests/test_oracle_*.py`` (run with
 ``-m "not gpu"``) against library routines, closed forms, invariants and the

@@ -232,6 +232,45 @@ def paged_decode_heads(q_bits, q_dtype, pool, block_tables, context_lens, scale,
 
 
 # --------------------------------------------------------------------------
+# Prefill / chunked prefill over the paged cache
+# --------------------------------------------------------------------------
+
+def paged_prefill(q_bits, q_dtype, pool, block_tables, context_lens, query_start_loc, scale,
+                  kv_dtype, kv_scale=1.0):
+    """Causal multi-query attention over the paged cache (a prefill step).
+
+    The pages schedule prefills beside decodes ("vLLM 部署深度指南", section
+    Continuous Batching, the scheduler sketch: a waiting sequence's prompt
+    tokens join the batch in one step) but do not spell out the attention; the
+    plainest reading is causal self-attention: a token at position ``p`` of a
+    sequence attends to that sequence's tokens ``0..p``.  For a chunk of the
+    prompt the chunk's ``n_i`` tokens are the last ``n_i`` of the ``L_i`` cached
+    ones (their K/V are written to the pool first, as for a decode step).
+
+    ``q_bits``: ``[T, Hq, D]`` raw bits, sequence ``i``'s queries in rows
+    ``query_start_loc[i] .. query_start_loc[i+1]-1`` at positions
+    ``L_i - n_i .. L_i - 1``.  Returns float64 ``[T, Hq, D]``.
+    """
+    block_size = pool.shape[1]
+    q = widen(q_bits, q_dtype)
+    out = np.zeros(q.shape, dtype=np.float64)
+    for i in range(len(context_lens)):
+        L = int(context_lens[i])
+        r0, r1 = int(query_start_loc[i]), int(query_start_loc[i + 1])
+        n = r1 - r0
+        assert 0 <= n <= L, "a sequence's query tokens are among its cached tokens"
+        if n == 0:
+            continue
+        kb, vb = gather_kv(pool, block_tables[i], L, block_size)
+        k = kv_values(kb, kv_dtype, kv_scale)
+        v = kv_values(vb, kv_dtype, kv_scale)
+        for t in range(n):
+            pos = L - n + t
+            out[r0 + t] = attention_contiguous(q[r0 + t], k[:pos + 1], v[:pos + 1], scale)
+    return out
+
+
+# --------------------------------------------------------------------------
 # Split-KV: partial attention over a token range and the log-sum-exp merge
 # --------------------------------------------------------------------------
 
