@@ -120,7 +120,9 @@ pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void
  * out, q        [num_seqs, num_q_heads, head_size] of q_dtype, contiguous.
  * block_tables  int32 [num_seqs, max_blocks_per_seq], row-major; entries past
  *               ceil(L / 16) are never read.
- * context_lens  int32 [num_seqs], 0 <= L <= max_blocks_per_seq * 16.
+ * context_lens  int32 [num_seqs], 0 <= L <= max_blocks_per_seq * 16 (a larger L
+ *               is cut to max_blocks_per_seq * 16, so no table entry past the
+ *               row is read; pa_check_tables reports such lengths).
  * num_blocks    number of blocks in the pool (bounds the loads).
  * partition_size  tokens per split-KV partition: 0 = library choice (see
  *               pa_decode_partition_size), else a multiple of 16.  Sequences longer than one partition are
@@ -207,6 +209,39 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const
                             int partition_size, void* stream);
 
 /*
+ * pa_prefill -- causal multi-query attention over the paged pool: a prefill
+ * (or a chunk of one) for every sequence of the batch.
+ *
+ * The pages schedule prefill steps beside decode steps ("vLLM 部署深度指南",
+ * section Continuous Batching, the scheduler sketch) and leave the attention
+ * itself to the plainest reading, causal self-attention: sequence i has
+ * L = context_lens[i] cached tokens, of which its n = query_start_loc[i+1] -
+ * query_start_loc[i] query tokens are the last n (positions L-n .. L-1, their
+ * K/V already written by pa_reshape_and_cache); the query at position p and
+ * query head h (KV head h / G, G = num_q_heads / num_kv_heads) gives
+ *   out[r, h, :] = softmax(scale * q[r, h, :] . K_i[0..p]^T) . V_i[0..p]
+ * for r = query_start_loc[i] + (p - (L - n)), with K_i / V_i read through the
+ * block table as in pa_decode.  A chunk of one token per sequence is a decode
+ * step.
+ *
+ * out, q           [T, num_q_heads, head_size] of dtype, T = query_start_loc[num_seqs];
+ *                  16-byte aligned, contiguous.
+ * query_start_loc  int32 [num_seqs + 1], non-decreasing, query_start_loc[0] = 0.
+ * max_query_len    >= every n (sizes the grid; the kernel checks it).
+ * block_tables, context_lens, num_blocks  as for pa_decode (n <= L <= max_blocks_per_seq * 16).
+ * dtype            PA_F16 or PA_BF16, shared by q, the cache and out (an E4M3
+ *                  cache returns PA_ERR_UNSUPPORTED).
+ * Rows of sequences whose n exceeds L or max_query_len are not written and the
+ * device status bit 2 is raised (pa_device_status).  Asynchronous on `stream`;
+ * no workspace.
+ */
+pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, const int32_t* context_lens,
+                     const int32_t* query_start_loc, int num_seqs, int max_query_len,
+                     int max_blocks_per_seq, int num_blocks, int num_q_heads, int num_kv_heads,
+                     int head_size, int block_size, float scale, pa_dtype dtype, void* stream);
+
+/*
  * pa_decode_workspace_size -- bytes of workspace pa_decode needs for these
  * arguments (0 when no sequence can span more than one partition).  Host only;
  * returns 0 and sets pa_last_error() for invalid arguments.
@@ -268,7 +303,8 @@ pa_status pa_check_tables(const int32_t* block_tables, const int32_t* context_le
 /*
  * pa_device_status -- error bits raised by kernels on the current device
  * instead of trapping (1 = a bounded wait inside a kernel timed out and the
- * kernel returned early; its outputs are then invalid).  Synchronises the
+ * kernel returned early; its outputs are then invalid; 2 = pa_prefill met a
+ * sequence whose query count exceeds its length or max_query_len).  Synchronises the
  * device.  `clear` != 0 resets the bits.  Returns 0xFFFFFFFF if the status
  * word cannot be read.
  */

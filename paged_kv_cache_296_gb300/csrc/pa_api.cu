@@ -150,6 +150,8 @@ pa_status decode_impl(const char* fn, void* out, const void* q, const void* k_ca
   if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "num_seqs %d exceeds 65535", num_seqs);
   if (max_blocks_per_seq <= 0)
     return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be > 0 (got %d)", max_blocks_per_seq);
+  if (max_blocks_per_seq > (1 << 26))
+    return fail(PA_ERR_UNSUPPORTED, "max_blocks_per_seq %d exceeds 2^26", max_blocks_per_seq);
   if ((st = check_block_size(block_size)) != PA_OK) return st;
   if ((st = check_head_size(head_size)) != PA_OK) return st;
   if ((st = check_pool(num_blocks, num_kv_heads)) != PA_OK) return st;
@@ -262,7 +264,7 @@ extern "C" {
 
 const char* pa_last_error(void) { return g_last_error.c_str(); }
 
-int pa_version(void) { return 100; }
+int pa_version(void) { return 110; }
 
 uint32_t pa_device_status(int clear) {
   unsigned* p = nullptr;
@@ -272,6 +274,71 @@ uint32_t pa_device_status(int clear) {
   if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return 0xFFFFFFFFu;
   if (clear && cudaMemset(p, 0, sizeof(unsigned)) != cudaSuccess) return 0xFFFFFFFFu;
   return v;
+}
+
+pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, const int32_t* context_lens,
+                     const int32_t* query_start_loc, int num_seqs, int max_query_len,
+                     int max_blocks_per_seq, int num_blocks, int num_q_heads, int num_kv_heads,
+                     int head_size, int block_size, float scale, pa_dtype dtype, void* stream) {
+  pa_status st;
+  if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs must be >= 0 (got %d)", num_seqs);
+  if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "num_seqs %d exceeds 65535", num_seqs);
+  if (max_query_len < 0)
+    return fail(PA_ERR_INVALID_ARG, "max_query_len must be >= 0 (got %d)", max_query_len);
+  if (max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be > 0 (got %d)", max_blocks_per_seq);
+  if (max_blocks_per_seq > (1 << 26))
+    return fail(PA_ERR_UNSUPPORTED, "max_blocks_per_seq %d exceeds 2^26", max_blocks_per_seq);
+  if ((st = check_block_size(block_size)) != PA_OK) return st;
+  if ((st = check_head_size(head_size)) != PA_OK) return st;
+  if ((st = check_pool(num_blocks, num_kv_heads)) != PA_OK) return st;
+  if (num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+                num_q_heads, num_kv_heads);
+  if (num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads exceeds 65535");
+  if (dtype == PA_E4M3)
+    return fail(PA_ERR_UNSUPPORTED, "pa_prefill reads 16-bit caches only (E4M3: not yet)");
+  if (dtype != PA_F16 && dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "dtype must be PA_F16 or PA_BF16");
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return fail(PA_ERR_INVALID_ARG, "scale must be finite");
+  if (num_seqs == 0 || max_query_len == 0) return ok();
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start_loc)
+    return fail(PA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "out, q, k_cache and v_cache must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(query_start_loc) & 3u))
+    return fail(PA_ERR_INVALID_ARG,
+                "block_tables, context_lens and query_start_loc must be 4-byte aligned");
+  if ((long long)max_query_len * (num_q_heads / num_kv_heads) > 0x7FFFFFFFll)
+    return fail(PA_ERR_UNSUPPORTED, "max_query_len too large");
+  pa::PrefillArgs a;
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.query_start_loc = query_start_loc;
+  a.num_seqs = num_seqs;
+  a.max_query_len = max_query_len;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_size = head_size;
+  a.dtype = dtype == PA_BF16 ? 1 : 0;
+  a.scale = scale;
+  cudaError_t e = pa::device_status_ptr(&a.status);
+  if (e != cudaSuccess) return cuda_fail(e, "status word");
+  const char* why = "launch failed";
+  e = pa::launch_prefill(a, static_cast<cudaStream_t>(stream), &why);
+  if (e == cudaErrorInvalidValue) return fail(PA_ERR_CUDA, "pa_prefill: %s", why);
+  if (e != cudaSuccess) return cuda_fail(e, "pa_prefill");
+  return ok();
 }
 
 pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
@@ -381,6 +448,8 @@ pa_status pa_gather_kv(void* k_out, void* v_out, const void* k_cache, const void
     return fail(PA_ERR_INVALID_ARG, "num_seqs must be in [0, 65535] (got %d)", num_seqs);
   if (max_blocks_per_seq <= 0)
     return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be > 0 (got %d)", max_blocks_per_seq);
+  if (max_blocks_per_seq > (1 << 26))
+    return fail(PA_ERR_UNSUPPORTED, "max_blocks_per_seq %d exceeds 2^26", max_blocks_per_seq);
   if ((st = check_block_size(block_size)) != PA_OK) return st;
   if ((st = check_head_size(head_size)) != PA_OK) return st;
   if ((st = check_pool(num_blocks, num_kv_heads)) != PA_OK) return st;

@@ -187,7 +187,7 @@ __device__ __forceinline__ BalancedItem balanced_plan_small(const DecodeParams& 
   const int lane = threadIdx.x & 31;
   if (threadIdx.x < 32) {
     const int B = p.num_seqs;
-    const int L = lane < B ? p.context_lens[lane] : -1;
+    const int L = lane < B ? min(p.context_lens[lane], p.max_blocks_per_seq * 16) : -1;
     const int n = L > 0 ? (L + 15) >> 4 : (L == 0 ? 0 : -1);  // -1: no item
     int total = max(n, 0), maxnb = n, nvalid = n >= 0 ? 1 : 0;
 #pragma unroll
@@ -259,7 +259,7 @@ __device__ __forceinline__ BalancedItem balanced_plan(const DecodeParams& p, Bal
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int B = p.num_seqs;
   for (int i = threadIdx.x; i < B; i += kThreads) {
-    const int L = p.context_lens[i];
+    const int L = min(p.context_lens[i], p.max_blocks_per_seq * 16);
     sc.nb[i] = L > 0 ? (L + 15) >> 4 : (L == 0 ? 0 : -1);
   }
   if (threadIdx.x == 0) sc.pick[0] = -1;
@@ -383,7 +383,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, DecodeCfg<D, KV>::
     seq = item.seq;
     L = item.len;
   }
-  if (L < 0) L = p.context_lens[seq];
+  // A length past the table's capacity is cut to it: no entry past the row is read.
+  if (L < 0) L = min(p.context_lens[seq], p.max_blocks_per_seq * 16);
   const int part_tokens = pb * 16;
   const int tok0 = part * part_tokens;
   if (part > 0 && tok0 >= L) return;  // past the end of this sequence
@@ -819,7 +820,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 
   const int idx = blockIdx.x;  // sequence * num_q_heads + query head
   const int seq = idx / p.num_q_heads;
-  const int L = p.context_lens[seq];
+  const int L = min(p.context_lens[seq], p.max_blocks_per_seq * 16);
   // The kernel before this one is always the same call's attention kernel,
   // which writes no lengths: they may be read before the wait.  A balanced
   // split never cuts a sequence shorter than its minimum partition.

@@ -47,6 +47,29 @@ cudaError_t launch_decode_f16(const DecodeArgs& a, cudaStream_t stream, const ch
 cudaError_t launch_decode_bf16(const DecodeArgs& a, cudaStream_t stream, const char** why);
 cudaError_t launch_decode_e4m3(const DecodeArgs& a, cudaStream_t stream, const char** why);
 
+// Everything one pa_prefill launch needs, already validated by the caller.
+struct PrefillArgs {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* query_start_loc;
+  int num_seqs;
+  int max_query_len;
+  int max_blocks_per_seq;
+  int num_blocks;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_size;
+  int dtype;  // 0 f16, 1 bf16 (q, cache and out)
+  float scale;
+  unsigned* status;
+};
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, const char** why);
+
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
                                      const int64_t* slot_mapping, int64_t n_tokens,
                                      int64_t src_stride_bytes, int64_t max_slot, int hkv_d,

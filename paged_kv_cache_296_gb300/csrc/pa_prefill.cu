@@ -1,0 +1,83 @@
+// Host launcher for the paged prefill kernel (fp16 / bf16, head_size 64 / 128).
+#include <algorithm>
+#include <atomic>
+
+#include <cuda_runtime.h>
+
+#include "pa_internal.h"
+#include "pa_prefill_kernel.cuh"
+
+namespace pa {
+namespace {
+
+template <int D, int QT>
+cudaError_t launch_prefill_instance(const PrefillArgs& a, cudaStream_t stream, const char** why) {
+  using C = PrefillCfg<D>;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  const long long tiles = ((long long)a.max_query_len * G + C::kRows - 1) / C::kRows;
+  if (tiles == 0 || a.num_seqs == 0) return cudaSuccess;
+  if (tiles > 0x7FFFFFFFll) {
+    *why = "max_query_len * heads per KV head is too large";
+    return cudaErrorInvalidValue;
+  }
+  alignas(64) CUtensorMap tk;
+  alignas(64) CUtensorMap tv;
+  if (!encode_kv_tensor_map(&tk, a.k_cache, a.num_blocks, a.num_kv_heads, D, 2, 1, why) ||
+      !encode_kv_tensor_map(&tv, a.v_cache, a.num_blocks, a.num_kv_heads, D, 2, 1, why)) {
+    return cudaErrorInvalidValue;
+  }
+  // Opt in to more than 48 KB of dynamic shared memory, once per device.
+  static std::atomic<unsigned long long> attr_done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(paged_prefill_kernel<D, QT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  PrefillParams p;
+  p.out = a.out;
+  p.q = a.q;
+  p.block_tables = a.block_tables;
+  p.context_lens = a.context_lens;
+  p.query_start_loc = a.query_start_loc;
+  p.status = a.status;
+  p.num_seqs = a.num_seqs;
+  p.max_query_len = a.max_query_len;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_blocks = a.num_blocks;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.group = G;
+  p.tiles = (int)tiles;
+  p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
+  // Programmatic stream serialisation: the grid may start while the kernel
+  // before it drains (every thread waits for it before reading inputs).
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)tiles, (unsigned)a.num_kv_heads, (unsigned)a.num_seqs);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, paged_prefill_kernel<D, QT>, tk, tv, p);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, const char** why) {
+  if (a.dtype == 0) {
+    if (a.head_size == 64) return launch_prefill_instance<64, 0>(a, stream, why);
+    return launch_prefill_instance<128, 0>(a, stream, why);
+  }
+  if (a.head_size == 64) return launch_prefill_instance<64, 1>(a, stream, why);
+  return launch_prefill_instance<128, 1>(a, stream, why);
+}
+
+}  // namespace pa

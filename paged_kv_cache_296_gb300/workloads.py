@@ -262,3 +262,134 @@ def random_spec(seed, head_size=None, group=None, kv_dtype=None, max_len=70, max
     lens[0] = max(lens[0], 1)
     return Spec(f"random seed {seed}", B, hkv * g, hkv, d, qd, kvd, ("fixed", lens),
                 ("factor", 1.5), partition_size=int(r.choice([16, 32, 64, 512])))
+
+
+# --------------------------------------------------------------------------
+# Prefill (a prompt, or a chunk of one, per sequence)
+# --------------------------------------------------------------------------
+
+@dataclass
+class PrefillSpec:
+    """Shape of one synthetic prefill batch.
+
+    ``context``: the sequences' lengths after the step, ``("fixed", [..])`` or
+    ``("uniform", lo, hi)``.  ``query``: how many of each sequence's last tokens
+    are this step's queries: ``("all",)`` (a whole prompt), ``("chunk", n)``
+    (min(n, L) tokens: chunked prefill over an already cached prefix) or
+    ``("fixed", [..])``.
+    """
+    name: str
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_size: int
+    dtype: str                        # "f16" | "bf16" (q, cache, out)
+    context: tuple
+    query: tuple
+    pool: tuple = ("factor", 1.25)
+    block_size: int = BLOCK_SIZE
+
+
+#: Prefill workloads (Llama-3-8B-shaped heads).  Seeds 11.. belong to them.
+PREFILL_SPECS = {
+    1: PrefillSpec("prefill: 4 prompts of 2048 tokens, 32/8 heads, d128, bf16",
+                   4, 32, 8, 128, "bf16", ("fixed", [2048] * 4), ("all",)),
+    2: PrefillSpec("chunked prefill: 16 seqs, context U[2048,8192], 512-token chunks, "
+                   "32/8 heads, d128, bf16",
+                   16, 32, 8, 128, "bf16", ("uniform", 2048, 8192), ("chunk", 512)),
+}
+
+
+@dataclass
+class PrefillWorkload:
+    """One prefill step's inputs.  ``pool`` is the cache before the step's write
+    of the query tokens' K/V (``k_new``/``v_new`` at ``slot_mapping``)."""
+    spec: PrefillSpec
+    seed: int
+    context_lens: torch.Tensor        # int32 [B]
+    query_start_loc: torch.Tensor     # int32 [B + 1]
+    block_tables: torch.Tensor        # int32 [B, max_blocks]
+    num_blocks: int
+    pool: torch.Tensor                # [NB, BS, 2, Hkv, D]
+    q: torch.Tensor                   # [T, Hq, D]
+    k_new: torch.Tensor               # [T, Hkv, D]
+    v_new: torch.Tensor               # [T, Hkv, D]
+    slot_mapping: torch.Tensor        # int64 [T]
+    scale: float
+
+    @property
+    def max_blocks_per_seq(self):
+        return self.block_tables.shape[1]
+
+    @property
+    def max_query_len(self):
+        qsl = self.query_start_loc.cpu()
+        return int((qsl[1:] - qsl[:-1]).max()) if len(qsl) > 1 else 0
+
+
+def make_prefill_workload(spec, seed, device="cpu", poison=False):
+    """Draw one prefill step for ``spec``.
+
+    Draw order: context lengths -> query counts -> block permutation -> pool ->
+    q -> the query tokens' k/v.  ``poison``: NaN in every slot the step must
+    not read before writing it (free blocks, tails, the query tokens' own
+    slots, which the step's write fills).
+    """
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    bs = spec.block_size
+    hkv, d = spec.num_kv_heads, spec.head_size
+    B = spec.num_seqs
+    if spec.context[0] == "fixed":
+        lens = np.array(spec.context[1], dtype=np.int64)
+    else:
+        lens = torch.randint(spec.context[1], spec.context[2] + 1, (B,), generator=gen).numpy()
+        lens = lens.astype(np.int64)
+    assert len(lens) == B
+    if spec.query[0] == "all":
+        nq = lens.copy()
+    elif spec.query[0] == "chunk":
+        nq = np.minimum(lens, spec.query[1])
+    else:
+        nq = np.array(spec.query[1], dtype=np.int64)
+    assert np.all((nq >= 0) & (nq <= lens))
+    qsl = np.concatenate([[0], np.cumsum(nq)]).astype(np.int64)
+    T = int(qsl[-1])
+
+    nblk = [_ceil_div(int(L), bs) for L in lens]
+    max_blocks = max(1, max(nblk))
+    needed = sum(nblk)
+    num_blocks = spec.pool[1] if spec.pool[0] == "fixed" else int(math.ceil(spec.pool[1] * needed))
+    num_blocks = max(num_blocks, needed, 1)
+    perm = torch.randperm(num_blocks, generator=gen).numpy().astype(np.int64)
+    tables = np.full((B, max_blocks), -1, dtype=np.int64)
+    nxt = 0
+    for i in range(B):
+        tables[i, :nblk[i]] = perm[nxt:nxt + nblk[i]]
+        nxt += nblk[i]
+
+    slots = np.empty(T, dtype=np.int64)
+    for i in range(B):
+        for t in range(int(nq[i])):
+            pos = int(lens[i] - nq[i] + t)
+            slots[qsl[i] + t] = tables[i, pos // bs] * bs + pos % bs
+
+    shape = (num_blocks, bs, 2, hkv, d)
+    dt = TORCH_DTYPE[spec.dtype]
+    pool = _randn(shape, dt, gen, device)
+    if poison:
+        live = np.zeros((num_blocks, bs), dtype=bool)
+        for i in range(B):
+            for j in range(int(lens[i] - nq[i])):
+                live[tables[i, j // bs], j % bs] = True
+        pool[torch.from_numpy(~live).to(device)] = float("nan")
+    q = _randn((T, spec.num_q_heads, d), dt, gen, device)
+    k_new = _randn((T, hkv, d), dt, gen, device)
+    v_new = _randn((T, hkv, d), dt, gen, device)
+    return PrefillWorkload(
+        spec=spec, seed=seed,
+        context_lens=torch.from_numpy(lens.astype(np.int32)).to(device),
+        query_start_loc=torch.from_numpy(qsl.astype(np.int32)).to(device),
+        block_tables=torch.from_numpy(tables.astype(np.int32)).to(device),
+        num_blocks=num_blocks, pool=pool, q=q, k_new=k_new, v_new=v_new,
+        slot_mapping=torch.from_numpy(slots).to(device), scale=1.0 / math.sqrt(d))

@@ -185,3 +185,36 @@ def test_decode_append_requires_token_buffers(lib):
     assert lib.pa_decode_append(*a) == 1
     a = [args[0], args[1], FAKE, FAKE, ctypes.c_void_p(0x10004), 0] + args[2:]
     assert lib.pa_decode_append(*a) == 1
+
+
+def prefill_args(**over):
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, qsl=FAKE, B=4, mq=64, mb=8, nb=64,
+             hq=8, hkv=2, d=128, bs=16, scale=0.1, dt=pa.PA_F16, stream=NULL)
+    a.update(over)
+    return [a[k] for k in ("out", "q", "k", "v", "bt", "cl", "qsl", "B", "mq", "mb", "nb", "hq",
+                           "hkv", "d", "bs", "scale", "dt", "stream")]
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(out=NULL), 1),
+    (dict(qsl=NULL), 1),
+    (dict(q=MISALIGNED), 1),
+    (dict(qsl=ctypes.c_void_p(0x10002)), 1),
+    (dict(d=96), 2),
+    (dict(bs=32), 2),
+    (dict(hq=6, hkv=4), 1),
+    (dict(dt=pa.PA_E4M3), 2),            # 16-bit caches only
+    (dict(dt=pa.PA_F32), 2),
+    (dict(scale=float("inf")), 1),
+    (dict(mq=-1), 1),
+    (dict(B=-1), 1),
+    (dict(nb=0), 1),
+])
+def test_prefill_rejects_bad_arguments(lib, over, status):
+    assert lib.pa_prefill(*prefill_args(**over)) == status
+    assert pa.pa_last_error() != ""
+
+
+def test_prefill_without_queries_is_a_no_op(lib):
+    assert lib.pa_prefill(*prefill_args(mq=0, out=NULL, q=NULL)) == 0
+    assert lib.pa_prefill(*prefill_args(B=0, out=NULL, q=NULL)) == 0

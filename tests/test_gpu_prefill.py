@@ -1,0 +1,172 @@
+"""Paged prefill on the GPU against the float64 oracle (GB300).
+
+Each case writes the step's query tokens' K/V into the pool with
+pa_reshape_and_cache (bit-exact against the oracle's write), then runs
+pa_prefill and compares every output with ``oracle.paged_prefill`` on the
+oracle's own pool.  Unused and not-yet-written slots hold NaN, so a stray read
+shows up.  Full-size workloads are checked on sampled rows: the query at
+position p of a sequence is the last query of that sequence cut to p + 1
+tokens, which the oracle computes on its own.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import paged_attention as ref
+from paged_kv_cache_296_gb300 import binding as pa
+from paged_kv_cache_296_gb300 import workloads as wl
+
+from harness import ATOL, ULP1, bits_of
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_prefill(W):
+    dev = "cuda"
+    pool = W.pool.to(dev, copy=True)
+    kc, vc = pa.kv_views(pool)
+    if W.q.shape[0]:
+        pa.pa_reshape_and_cache(W.k_new.to(dev), W.v_new.to(dev), kc, vc, W.slot_mapping.to(dev))
+    out = torch.full(W.q.shape, float("nan"), dtype=W.q.dtype, device=dev)
+    pa.pa_prefill(out, W.q.to(dev), kc, vc, W.block_tables.to(dev), W.context_lens.to(dev),
+                  W.query_start_loc.to(dev), W.max_query_len, W.scale)
+    return out, pool
+
+
+def oracle_pool(W):
+    d = W.spec.dtype
+    return ref.reshape_and_cache(bits_of(W.pool.cpu()), bits_of(W.k_new.cpu()),
+                                 bits_of(W.v_new.cpu()), W.slot_mapping.cpu().numpy(), d, d)
+
+
+def check_close(got, want, dtype, what):
+    bound = np.maximum(ATOL[dtype],
+                       ULP1[dtype] * np.exp2(np.floor(np.log2(np.maximum(np.abs(want), 1e-30)))))
+    err = np.abs(got - want)
+    bad = ~(err <= bound)
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance, max err "
+                           f"{np.nanmax(err):.3e} at {np.argwhere(bad)[:3].tolist()}")
+
+
+def full_check(W):
+    out, pool = gpu_prefill(W)
+    opool = oracle_pool(W)
+    assert np.array_equal(bits_of(pool.cpu()), opool), "pool after the write differs"
+    got = ref.widen(bits_of(out.cpu()), W.spec.dtype)
+    assert np.isfinite(got).all(), "NaN output: a slot not yet written or unused was read"
+    want = ref.paged_prefill(bits_of(W.q.cpu()), W.spec.dtype, opool, W.block_tables.cpu().numpy(),
+                             W.context_lens.cpu().numpy(), W.query_start_loc.cpu().numpy(),
+                             W.scale, W.spec.dtype)
+    check_close(got, want, W.spec.dtype, W.spec.name)
+
+
+def random_prefill_spec(seed):
+    r = np.random.default_rng(seed)
+    d = int(r.choice([64, 128]))
+    g = int(r.choice([1, 2, 3, 4, 8]))
+    hkv = int(r.choice([1, 2, 3]))
+    dt = str(r.choice(["f16", "bf16"]))
+    B = int(r.integers(1, 5))
+    lens = [int(x) for x in r.integers(1, 160, B)]
+    kind = r.integers(0, 3)
+    if kind == 0:
+        nq = lens                                            # whole prompts
+    elif kind == 1:
+        nq = [int(r.integers(0, L + 1)) for L in lens]       # chunks over cached prefixes
+    else:
+        nq = [min(L, int(r.choice([1, 15, 16, 17, 64]))) for L in lens]
+    return wl.PrefillSpec(f"random prefill {seed}", B, hkv * g, hkv, d, dt, ("fixed", lens),
+                          ("fixed", nq), ("factor", 1.5))
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_shapes(seed):
+    W = wl.make_prefill_workload(random_prefill_spec(seed), 3000 + seed, poison=True)
+    full_check(W)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("head_size,group", [(128, 1), (128, 4), (64, 8), (128, 6)])
+def test_tile_edges(dtype, head_size, group):
+    # query counts around the 64-row tile and the 16-token block
+    lens = [63, 64, 65, 200, 129, 16, 1]
+    nq = [63, 64, 65, 130, 1, 16, 1]
+    spec = wl.PrefillSpec("tile edges", len(lens), 2 * group, 2, head_size, dtype,
+                          ("fixed", lens), ("fixed", nq), ("factor", 1.3))
+    full_check(wl.make_prefill_workload(spec, 71, poison=True))
+
+
+def test_one_query_per_sequence_matches_decode():
+    # A chunk of one token per sequence is a decode step: both kernels agree
+    # within the tolerance (they round differently).
+    spec = wl.PrefillSpec("decode-shaped", 6, 32, 8, 128, "bf16",
+                          ("fixed", [1, 17, 300, 1000, 33, 2048]), ("chunk", 1))
+    W = wl.make_prefill_workload(spec, 5)
+    out, pool = gpu_prefill(W)
+    kc, vc = pa.kv_views(pool)
+    dec = torch.empty_like(out)
+    pa.pa_decode(dec, W.q.cuda(), kc, vc, W.block_tables.cuda(), W.context_lens.cuda(), W.scale)
+    a = out.float().cpu().numpy()
+    b = dec.float().cpu().numpy()
+    assert np.abs(a - b).max() <= 2 * ATOL["bf16"]
+
+
+@pytest.mark.parametrize("n", sorted(wl.PREFILL_SPECS))
+def test_full_size_sampled_rows(n):
+    W = wl.make_prefill_workload(wl.PREFILL_SPECS[n], 10 + n, device="cuda")
+    out, pool = gpu_prefill(W)
+    dt = W.spec.dtype
+    got_all = ref.widen(bits_of(out.cpu()), dt)
+    assert np.isfinite(got_all).all()
+    lens = W.context_lens.cpu().numpy()
+    qsl = W.query_start_loc.cpu().numpy()
+    tables = W.block_tables.cpu().numpy()
+    rng = np.random.default_rng(n)
+    for i in range(W.spec.num_seqs):
+        nq = int(qsl[i + 1] - qsl[i])
+        L = int(lens[i])
+        for t in sorted({0, nq - 1, int(rng.integers(nq)), int(rng.integers(nq))}):
+            pos = L - nq + t
+            nb = pos // 16 + 1
+            blocks = tables[i, :nb].astype(np.int64)
+            # the sequence cut to pos + 1 tokens; its one query is the last token
+            sub = bits_of(pool[torch.from_numpy(blocks).cuda()].cpu())
+            want = ref.paged_prefill(bits_of(W.q[qsl[i] + t:qsl[i] + t + 1].cpu()), dt, sub,
+                                     np.arange(nb)[None, :], np.array([pos + 1]),
+                                     np.array([0, 1]), W.scale, dt)
+            check_close(got_all[qsl[i] + t][None], want, dt, f"seq {i} token {t}")
+
+
+def test_run_to_run_bitwise_deterministic():
+    W = wl.make_prefill_workload(wl.PREFILL_SPECS[2], 12, device="cuda")
+    first, _ = gpu_prefill(W)
+    for _ in range(3):
+        again, _ = gpu_prefill(W)
+        assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+
+
+def test_bad_query_layout_is_reported_and_skipped():
+    # Sequence 1 claims more queries than it has tokens: its rows stay untouched,
+    # the device status raises bit 2, the other sequences are still right.
+    spec = wl.PrefillSpec("bad layout", 3, 8, 2, 64, "f16", ("fixed", [30, 10, 40]),
+                          ("fixed", [30, 10, 40]))
+    W = wl.make_prefill_workload(spec, 8)
+    opool = oracle_pool(W)
+    want = ref.paged_prefill(bits_of(W.q), "f16", opool, W.block_tables.numpy(),
+                             W.context_lens.numpy(), W.query_start_loc.numpy(), W.scale, "f16")
+    W.context_lens[1] = 5                      # now 10 queries > 5 tokens
+    pa.pa_device_status(clear=True)
+    out, _ = gpu_prefill(W)
+    assert pa.pa_device_status(clear=True) & 2
+    got = ref.widen(bits_of(out.cpu()), "f16")
+    assert np.isnan(got[30:40]).all(), "rows of the rejected sequence were written"
+    check_close(got[:30], want[:30], "f16", "seq 0")
+    check_close(got[40:], want[40:], "f16", "seq 2")
+
+
+def test_empty_batch_and_no_queries_are_no_ops():
+    spec = wl.PrefillSpec("no queries", 2, 4, 4, 64, "f16", ("fixed", [20, 9]), ("fixed", [0, 0]))
+    W = wl.make_prefill_workload(spec, 9)
+    out, _ = gpu_prefill(W)
+    assert out.numel() == 0
