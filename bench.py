@@ -43,6 +43,8 @@ from paged_kv_cache_296_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "paged-decode attended-KV GB/s (fraction of GB300 HBM peak); µs per decode step"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+PREFILL_METRIC = "paged-prefill TFLOP/s (causal attention FLOPs); µs per prefill step"
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = ["pa_decode_kernel.cuh", "pa_ptx.cuh", "pa_decode_launch.cuh", "pa_api.cu",
                   "pa_cache.cu"]
@@ -91,6 +93,16 @@ def hbm_peak():
         return v, "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 tensor-core peak (TFLOP/s): the measured cuBLAS burst figure."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured bf16_tflops (burst)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback bf16"
 
 
 def kernel_source_hash():
@@ -451,6 +463,207 @@ def run_ours(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
+def prefill_oracle_sample(W, seconds):
+    """Time the float64 oracle on query rows of a prefill batch (all heads of
+    each row), spread over its sequences, until ``seconds`` of CPU work.
+    Returns (flops, seconds, rows)."""
+    from oracle import paged_attention as ref
+    spec = W.spec
+    dt = spec.dtype
+    lens = W.context_lens.cpu().numpy()
+    qsl = W.query_start_loc.cpu().numpy()
+    tables = W.block_tables.cpu().numpy()
+    q_bits = W.q.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    pool = W.pool.cpu()
+    # the oracle's pool after the step's write
+    pbits = ref.reshape_and_cache(pool.view(torch.int16).numpy().view(np.uint16),
+                                  W.k_new.cpu().view(torch.int16).numpy().view(np.uint16),
+                                  W.v_new.cpu().view(torch.int16).numpy().view(np.uint16),
+                                  W.slot_mapping.cpu().numpy(), dt, dt)
+    rng = np.random.default_rng(0)
+    flops, elapsed, rows = 0, 0.0, 0
+    while elapsed < seconds:
+        i = int(rng.integers(spec.num_seqs))
+        n = int(qsl[i + 1] - qsl[i])
+        if n == 0:
+            continue
+        t_ = int(rng.integers(n))
+        pos = int(lens[i]) - n + t_
+        nb = pos // 16 + 1
+        sub = pbits[tables[i, :nb].astype(np.int64)]
+        t0 = time.perf_counter()
+        ref.paged_prefill(q_bits[qsl[i] + t_:qsl[i] + t_ + 1], dt, sub, np.arange(nb)[None, :],
+                          np.array([pos + 1]), np.array([0, 1]), W.scale, dt)
+        elapsed += time.perf_counter() - t0
+        flops += 4 * spec.head_size * spec.num_q_heads * (pos + 1)
+        rows += 1
+    return flops, elapsed, rows
+
+
+def run_prefill(args, world, rank, local):
+    """The prefill leg: one step = the write of the query tokens' K/V plus
+    pa_prefill over a seeded prefill batch; value = causal attention TFLOP/s."""
+    from paged_kv_cache_296_gb300 import binding as pa
+    from paged_kv_cache_296_gb300.runner import PrefillStep, prefill_flops
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    pa.load()
+    spec = wl.PREFILL_SPECS[args.prefill]
+    W = wl.make_prefill_workload(spec, 10 + args.prefill + 1000 * rank, device=str(device))
+    S = PrefillStep(W, device=device)
+    flops = prefill_flops(W)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        S.step()
+    torch.cuda.synchronize(device)
+    pa.pa_device_status(clear=True)
+    n = args.steps
+    graphs = []
+
+    def runner(fn):
+        if args.no_graph:
+            def run():
+                for _ in range(n):
+                    fn()
+            return run, "stream"
+        spg = max(d for d in range(1, min(n, 20) + 1) if n % d == 0)
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize(device)
+        with torch.cuda.graph(g):
+            for _ in range(spg):
+                fn()
+        g.replay()
+        torch.cuda.synchronize(device)
+        graphs.append(g)
+
+        def run():
+            for _ in range(n // spg):
+                g.replay()
+        return run, f"CUDA graph replay, {spg} steps per graph"
+
+    def timed(run):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(device)
+        t0 = time.time()
+        a.record(stream)
+        run()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+        return a.elapsed_time(b) / n, t0, time.time()
+
+    run, launch = runner(S.step)
+    sampler = ClockSampler(device.index)
+    sampler.start()
+    time.sleep(0.3)
+    ms_local, t0, t1 = timed(run)
+    sampler.stop()
+    ms_step = max_over_ranks(ms_local, world, device)
+    status = pa.pa_device_status(clear=True)
+    if status != 0:
+        raise RuntimeError(f"device status {status:#x}")
+    # the attention kernel alone (the write is a small share of the step)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    S.step()
+    torch.cuda.synchronize(device)
+    ev[0].record(stream)
+    for _ in range(min(n, 50)):
+        pa.pa_prefill(S.out, S.q, S.k_cache, S.v_cache, S.block_tables, S.context_lens,
+                      S.query_start_loc, S.max_query_len, S.scale)
+    ev[1].record(stream)
+    torch.cuda.synchronize(device)
+    attn_ms = ev[0].elapsed_time(ev[1]) / min(n, 50)
+
+    e2e = None
+    if not args.no_e2e:
+        host_in, dev_in = S.stage_inputs()
+        out_host = torch.empty(S.out.shape, dtype=S.out.dtype).pin_memory()
+
+        def e2e_step():
+            dev_in.copy_(host_in, non_blocking=True)
+            S.step()
+            out_host.copy_(S.out, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        run_e2e, _ = runner(e2e_step)
+        e_ms, _, _ = timed(run_e2e)
+        e_ms = max_over_ranks(e_ms, world, device)
+        e2e = {"value": round(sum_over_ranks(flops, world, device) / (e_ms * 1e-3) / 1e12, 2),
+               "unit": "TFLOP/s", "ms_per_step": round(e_ms, 5),
+               "h2d_bytes_per_step": host_in.numel(),
+               "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f, secs, rows = prefill_oracle_sample(W, args.cpu_seconds)
+        cpu = {"value": round(f / secs / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"float64 NumPy oracle, {rows} query rows (all heads) of this batch, "
+                         f"{secs:.1f} s, 1 BLAS thread"}
+    peak, peak_kind = tensor_peak()
+    value = sum_over_ranks(flops, world, device) / (ms_step * 1e-3) / 1e12
+    achieved = flops / (attn_ms * 1e-3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": n, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "us_per_step": round(ms_step * 1e3, 2), "us_prefill_call": round(attn_ms * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": spec.dtype, "data": "synthetic (seeded N(0,1) K/V/q; no model weights)",
+        "config": {"workload": spec.name, "num_seqs": spec.num_seqs,
+                   "num_q_heads": spec.num_q_heads, "num_kv_heads": spec.num_kv_heads,
+                   "head_size": spec.head_size, "block_size": 16,
+                   "query_tokens": int(W.q.shape[0]), "max_query_len": S.max_query_len,
+                   "mean_context": float(W.context_lens.float().mean()),
+                   "step": "pa_reshape_and_cache of the query tokens + pa_prefill",
+                   "launch": launch, "l2": "K/V re-read by a sequence's tiles comes from L2",
+                   "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "kernel": "paged_prefill_kernel (mma.sync m16n8k16)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "algorithmic_flops_per_launch": flops, "traffic": None},
+        "gpu_launches": S.launches_per_step * n,
+        "e2e": e2e, "cpu_baseline": cpu,
+        "clocks": sampler.summary(t0, t1),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference_prefill(args, world, rank, local):
+    """The CPU oracle on a prefill workload: rank 0 alone, a bounded sample per step."""
+    if rank != 0:
+        return
+    spec = wl.PREFILL_SPECS[args.prefill]
+    W = wl.make_prefill_workload(spec, 10 + args.prefill, device="cpu")
+    per_step = max(1.0, args.ref_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        prefill_oracle_sample(W, per_step)
+    tot_f, tot_s, rows = 0, 0.0, 0
+    for _ in range(args.steps):
+        f, sec, r = prefill_oracle_sample(W, per_step)
+        tot_f, tot_s, rows = tot_f + f, tot_s + sec, rows + r
+    value = tot_f / tot_s / 1e12
+    cpu = {"value": round(value, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+           "sample": f"float64 NumPy oracle, {rows} query rows over {args.steps} steps "
+                     f"({tot_s:.1f} s), 1 BLAS thread"}
+    print(json.dumps({
+        "impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) K/V/q; no model weights)",
+        "config": {"workload": spec.name, "parallelism": "host cores, one thread"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
 def run_reference(args, world, rank, local):
     """The CPU oracle as the reference arm: rank 0 alone, a bounded sample per step."""
     if rank != 0:
@@ -501,11 +714,17 @@ def main(argv=None):
     p.add_argument("--no-graph", action="store_true",
                    help="issue every call from Python instead of replaying captured steps")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--prefill", type=int, default=0, choices=[0] + sorted(wl.PREFILL_SPECS),
+                   help="time a prefill workload (pa_prefill) instead of the decode step")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
     world, rank, local = dist_env()
-    if args.impl == "reference":
+    if args.prefill and args.impl == "ours":
+        run_prefill(args, world, rank, local)
+    elif args.prefill:
+        run_reference_prefill(args, world, rank, local)
+    elif args.impl == "reference":
         run_reference(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)

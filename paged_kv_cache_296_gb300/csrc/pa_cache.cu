@@ -71,6 +71,39 @@ EncodeTiledFn encode_fn() {
 }
 }  // namespace
 
+bool encode_kv_tensor_map_planes(void* desc, const void* base, int num_blocks, int num_kv_heads,
+                                 int head_size, int elt_bytes, const char** why) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    *why = "cuTensorMapEncodeTiled is not available from the driver";
+    return false;
+  }
+  const cuuint64_t row = (cuuint64_t)head_size * elt_bytes;
+  if (row % 128 != 0) {
+    *why = "128-byte planes need rows of a multiple of 128 bytes";
+    return false;
+  }
+  const cuuint64_t token_stride = 2ull * num_kv_heads * row;
+  const cuuint64_t ntok = (cuuint64_t)num_blocks * 16;
+  const CUtensorMapDataType dt =
+      elt_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  // dims (elements of a 128-byte piece, token rows, pieces of a row, kv heads):
+  // a box lands as [piece][token][128 B], each piece a 16-row swizzled tile.
+  const cuuint64_t dims[4] = {128ull / elt_bytes, ntok, row / 128, (cuuint64_t)num_kv_heads};
+  const cuuint64_t strides[3] = {token_stride, 128ull, row};
+  const cuuint32_t box[4] = {128u / elt_bytes, 16u, (cuuint32_t)(row / 128), 1u};
+  const cuuint32_t es[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = fn(static_cast<CUtensorMap*>(desc), dt, 4, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *why = "cuTensorMapEncodeTiled rejected the plane view of the KV pool";
+    return false;
+  }
+  return true;
+}
+
 bool encode_kv_tensor_map(void* desc, const void* base, int num_blocks, int num_kv_heads,
                           int head_size, int elt_bytes, int box_heads, const char** why) {
   EncodeTiledFn fn = encode_fn();

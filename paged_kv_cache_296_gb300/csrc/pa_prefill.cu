@@ -22,8 +22,8 @@ cudaError_t launch_prefill_instance(const PrefillArgs& a, cudaStream_t stream, c
   }
   alignas(64) CUtensorMap tk;
   alignas(64) CUtensorMap tv;
-  if (!encode_kv_tensor_map(&tk, a.k_cache, a.num_blocks, a.num_kv_heads, D, 2, 1, why) ||
-      !encode_kv_tensor_map(&tv, a.v_cache, a.num_blocks, a.num_kv_heads, D, 2, 1, why)) {
+  if (!encode_kv_tensor_map_planes(&tk, a.k_cache, a.num_blocks, a.num_kv_heads, D, 2, why) ||
+      !encode_kv_tensor_map_planes(&tv, a.v_cache, a.num_blocks, a.num_kv_heads, D, 2, why)) {
     return cudaErrorInvalidValue;
   }
   // Opt in to more than 48 KB of dynamic shared memory, once per device.

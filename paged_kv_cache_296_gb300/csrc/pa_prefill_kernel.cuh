@@ -66,17 +66,24 @@ struct PrefillCfg {
   static constexpr int kThreads = (kConsumerWarps + 1) * 32;
   static constexpr int kRows = 16 * kConsumerWarps;   // rows per CTA
   static constexpr int kSwizzle = (kRowBytes >= 128) ? 128 : 64;
+  // Tiles land piece-major, [kRowBytes / 128][16 tokens][128 B] (one piece
+  // for 64-byte rows); each piece is a 128B-swizzled 16-row tile.
+  static constexpr int kPieceBytes = 16 * 128;
   static constexpr int kKSteps = D / 16;              // k-steps of Q K^T
   static constexpr int kDTiles = D / 8;               // n-tiles of O
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kSmemBytes = kRingBytes + 1024 + 2 * kStages * 8;
 };
 
-template <int SW>
-__device__ __forceinline__ uint32_t pf_swz(uint32_t off) {
-  if constexpr (SW == 128) {
+// Byte offset of (token row, byte column) inside a piece-major K or V tile.
+template <int D>
+__device__ __forceinline__ uint32_t pf_off(int tok, int col_bytes) {
+  if constexpr (D * 2 >= 128) {
+    const uint32_t off = (uint32_t)((col_bytes >> 7) * PrefillCfg<D>::kPieceBytes + tok * 128 +
+                                    (col_bytes & 127));
     return off ^ (((off >> 7) & 7u) << 4);
   } else {
+    const uint32_t off = (uint32_t)(tok * (D * 2) + col_bytes);
     return off ^ (((off >> 7) & 3u) << 4);
   }
 }
@@ -183,13 +190,8 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 2)
             const int row = (blk >= 0 && blk < p.num_blocks) ? blk * 16 : oob_row;
             uint8_t* ks = smem + s * C::kStageBytes;
             mbar_arrive_expect_tx(&full_bar[s], C::kStageBytes);
-            if constexpr (C::kRowBytes > 128) {
-              tma_load_4d(ks, &tmap_k, &full_bar[s], 0, 0, kvh, row, pol);
-              tma_load_4d(ks + C::kTileBytes, &tmap_v, &full_bar[s], 0, 0, kvh, row, pol);
-            } else {
-              tma_load_3d(ks, &tmap_k, &full_bar[s], 0, kvh, row, pol);
-              tma_load_3d(ks + C::kTileBytes, &tmap_v, &full_bar[s], 0, kvh, row, pol);
-            }
+            tma_load_4d(ks, &tmap_k, &full_bar[s], 0, row, 0, kvh, pol);
+            tma_load_4d(ks + C::kTileBytes, &tmap_v, &full_bar[s], 0, row, 0, kvh, pol);
             ++issued;
           }
         }
@@ -251,13 +253,25 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 2)
     const uint32_t vbase = kbase + C::kTileBytes;
 
     // ---- S = Q K^T for the block's 16 keys (two n-tiles of 8)
+    // Two accumulators per n-tile (even / odd k-steps): half-length MMA chains.
     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float sd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int ks = 0; ks < C::kKSteps; ++ks) {
       uint32_t b[4];
-      ldsm_x4(b, kbase + pf_swz<C::kSwizzle>(k_row * C::kRowBytes + (16 * ks + k_col) * 2));
-      pf_mma<QT>(sc[0], qa[ks], b[0], b[1]);
-      pf_mma<QT>(sc[1], qa[ks], b[2], b[3]);
+      ldsm_x4(b, kbase + pf_off<D>(k_row, (16 * ks + k_col) * 2));
+      if (ks & 1) {
+        pf_mma<QT>(sd[0], qa[ks], b[0], b[1]);
+        pf_mma<QT>(sd[1], qa[ks], b[2], b[3]);
+      } else {
+        pf_mma<QT>(sc[0], qa[ks], b[0], b[1]);
+        pf_mma<QT>(sc[1], qa[ks], b[2], b[3]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[j][e] = __fadd_rn(sc[j][e], sd[j][e]);
     }
     // ---- causal mask and online softmax (rows g: c0/c1, g+8: c2/c3)
     const int key0 = it * 16;
@@ -319,7 +333,7 @@ __global__ void __launch_bounds__(PrefillCfg<D>::kThreads, 2)
 #pragma unroll
     for (int dt = 0; dt < C::kDTiles / 2; ++dt) {
       uint32_t b[4];
-      ldsm_x4_trans(b, vbase + pf_swz<C::kSwizzle>(v_row * C::kRowBytes + (16 * dt + v_col) * 2));
+      ldsm_x4_trans(b, vbase + pf_off<D>(v_row, (16 * dt + v_col) * 2));
       if (valid < 16) {
         b[0] &= mlo; b[1] &= mhi; b[2] &= mlo; b[3] &= mhi;
       }

@@ -1,8 +1,9 @@
-"""One decode step of the hot path on the GPU: reshape_and_cache, then paged decode.
+"""One step of the hot path on the GPU, through the C ABI.
 
-:class:`DecodeStep` holds a workload's device-resident state (pool, tables,
-lengths, q, the step's new k/v, output, split-KV workspace) and runs a step
-through the C ABI.  The pool is the cache: it stays in HBM between steps.
+:class:`DecodeStep` holds a decode workload's device-resident state (pool,
+tables, lengths, q, the step's new k/v, output, split-KV workspace);
+:class:`PrefillStep` the same for a prefill (or chunked prefill) workload.
+The pool is the cache: it stays in HBM between steps.
 """
 
 import torch
@@ -151,3 +152,48 @@ def unique_kv_bytes(W):
             seen.add(key)
             total += n
     return total * spec.num_kv_heads * spec.head_size * 2 * elt
+
+
+class PrefillStep:
+    """Device buffers for one prefill workload: the step writes the query
+    tokens' K/V into the pool (pa_reshape_and_cache), then runs pa_prefill."""
+
+    #: Per-step inputs, packed by :meth:`stage_inputs` for host-to-device copies.
+    STEP_INPUTS = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens",
+                   "query_start_loc")
+
+    def __init__(self, W, device="cuda"):
+        self.W = W
+        self.device = torch.device(device)
+        self.pool = W.pool.to(self.device, copy=True)
+        self.k_cache, self.v_cache = pa.kv_views(self.pool)
+        for name in self.STEP_INPUTS:
+            setattr(self, name, getattr(W, name).to(self.device))
+        self.out = torch.empty_like(self.q)
+        self.max_query_len = W.max_query_len
+        self.scale = W.scale
+
+    stage_inputs = DecodeStep.stage_inputs
+
+    def step(self):
+        if self.q.shape[0]:
+            pa.pa_reshape_and_cache(self.k_new, self.v_new, self.k_cache, self.v_cache,
+                                    self.slot_mapping)
+        pa.pa_prefill(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
+                      self.context_lens, self.query_start_loc, self.max_query_len, self.scale)
+        return self.out
+
+    launches_per_step = 2
+
+
+def prefill_flops(W):
+    """Causal attention FLOPs of one prefill step: for every query (position p)
+    and query head, 2*D multiply-adds for each of the p + 1 scores and 2*D for
+    the weighted sum of as many V rows: 4 * D * Hq * sum (p + 1)."""
+    lens = W.context_lens.cpu().long().tolist()
+    qsl = W.query_start_loc.cpu().long().tolist()
+    keys = 0
+    for i, L in enumerate(lens):
+        n = qsl[i + 1] - qsl[i]
+        keys += (L - n) * n + n * (n + 1) // 2
+    return 4 * W.spec.head_size * W.spec.num_q_heads * keys
