@@ -23,6 +23,8 @@ Modules:
   paged_attention  -- reshape_and_cache, block-table gather, paged decode,
                       causal paged prefill, contiguous attention, split-KV
                       partials and their merge.
+  block_manager    -- the block allocator: free list, ceil growth, sharing by
+                      reference counts, copy-on-write of a shared last block.
 
 Every function is pinned by ``tests/test_oracle_*.py`` (run with
 ``-m "not gpu"``) against library routines, closed forms, invariants and the
