@@ -635,6 +635,95 @@ def run_prefill(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
+BLOCKS_METRIC = "block manager: pa_copy_blocks GB/s (copy-on-write block copies); host µs per decode step"
+
+
+def run_blocks(args, world, rank, local):
+    """The block manager leg.  GPU: pa_copy_blocks over 4096 (src, dst) pairs
+    of 64 KB blocks (fp16 pool, 8 KV heads, d128), read + write bytes against
+    the HBM peak.  Host: the native manager's decode step for 256 sequences
+    (append one token each, export the block tables), microseconds per step."""
+    from paged_kv_cache_296_gb300 import binding as pa
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    pa.load()
+    nb, hkv, d, npairs = 16384, 8, 128, 4096
+    pool = torch.empty((nb, 16, 2, hkv, d), dtype=torch.float16, device=device)
+    pool.normal_()
+    g = torch.Generator(device="cpu").manual_seed(7 + rank)
+    perm = torch.randperm(nb, generator=g)
+    pairs = torch.stack([perm[:npairs], perm[npairs:2 * npairs]], 1).to(torch.int64).to(device)
+    block_bytes = pool[0].numel() * 2
+    moved = 2 * npairs * block_bytes
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        pa.pa_copy_blocks(pool, pairs)
+    torch.cuda.synchronize(device)
+    n = args.steps
+    sampler = ClockSampler(device.index)
+    sampler.start()
+    time.sleep(0.3)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    t0 = time.time()
+    a.record(stream)
+    for _ in range(n):
+        pa.pa_copy_blocks(pool, pairs)
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    t1 = time.time()
+    sampler.stop()
+    ms = max_over_ranks(a.elapsed_time(b) / n, world, device)
+    if pa.pa_device_status(clear=True) != 0:
+        raise RuntimeError("pa_copy_blocks raised a device status bit")
+    gbs = sum_over_ranks(moved, world, device) / (ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    # host: the manager's side of a decode step, 256 running sequences
+    bm = pa.BlockManager(1 << 16)
+    seqs = list(range(256))
+    for s_ in seqs:
+        bm.allocate(s_, 1000 + 7 * s_)
+    for s_ in seqs[::4]:
+        bm.fork(s_, 10000 + s_)                 # some shared blocks: copy-on-write happens
+    ids = seqs + [10000 + s_ for s_ in seqs[::4]]
+    host_steps = 200
+    t_h = time.perf_counter()
+    ids_np = np.array(ids, dtype=np.int64)
+    ones = np.ones(len(ids), dtype=np.int64)
+    for _ in range(host_steps):
+        bm.append_batch(ids_np, ones, as_arrays=True)
+        bm.block_tables(ids_np, 256)
+    host_us = (time.perf_counter() - t_h) / host_steps * 1e6
+    line = {
+        "metric": BLOCKS_METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": n, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (N(0,1) pool, random block pairs)",
+        "config": {"workload": f"{npairs} copies of 64 KB blocks (16 tokens x 2 x 8 heads x "
+                               f"d128 fp16) in a {nb}-block pool",
+                   "l2": f"{moved / 1e9:.2f} GB moved per step, larger than L2",
+                   "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "copy_blocks_kernel", "achieved": round(gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+                     "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": moved,
+                     "traffic": None},
+        "host": {"us_per_decode_step": round(host_us, 2), "sequences": len(ids),
+                 "what": "pa_bm_append_batch (one token each) + pa_bm_block_tables (width 256), "
+                         "through the Python binding"},
+        "gpu_launches": n, "e2e": None, "cpu_baseline": None,
+        "clocks": sampler.summary(t0, t1),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def run_reference_prefill(args, world, rank, local):
     """The CPU oracle on a prefill workload: rank 0 alone, a bounded sample per step."""
     if rank != 0:
@@ -716,11 +805,15 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--prefill", type=int, default=0, choices=[0] + sorted(wl.PREFILL_SPECS),
                    help="time a prefill workload (pa_prefill) instead of the decode step")
+    p.add_argument("--blocks", action="store_true",
+                   help="time the block manager (pa_copy_blocks; host step of pa_bm_*)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
     world, rank, local = dist_env()
-    if args.prefill and args.impl == "ours":
+    if args.blocks:
+        run_blocks(args, world, rank, local)
+    elif args.prefill and args.impl == "ours":
         run_prefill(args, world, rank, local)
     elif args.prefill:
         run_reference_prefill(args, world, rank, local)

@@ -71,7 +71,8 @@ typedef enum {
   PA_ERR_UNSUPPORTED = 2, /* a shape or dtype outside the supported set above */
   PA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than pa_decode_workspace_size() */
   PA_ERR_CUDA = 4,        /* the CUDA runtime or driver reported an error */
-  PA_ERR_BAD_INDEX = 5    /* pa_check_tables() found out-of-range indices */
+  PA_ERR_BAD_INDEX = 5,   /* pa_check_tables() found out-of-range indices */
+  PA_ERR_OUT_OF_BLOCKS = 6 /* the block manager has too few free blocks (nothing changed) */
 } pa_status;
 
 /*
@@ -304,11 +305,87 @@ pa_status pa_check_tables(const int32_t* block_tables, const int32_t* context_le
  * pa_device_status -- error bits raised by kernels on the current device
  * instead of trapping (1 = a bounded wait inside a kernel timed out and the
  * kernel returned early; its outputs are then invalid; 2 = pa_prefill met a
- * sequence whose query count exceeds its length or max_query_len).  Synchronises the
+ * sequence whose query count exceeds its length or max_query_len; 4 =
+ * pa_copy_blocks skipped a pair naming a block outside the pool).  Synchronises the
  * device.  `clear` != 0 resets the bits.  Returns 0xFFFFFFFF if the status
  * word cannot be read.
  */
 uint32_t pa_device_status(int clear);
+
+/*
+ * ---------------------------------------------------------------- block manager
+ *
+ * pa_bm_* -- the host-side allocator of the pool's physical blocks (native
+ * C++; no GPU needed).  It follows the pages' KV cache sketch ("vLLM 部署深度指南",
+ * section 代码层面理解; "vLLM GitHub 项目…", section 二 items 1 and 4, section 三
+ * item 1): the free list starts as every block id in increasing order and
+ * blocks are taken from its front; a sequence of n tokens holds ceil(n /
+ * block_size) blocks and takes a new block when a token falls past its last
+ * one; too few free blocks is PA_ERR_OUT_OF_BLOCKS (the pages' OOMError), and
+ * the failed call changes nothing.  Sequences may share blocks (pa_bm_fork,
+ * for parallel sampling / beam search); blocks are reference counted and go
+ * to the back of the free list, in table order, when the last table lets go.
+ * An append whose first token lands in a partially filled block that another
+ * table also holds first moves the sequence to a private copy: it takes a new
+ * block and returns the (src, dst) pair, which the caller copies on the GPU
+ * (pa_copy_blocks) before writing the new tokens (pa_reshape_and_cache at the
+ * returned slots).  Sequence ids are arbitrary int64 keys.  Every call locks
+ * the manager.  Errors set pa_last_error().
+ */
+typedef struct pa_block_manager pa_block_manager;
+
+/* A manager of num_blocks blocks of block_size tokens; NULL on bad arguments. */
+pa_block_manager* pa_bm_create(int32_t num_blocks, int32_t block_size);
+void pa_bm_destroy(pa_block_manager* bm);
+
+/* Free blocks (-1 for a NULL manager); reference count of one block (-1 if out of range). */
+int32_t pa_bm_num_free(pa_block_manager* bm);
+int32_t pa_bm_ref_count(pa_block_manager* bm, int32_t block);
+
+/* A new sequence already holding num_tokens tokens (a prompt): ceil(n / block_size) blocks. */
+pa_status pa_bm_allocate(pa_block_manager* bm, int64_t seq_id, int64_t num_tokens);
+
+/*
+ * pa_bm_append_batch -- reserve counts[i] new tokens at the end of sequence
+ * seq_ids[i] (distinct ids), all or nothing.  slots_out (int64, sum(counts)
+ * entries, in batch order) receives each new token's slot block*block_size +
+ * offset, the slot_mapping of pa_reshape_and_cache; copies_out (int64 pairs,
+ * room for n_seqs pairs) receives the copy-on-write (src, dst) block pairs
+ * and *n_copies_out their number.
+ */
+pa_status pa_bm_append_batch(pa_block_manager* bm, const int64_t* seq_ids, const int64_t* counts,
+                             int32_t n_seqs, int64_t* slots_out, int64_t* copies_out,
+                             int32_t* n_copies_out);
+/* pa_bm_append_batch for one sequence (copies_out: room for one pair). */
+pa_status pa_bm_append(pa_block_manager* bm, int64_t seq_id, int64_t n, int64_t* slots_out,
+                       int64_t* copies_out, int32_t* n_copies_out);
+
+/* child (a new id) shares every block of parent; both hold the same tokens. */
+pa_status pa_bm_fork(pa_block_manager* bm, int64_t parent, int64_t child);
+
+/* Release a finished sequence (its blocks return to the free list once unreferenced). */
+pa_status pa_bm_free(pa_block_manager* bm, int64_t seq_id);
+
+/*
+ * Block tables of n_seqs sequences as pa_decode reads them: tables_out int32
+ * [n_seqs, width] row-major, -1 past each sequence's blocks; lens_out int32
+ * [n_seqs] (context lengths).  PA_ERR_INVALID_ARG if a table is wider than width.
+ */
+pa_status pa_bm_block_tables(pa_block_manager* bm, const int64_t* seq_ids, int32_t n_seqs,
+                             int32_t width, int32_t* tables_out, int32_t* lens_out);
+
+/*
+ * pa_copy_blocks -- copy whole physical blocks of the pool on the GPU: for
+ * each pair p, block pairs[2p + 1] becomes a byte copy of block pairs[2p]
+ * (all tokens, K and V, every head: a block is block_bytes = block_size * 2 *
+ * num_kv_heads * head_size * elt contiguous bytes of the pool's layout).
+ * pairs: device int64 [n_pairs, 2]; no destination may also be a source in
+ * the same call.  Pairs naming a block outside [0, num_blocks) are skipped
+ * and raise device status bit 4.  pool 16-byte aligned, block_bytes a
+ * multiple of 16.  Asynchronous on `stream`.
+ */
+pa_status pa_copy_blocks(void* pool, const int64_t* pairs, int64_t n_pairs, int32_t num_blocks,
+                         int64_t block_bytes, void* stream);
 
 /* Message describing the last error returned on the calling thread ("" if none). */
 const char* pa_last_error(void);

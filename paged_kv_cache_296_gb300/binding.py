@@ -10,6 +10,8 @@ library is missing or a call fails, an exception is raised.
 import ctypes
 import os
 
+import numpy as np
+
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -17,7 +19,8 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libpagedattn.so")
 
 PA_F16, PA_BF16, PA_E4M3, PA_F32 = 0, 1, 2, 3
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
-                3: "PA_ERR_WORKSPACE", 4: "PA_ERR_CUDA", 5: "PA_ERR_BAD_INDEX"}
+                3: "PA_ERR_WORKSPACE", 4: "PA_ERR_CUDA", 5: "PA_ERR_BAD_INDEX",
+                6: "PA_ERR_OUT_OF_BLOCKS"}
 
 #: Every function include/pa.h declares, with (restype, argtypes).
 _P, _I, _I64, _F, _SZ, _U32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
@@ -36,6 +39,17 @@ SIGNATURES = {
     "pa_gather_kv": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
     "pa_check_tables": (_I, [_P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P]),
     "pa_device_status": (_U32, [_I]),
+    "pa_bm_create": (_P, [ctypes.c_int32, ctypes.c_int32]),
+    "pa_bm_destroy": (None, [_P]),
+    "pa_bm_num_free": (ctypes.c_int32, [_P]),
+    "pa_bm_ref_count": (ctypes.c_int32, [_P, ctypes.c_int32]),
+    "pa_bm_allocate": (_I, [_P, _I64, _I64]),
+    "pa_bm_append_batch": (_I, [_P, _P, _P, ctypes.c_int32, _P, _P, _P]),
+    "pa_bm_append": (_I, [_P, _I64, _I64, _P, _P, _P]),
+    "pa_bm_fork": (_I, [_P, _I64, _I64]),
+    "pa_bm_free": (_I, [_P, _I64]),
+    "pa_bm_block_tables": (_I, [_P, _P, ctypes.c_int32, ctypes.c_int32, _P, _P]),
+    "pa_copy_blocks": (_I, [_P, _P, _I64, ctypes.c_int32, _I64, _P]),
     "pa_last_error": (ctypes.c_char_p, []),
     "pa_version": (_I, []),
 }
@@ -296,3 +310,100 @@ def pa_last_error():
 
 def pa_version():
     return int(load().pa_version())
+
+
+# ---------------------------------------------------------------- block manager
+
+class OutOfBlocks(PagedAttentionError):
+    """The block manager has too few free blocks (the call changed nothing)."""
+
+
+class BlockManager:
+    """The library's native block allocator (pa_bm_* in include/pa.h).
+
+    Sequence ids are Python ints.  ``append`` returns the new tokens' slots
+    (the slot_mapping of pa_reshape_and_cache) and the copy-on-write block
+    pairs to copy first (pa_copy_blocks).
+    """
+
+    def __init__(self, num_blocks, block_size=16):
+        self._lib = load()
+        self._h = self._lib.pa_bm_create(int(num_blocks), int(block_size))
+        if not self._h:
+            raise PagedAttentionError("pa_bm_create", 1, self._lib.pa_last_error().decode())
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            self._lib.pa_bm_destroy(h)
+
+    def _check(self, fn, st):
+        if st == 6:
+            raise OutOfBlocks(fn, st, self._lib.pa_last_error().decode())
+        _check(fn, st)
+
+    def num_free(self):
+        return self._lib.pa_bm_num_free(self._h)
+
+    def ref_count(self, block):
+        return self._lib.pa_bm_ref_count(self._h, int(block))
+
+    def allocate(self, seq_id, num_tokens):
+        self._check("pa_bm_allocate", self._lib.pa_bm_allocate(self._h, int(seq_id), int(num_tokens)))
+
+    def append_batch(self, seq_ids, counts, as_arrays=False):
+        """Reserve counts[i] tokens for seq_ids[i].
+
+        Returns (slots, copies): lists, or with ``as_arrays`` an int64 NumPy
+        array of slots and an int64 ``[n_copies, 2]`` array of pairs.
+        """
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        cnt = np.ascontiguousarray(counts, dtype=np.int64)
+        n = ids.shape[0]
+        total = int(cnt.sum()) if n else 0
+        slots = np.empty(max(total, 1), dtype=np.int64)
+        copies = np.empty((max(n, 1), 2), dtype=np.int64)
+        ncopy = ctypes.c_int32(0)
+        st = self._lib.pa_bm_append_batch(self._h, ids.ctypes.data, cnt.ctypes.data, n,
+                                          slots.ctypes.data, copies.ctypes.data,
+                                          ctypes.byref(ncopy))
+        self._check("pa_bm_append_batch", st)
+        slots, copies = slots[:total], copies[:ncopy.value]
+        if as_arrays:
+            return slots, copies
+        return slots.tolist(), [tuple(c) for c in copies.tolist()]
+
+    def append(self, seq_id, n):
+        return self.append_batch([seq_id], [n])
+
+    def fork(self, parent, child):
+        self._check("pa_bm_fork", self._lib.pa_bm_fork(self._h, int(parent), int(child)))
+
+    def free(self, seq_id):
+        self._check("pa_bm_free", self._lib.pa_bm_free(self._h, int(seq_id)))
+
+    def block_tables(self, seq_ids, width):
+        """int32 tensors (tables [n, width] padded with -1, lengths [n]) on the CPU."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = ids.shape[0]
+        tables = torch.empty((n, width), dtype=torch.int32)
+        lens = torch.empty((n,), dtype=torch.int32)
+        st = self._lib.pa_bm_block_tables(self._h, ids.ctypes.data, n, int(width),
+                                          ctypes.c_void_p(tables.data_ptr()),
+                                          ctypes.c_void_p(lens.data_ptr()))
+        self._check("pa_bm_block_tables", st)
+        return tables, lens
+
+
+def pa_copy_blocks(pool, pairs):
+    """Copy whole physical blocks of ``pool`` ``[NB, BS, 2, Hkv, D]`` on its device:
+    ``pairs`` int64 ``[n, 2]`` (src, dst) on the same device."""
+    if not pool.is_contiguous() or pairs.dtype != torch.int64 or not pairs.is_contiguous():
+        raise ValueError("pool must be contiguous and pairs a contiguous int64 [n, 2] tensor")
+    nb = pool.shape[0]
+    block_bytes = pool[0].numel() * pool.element_size()
+    st = load().pa_copy_blocks(_ptr(pool), _ptr(pairs), int(pairs.shape[0]), nb, block_bytes,
+                               _stream(pool))
+    _check("pa_copy_blocks", st)

@@ -276,6 +276,27 @@ uint32_t pa_device_status(int clear) {
   return v;
 }
 
+pa_status pa_copy_blocks(void* pool, const int64_t* pairs, int64_t n_pairs, int32_t num_blocks,
+                         int64_t block_bytes, void* stream) {
+  if (n_pairs < 0) return fail(PA_ERR_INVALID_ARG, "n_pairs must be >= 0");
+  if (n_pairs == 0) return ok();
+  if (n_pairs > 65535) return fail(PA_ERR_UNSUPPORTED, "at most 65535 pairs per call");
+  if (!pool || !pairs) return fail(PA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(pool)) return fail(PA_ERR_INVALID_ARG, "pool must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(pairs) & 7u)
+    return fail(PA_ERR_INVALID_ARG, "pairs must be 8-byte aligned");
+  if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "num_blocks must be > 0");
+  if (block_bytes <= 0 || block_bytes % 16 != 0)
+    return fail(PA_ERR_INVALID_ARG, "block_bytes must be a positive multiple of 16");
+  unsigned* status = nullptr;
+  cudaError_t e = pa::device_status_ptr(&status);
+  if (e != cudaSuccess) return cuda_fail(e, "status word");
+  e = pa::launch_copy_blocks(pool, pairs, n_pairs, num_blocks, block_bytes, status,
+                             static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "pa_copy_blocks");
+  return ok();
+}
+
 pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
                      const int32_t* block_tables, const int32_t* context_lens,
                      const int32_t* query_start_loc, int num_seqs, int max_query_len,

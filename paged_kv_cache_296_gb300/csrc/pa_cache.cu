@@ -305,6 +305,60 @@ cudaError_t launch_gather_kv(void* k_out, void* v_out, const void* k_cache, cons
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- block copies
+
+namespace {
+
+// Copy-on-write copies: pair p copies block pairs[2p] onto block pairs[2p+1]
+// (a block is one contiguous run of block_bytes bytes of the pool).  A grid of
+// (chunks, pairs) CTAs; each thread moves kCopyUnroll 16-byte vectors per
+// step, all loads issued before the stores, coalesced on both sides.
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+
+__global__ void __launch_bounds__(kCopyThreads)
+    copy_blocks_kernel(uint8_t* __restrict__ pool, const int64_t* __restrict__ pairs,
+                       int num_blocks, int64_t block_bytes, unsigned* status) {
+  const int64_t p = blockIdx.y;
+  const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(status, 4u);
+    return;
+  }
+  const uint4* s = reinterpret_cast<const uint4*>(pool + src * block_bytes);
+  uint4* d = reinterpret_cast<uint4*>(pool + dst * block_bytes);
+  const int64_t n = block_bytes / 16;
+  constexpr int64_t kSpan = (int64_t)kCopyThreads * kCopyUnroll;
+  for (int64_t base = (int64_t)blockIdx.x * kSpan + threadIdx.x; base < n;
+       base += (int64_t)gridDim.x * kSpan) {
+    uint4 v[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t i = base + (int64_t)u * kCopyThreads;
+      if (i < n) v[u] = s[i];
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t i = base + (int64_t)u * kCopyThreads;
+      if (i < n) d[i] = v[u];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_copy_blocks(void* pool, const int64_t* pairs, int64_t n_pairs, int num_blocks,
+                               int64_t block_bytes, unsigned* status, cudaStream_t stream) {
+  if (n_pairs == 0) return cudaSuccess;
+  const int64_t vec = block_bytes / 16;
+  const int64_t span = (int64_t)kCopyThreads * kCopyUnroll;
+  const int64_t chunks = std::min<int64_t>((vec + span - 1) / span, 64);
+  const dim3 grid((unsigned)std::max<int64_t>(chunks, 1), (unsigned)n_pairs);
+  copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(static_cast<uint8_t*>(pool), pairs,
+                                                        num_blocks, block_bytes, status);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- index validation
 
 namespace {

@@ -81,6 +81,9 @@ cudaError_t launch_gather_kv(void* k_out, void* v_out, const void* k_cache, cons
                              const int64_t* cu_seqlens, int num_seqs, int max_blocks_per_seq,
                              int num_blocks, int row_bytes, cudaStream_t stream);
 
+cudaError_t launch_copy_blocks(void* pool, const int64_t* pairs, int64_t n_pairs, int num_blocks,
+                               int64_t block_bytes, unsigned* status, cudaStream_t stream);
+
 cudaError_t launch_check_tables(const int32_t* block_tables, const int32_t* context_lens,
                                 const int64_t* slot_mapping, int64_t n_tokens, int num_seqs,
                                 int max_blocks_per_seq, int num_blocks, int block_size,

@@ -1,0 +1,149 @@
+"""The native block manager (pa_bm_*) against the oracle's model (CPU only).
+
+Both follow the same policy, so every observable result must be identical:
+block tables, lengths, the slots an append returns, the copy-on-write pairs,
+free-block counts, reference counts and which requests run out of blocks.
+"""
+
+import random
+
+import pytest
+
+from oracle.block_manager import BlockManager as RefManager, OutOfBlocks as RefOOM
+from paged_kv_cache_296_gb300 import binding as pa
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_296_gb300 import build
+    build()
+    return pa.load()
+
+
+def _same_state(bm, ref):
+    assert bm.num_free() == ref.num_free()
+    for b in range(ref.num_blocks):
+        assert bm.ref_count(b) == ref.ref[b], f"block {b}"
+    ids = sorted(ref.tables)
+    if not ids:
+        return
+    width = max(1, max(len(t) for t in ref.tables.values()))
+    tables, lens = bm.block_tables(ids, width)
+    for k, s in enumerate(ids):
+        assert tables[k].tolist() == ref.block_table(s, width), f"seq {s}"
+        assert int(lens[k]) == ref.lens[s]
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_native_manager_matches_the_oracle(lib, seed):
+    rnd = random.Random(seed)
+    nblocks = rnd.choice([5, 16, 64])
+    bm = pa.BlockManager(nblocks)
+    ref = RefManager(nblocks)
+    next_id = 0
+    for _ in range(300):
+        live = sorted(ref.tables)
+        op = rnd.random()
+        if op < 0.2 or not live:
+            n = rnd.randint(0, 60)
+            exp_oom = False
+            try:
+                ref.allocate(next_id, n)
+            except RefOOM:
+                exp_oom = True
+            if exp_oom:
+                with pytest.raises(pa.OutOfBlocks):
+                    bm.allocate(next_id, n)
+            else:
+                bm.allocate(next_id, n)
+            next_id += 1
+        elif op < 0.55:
+            k = rnd.randint(1, min(4, len(live)))
+            seqs = rnd.sample(live, k)
+            counts = [rnd.randint(0, 20) for _ in seqs]
+            # the oracle applies the batch as one request: all or nothing
+            snapshot = (list(ref.free), list(ref.ref), {s: list(t) for s, t in ref.tables.items()},
+                        dict(ref.lens))
+            want_slots, want_copies, oom = [], [], False
+            try:
+                for s, c in zip(seqs, counts):
+                    sl, cp = ref.append(s, c)
+                    want_slots += sl
+                    want_copies += cp
+            except RefOOM:
+                oom = True
+                from collections import deque
+                ref.free = deque(snapshot[0])
+                ref.ref = snapshot[1]
+                ref.tables = snapshot[2]
+                ref.lens = snapshot[3]
+            if oom:
+                with pytest.raises(pa.OutOfBlocks):
+                    bm.append_batch(seqs, counts)
+            else:
+                slots, copies = bm.append_batch(seqs, counts)
+                assert slots == want_slots
+                assert copies == want_copies
+        elif op < 0.75:
+            s = rnd.choice(live)
+            ref.fork(s, next_id)
+            bm.fork(s, next_id)
+            next_id += 1
+        else:
+            s = rnd.choice(live)
+            ref.free_seq(s)
+            bm.free(s)
+        _same_state(bm, ref)
+
+
+def test_errors_change_nothing(lib):
+    bm = pa.BlockManager(4)
+    bm.allocate(1, 40)
+    with pytest.raises(pa.OutOfBlocks):
+        bm.allocate(2, 40)
+    with pytest.raises(pa.PagedAttentionError):
+        bm.allocate(1, 1)                   # id already present
+    with pytest.raises(pa.PagedAttentionError):
+        bm.append(7, 1)                     # unknown id
+    with pytest.raises(pa.PagedAttentionError):
+        bm.append_batch([1, 1], [1, 1])     # the same id twice in one batch
+    with pytest.raises(pa.PagedAttentionError):
+        bm.fork(1, 1)
+    with pytest.raises(pa.PagedAttentionError):
+        bm.block_tables([1], 2)             # 3 blocks do not fit in width 2
+    assert bm.num_free() == 1
+    t, lens = bm.block_tables([1], 3)
+    assert t.tolist() == [[0, 1, 2]] and lens.tolist() == [40]
+
+
+def test_batch_that_does_not_fit_changes_nothing(lib):
+    bm = pa.BlockManager(6)
+    bm.allocate(1, 16)
+    bm.allocate(2, 16)
+    with pytest.raises(pa.OutOfBlocks):
+        bm.append_batch([1, 2], [40, 40])   # 3 + 3 new blocks, 4 free
+    t, lens = bm.block_tables([1, 2], 4)
+    assert lens.tolist() == [16, 16] and bm.num_free() == 4
+
+
+def test_manager_from_several_threads(lib):
+    import threading
+    bm = pa.BlockManager(4096)
+    errors = []
+
+    def worker(base):
+        try:
+            for k in range(200):
+                sid = base * 1000 + k
+                bm.allocate(sid, 20)
+                bm.append(sid, 30)
+                bm.free(sid)
+        except Exception as e:   # pragma: no cover - reported below
+            errors.append(e)
+
+    ts = [threading.Thread(target=worker, args=(i,)) for i in range(8)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors and bm.num_free() == 4096
