@@ -21,6 +21,19 @@ Readings where the pages are silent (each listed in the design notes):
     the copy (old -> new) is recorded for the cache, the old block loses one
     reference.
 
+Prefix caching ("vLLM 部署深度指南", Prefix Caching 加速 table and the
+PagedAttention table's 前缀共享 row; "vLLM高性能推理引擎实战解密", section 3.1
+PagedAttention内存管理机制, cross-request sharing: requests with the same
+prefix share its KV cache)
+is read as: a full block can serve any request whose tokens, from the first
+up to that block's last, are the same.  A cached block is found by the key
+(parent block, the parent's generation, the block's tokens) -- exact, no
+hashing shortcuts -- where the generation counts how often a block id has
+been handed out, so a key naming a block that was since reused never
+matches.  Released cached blocks stay findable until the allocator hands
+them out again (then their key is dropped).  At least one prompt token is
+always left to compute, so a fully cached prompt recomputes its last block.
+
 Everything is plain Python lists and dicts, step by step.
 """
 
@@ -39,6 +52,9 @@ class BlockManager:
         self.ref = [0] * num_blocks
         self.tables = {}   # seq_id -> list of physical block ids
         self.lens = {}     # seq_id -> tokens held
+        self.gen = [0] * num_blocks   # times each block id was handed out
+        self.cache = {}    # (parent block, parent gen, tokens) -> cached block
+        self.key_of = {}   # cached block -> its key
 
     def blocks_for(self, num_tokens):
         return (num_tokens + self.block_size - 1) // self.block_size
@@ -48,6 +64,9 @@ class BlockManager:
 
     def _take(self):
         b = self.free.popleft()
+        if b in self.key_of:               # handing out a cached block evicts it
+            del self.cache[self.key_of.pop(b)]
+        self.gen[b] += 1
         self.ref[b] = 1
         return b
 
@@ -111,3 +130,52 @@ class BlockManager:
     def block_table(self, seq_id, width):
         t = self.tables[seq_id]
         return t + [-1] * (width - len(t))
+
+    # ---------------------------------------------------------- prefix caching
+
+    def _key(self, parent, tokens):
+        return (parent, self.gen[parent] if parent >= 0 else 0, tuple(tokens))
+
+    def register(self, seq_id, tokens):
+        """Make the full blocks of ``seq_id`` findable; ``tokens`` are its token
+        ids from the first (at least its length's worth of full blocks)."""
+        bs = self.block_size
+        table = self.tables[seq_id]
+        parent = -1
+        for j in range(min(len(tokens), self.lens[seq_id]) // bs):
+            b = table[j]
+            key = self._key(parent, tokens[j * bs:(j + 1) * bs])
+            if key not in self.cache and b not in self.key_of:
+                self.cache[key] = b
+                self.key_of[b] = key
+            parent = b
+
+    def allocate_cached(self, seq_id, tokens):
+        """A new sequence for the prompt ``tokens`` that reuses the longest run
+        of cached full blocks from its start.  Returns the number of tokens
+        whose K/V are already cached (a multiple of block_size, < len(tokens)
+        unless the prompt is empty); the caller computes the rest."""
+        assert seq_id not in self.tables
+        bs = self.block_size
+        n = len(tokens)
+        reusable = (n - 1) // bs if n > 0 else 0
+        hits = []
+        parent = -1
+        for j in range(reusable):
+            b = self.cache.get(self._key(parent, tokens[j * bs:(j + 1) * bs]))
+            if b is None:
+                break
+            hits.append(b)
+            parent = b
+        need = self.blocks_for(n) - len(hits)
+        idle = sum(1 for b in hits if self.ref[b] == 0)   # cached blocks on the free list
+        if need > len(self.free) - idle:
+            raise OutOfBlocks(f"need {need} blocks, {len(self.free) - idle} free")
+        for b in hits:
+            if self.ref[b] == 0:
+                self.free.remove(b)
+            self.ref[b] += 1
+        self.tables[seq_id] = hits + [self._take() for _ in range(need)]
+        self.lens[seq_id] = n
+        self.register(seq_id, tokens)
+        return len(hits) * bs

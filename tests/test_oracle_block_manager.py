@@ -148,3 +148,121 @@ def test_memory_model_random_operations(seed):
             L = bm.lens[s]
             got = [pool.get(t[p // bs] * bs + p % bs) for p in range(L)]
             assert got == logical[s], f"seq {s}"
+
+
+# ---------------------------------------------------------------- prefix caching
+
+def _toks(*runs):
+    out = []
+    for start, n in runs:
+        out += list(range(start, start + n))
+    return out
+
+
+def test_prefix_hits_for_a_shared_system_prompt():
+    bm = BlockManager(32)
+    system = _toks((1000, 40))                      # 2 full blocks + 8 tokens
+    a = system + _toks((1, 30))
+    b = system + _toks((500, 25))
+    assert bm.allocate_cached("a", a) == 0
+    assert bm.allocate_cached("b", b) == 32          # the 2 full system blocks
+    assert bm.tables["b"][:2] == bm.tables["a"][:2]
+    assert bm.tables["b"][2] != bm.tables["a"][2]    # the block mixing prompts differs
+    assert bm.ref[bm.tables["a"][0]] == 2
+
+
+def test_cached_blocks_survive_release_until_handed_out_again():
+    bm = BlockManager(8)
+    p = _toks((7, 48))                               # 3 full blocks
+    bm.allocate_cached("a", p)
+    held = list(bm.tables["a"])
+    bm.free_seq("a")
+    assert bm.allocate_cached("b", p + [1]) == 48    # all three reused from the free list
+    assert bm.tables["b"][:3] == held
+    bm.free_seq("b")
+    bm.allocate("x", 8 * 16 - 16)                    # takes 7 blocks: evicts cached ones
+    bm.free_seq("x")
+    assert bm.allocate_cached("c", p + [1]) < 48
+
+
+def test_a_fully_cached_prompt_still_computes_its_last_block():
+    bm = BlockManager(8)
+    p = _toks((3, 32))
+    bm.allocate_cached("a", p)
+    assert bm.allocate_cached("b", p) == 16          # not 32: one block is recomputed
+    assert bm.allocate_cached("c", p[:31]) == 16
+
+
+def test_a_reused_parent_id_does_not_match_old_children():
+    # Block 0 (the first block of prompt p) is handed out again for other
+    # content X while block 1 (p's second block, keyed under block 0's old
+    # generation) is still cached.  A prompt X + p's second block must not
+    # pick up block 1: its K/V were computed after p's first block, not X's.
+    bm = BlockManager(4)
+    p = _toks((100, 33))                             # blocks 0, 1 full, 2 partial
+    bm.allocate_cached("a", p)
+    bm.free_seq("a")                                 # free list: 3, 0, 1, 2
+    bm.allocate("x", 16)                             # takes 3
+    X = _toks((9, 16))
+    assert bm.allocate_cached("y", X) == 0           # takes 0 (evicted), registers X there
+    assert bm.tables["y"] == [0]
+    z = X + p[16:32] + [5]
+    assert bm.allocate_cached("z", z) == 16          # block 0 hits; block 1 must not
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_prefix_cache_memory_model(seed):
+    # The K/V a slot holds stands for the token prefix that produced it; every
+    # sequence read back through its table must see its own prefixes.
+    rnd = random.Random(1000 + seed)
+    bs = 16
+    bm = BlockManager(rnd.choice([10, 24, 64]), bs)
+    pool = {}
+    seqs = {}    # seq -> its token list
+    bases = [_toks((rnd.randint(0, 5) * 100, rnd.randint(0, 70))) for _ in range(4)]
+    nid = 0
+    for _ in range(150):
+        op = rnd.random()
+        live = list(bm.tables)
+        try:
+            if op < 0.45 or not live:
+                toks = list(rnd.choice(bases)) + _toks((rnd.randint(0, 3) * 7, rnd.randint(0, 40)))
+                if rnd.random() < 0.3:
+                    toks = toks[:rnd.randint(0, len(toks))]
+                cached = bm.allocate_cached(nid, toks)
+                assert cached % bs == 0 and (cached < len(toks) or len(toks) == 0)
+                t = bm.tables[nid]
+                for pos in range(cached, len(toks)):         # compute only what is not cached
+                    pool[t[pos // bs] * bs + pos % bs] = tuple(toks[:pos + 1])
+                seqs[nid] = toks
+                nid += 1
+            elif op < 0.7:
+                s = rnd.choice(live)
+                extra = _toks((rnd.randint(0, 9) * 11, rnd.randint(1, 20)))
+                slots, copies = bm.append(s, len(extra))
+                for src, dst in copies:
+                    for o in range(bs):
+                        if src * bs + o in pool:
+                            pool[dst * bs + o] = pool[src * bs + o]
+                base = len(seqs[s])
+                seqs[s] = seqs[s] + extra
+                for k, sl in enumerate(slots):
+                    pool[sl] = tuple(seqs[s][:base + k + 1])
+                if rnd.random() < 0.5:
+                    bm.register(s, seqs[s])
+            elif op < 0.8:
+                s = rnd.choice(live)
+                bm.fork(s, nid)
+                seqs[nid] = list(seqs[s])
+                nid += 1
+            else:
+                s = rnd.choice(live)
+                bm.free_seq(s)
+                del seqs[s]
+        except OutOfBlocks:
+            pass
+        _check_invariants(bm)
+        for s, t in bm.tables.items():
+            toks = seqs[s]
+            for pos in range(len(toks)):
+                assert pool.get(t[pos // bs] * bs + pos % bs) == tuple(toks[:pos + 1]), (s, pos)
