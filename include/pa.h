@@ -360,6 +360,25 @@ pa_status pa_bm_append_batch(pa_block_manager* bm, const int64_t* seq_ids, const
 pa_status pa_bm_append(pa_block_manager* bm, int64_t seq_id, int64_t n, int64_t* slots_out,
                        int64_t* copies_out, int32_t* n_copies_out);
 
+/*
+ * pa_bm_allocate_cached -- pa_bm_allocate for a prompt given by its token ids,
+ * with prefix caching ("vLLM 部署深度指南", Prefix Caching 加速 and the 前缀共享 row;
+ * "vLLM高性能推理引擎实战解密", section 3.1, cross-request sharing): the longest
+ * run of cached full blocks from the prompt's start is reused (a block is
+ * found by its parent block, the parent's generation and its tokens, exactly;
+ * released cached blocks stay findable until handed out again), the rest is
+ * allocated, and the prompt's full blocks become findable.  *n_cached_out
+ * receives the number of leading tokens whose K/V are already in the pool (a
+ * multiple of block_size, below n_tokens unless the prompt is empty): the
+ * caller writes and prefills only the tokens after them.
+ */
+pa_status pa_bm_allocate_cached(pa_block_manager* bm, int64_t seq_id, const int32_t* tokens,
+                                int64_t n_tokens, int64_t* n_cached_out);
+
+/* Make the full blocks of seq_id findable by later prompts (tokens: its ids from the first). */
+pa_status pa_bm_register(pa_block_manager* bm, int64_t seq_id, const int32_t* tokens,
+                         int64_t n_tokens);
+
 /* child (a new id) shares every block of parent; both hold the same tokens. */
 pa_status pa_bm_fork(pa_block_manager* bm, int64_t parent, int64_t child);
 

@@ -47,6 +47,8 @@ SIGNATURES = {
     "pa_bm_append_batch": (_I, [_P, _P, _P, ctypes.c_int32, _P, _P, _P]),
     "pa_bm_append": (_I, [_P, _I64, _I64, _P, _P, _P]),
     "pa_bm_fork": (_I, [_P, _I64, _I64]),
+    "pa_bm_allocate_cached": (_I, [_P, _I64, _P, _I64, _P]),
+    "pa_bm_register": (_I, [_P, _I64, _P, _I64]),
     "pa_bm_free": (_I, [_P, _I64]),
     "pa_bm_block_tables": (_I, [_P, _P, ctypes.c_int32, ctypes.c_int32, _P, _P]),
     "pa_copy_blocks": (_I, [_P, _P, _I64, ctypes.c_int32, _I64, _P]),
@@ -377,6 +379,21 @@ class BlockManager:
 
     def append(self, seq_id, n):
         return self.append_batch([seq_id], [n])
+
+    def allocate_cached(self, seq_id, tokens):
+        """A new sequence for the prompt ``tokens`` (ints) with prefix caching;
+        returns how many leading tokens are already cached."""
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        cached = ctypes.c_int64(0)
+        st = self._lib.pa_bm_allocate_cached(self._h, int(seq_id), toks.ctypes.data,
+                                             toks.shape[0], ctypes.byref(cached))
+        self._check("pa_bm_allocate_cached", st)
+        return cached.value
+
+    def register(self, seq_id, tokens):
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        self._check("pa_bm_register",
+                    self._lib.pa_bm_register(self._h, int(seq_id), toks.ctypes.data, toks.shape[0]))
 
     def fork(self, parent, child):
         self._check("pa_bm_fork", self._lib.pa_bm_fork(self._h, int(parent), int(child)))

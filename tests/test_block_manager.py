@@ -147,3 +147,53 @@ def test_manager_from_several_threads(lib):
     for t in ts:
         t.join()
     assert not errors and bm.num_free() == 4096
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_native_prefix_caching_matches_the_oracle(lib, seed):
+    rnd = random.Random(500 + seed)
+    nblocks = rnd.choice([6, 20, 64])
+    bm = pa.BlockManager(nblocks)
+    ref = RefManager(nblocks)
+    bases = [[rnd.randint(0, 3) for _ in range(rnd.randint(0, 70))] for _ in range(4)]
+    toks_of = {}
+    nid = 0
+    for _ in range(250):
+        live = sorted(ref.tables)
+        op = rnd.random()
+        if op < 0.45 or not live:
+            toks = list(rnd.choice(bases)) + [rnd.randint(0, 3) for _ in range(rnd.randint(0, 40))]
+            try:
+                want = ref.allocate_cached(nid, toks)
+            except RefOOM:
+                with pytest.raises(pa.OutOfBlocks):
+                    bm.allocate_cached(nid, toks)
+            else:
+                assert bm.allocate_cached(nid, toks) == want
+                toks_of[nid] = toks
+            nid += 1
+        elif op < 0.65:
+            s = rnd.choice(live)
+            k = rnd.randint(1, 20)
+            try:
+                want = ref.append(s, k)
+            except RefOOM:
+                with pytest.raises(pa.OutOfBlocks):
+                    bm.append(s, k)
+            else:
+                assert bm.append(s, k) == (want[0], want[1])
+                toks_of[s] = toks_of[s] + [rnd.randint(0, 3) for _ in range(k)]
+                if rnd.random() < 0.5:
+                    ref.register(s, toks_of[s])
+                    bm.register(s, toks_of[s])
+        elif op < 0.75:
+            s = rnd.choice(live)
+            ref.fork(s, nid)
+            bm.fork(s, nid)
+            toks_of[nid] = list(toks_of[s])
+            nid += 1
+        else:
+            s = rnd.choice(live)
+            ref.free_seq(s)
+            bm.free(s)
+        _same_state(bm, ref)
