@@ -112,3 +112,61 @@ def test_parallel_sampling_driven_by_the_manager(prompt_len, samples):
     for s in ids:
         bm.free(s)
     assert bm.num_free() == nb
+
+
+def test_prefix_cached_prefill_equals_the_full_prompt():
+    """The pages' system-prompt scenario: a second request with the same 2000
+    -token system prompt finds its 125 blocks cached, writes and prefills only
+    its own 100 tokens (a chunked prefill over the cached prefix), and its
+    outputs equal the oracle's prefill of the whole prompt."""
+    hq, hkv, d, nb = 8, 2, 64, 512
+    g = torch.Generator().manual_seed(11)
+    bm = pa.BlockManager(nb)
+    pool = torch.full((nb, 16, 2, hkv, d), float("nan"), dtype=torch.bfloat16).cuda()
+    kc, vc = pa.kv_views(pool)
+    system = torch.randint(0, 32000, (2000,), generator=g).tolist()
+    # K/V of a token stand for the token and its prefix: draw them per request
+    # position from the token ids, so equal prefixes give equal K/V
+    def kv_for(tokens, start):
+        out_k, out_v = [], []
+        for p in range(start, len(tokens)):
+            gg = torch.Generator().manual_seed(hash((tuple(tokens[:p + 1]),)) & 0x7FFFFFFF)
+            out_k.append(torch.randn((hkv, d), generator=gg))
+            out_v.append(torch.randn((hkv, d), generator=gg))
+        return torch.stack(out_k).bfloat16(), torch.stack(out_v).bfloat16()
+
+    def run(seq_id, tokens):
+        cached = bm.allocate_cached(seq_id, tokens)
+        n = len(tokens)
+        t, lens = bm.block_tables([seq_id], 256)
+        slots = [int(t[0, p // 16]) * 16 + p % 16 for p in range(cached, n)]
+        k, v = kv_for(tokens, cached)
+        pa.pa_reshape_and_cache(k.cuda(), v.cuda(), kc, vc,
+                                torch.tensor(slots, dtype=torch.int64).cuda())
+        q = torch.randn((n - cached, hq, d), generator=g).bfloat16()
+        out = torch.empty_like(q).cuda()
+        qsl = torch.tensor([0, n - cached], dtype=torch.int32)
+        pa.pa_prefill(out, q.cuda(), kc, vc, t.cuda(), lens.cuda(), qsl.cuda(), n - cached, 0.125)
+        return cached, q, out, t, lens, qsl
+
+    user_a = torch.randint(0, 32000, (100,), generator=g).tolist()
+    user_b = torch.randint(0, 32000, (100,), generator=g).tolist()
+    c_a, *_ = run(1, system + user_a)
+    assert c_a == 0
+    c_b, q, out, t, lens, qsl = run(2, system + user_b)
+    assert c_b == 2000
+    assert bm.ref_count(int(t[0, 0])) == 2
+    # the oracle: the whole second prompt's K/V laid out privately, the last
+    # 100 tokens as queries
+    toks = system + user_b
+    k_all, v_all = kv_for(toks, 0)
+    nblk = -(-len(toks) // 16)
+    opool = np.full((nblk, 16, 2, hkv, d), 0, dtype=np.uint16)
+    for p in range(len(toks)):
+        opool[p // 16, p % 16, 0] = bits_of(k_all[p])
+        opool[p // 16, p % 16, 1] = bits_of(v_all[p])
+    want = ref.paged_prefill(bits_of(q), "bf16", opool, np.arange(nblk)[None, :],
+                             np.array([len(toks)]), np.array([0, 100]), 0.125, "bf16")
+    got = ref.widen(bits_of(out.cpu()), "bf16")
+    assert np.isfinite(got).all()
+    assert np.abs(got - want).max() <= ATOL["bf16"]
