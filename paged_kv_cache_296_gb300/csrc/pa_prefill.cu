@@ -6,13 +6,14 @@
 
 #include "pa_internal.h"
 #include "pa_prefill_kernel.cuh"
+#include "pa_prefill_tc.cuh"
 
 namespace pa {
 namespace {
 
 template <int D, int QT>
 cudaError_t launch_prefill_instance(const PrefillArgs& a, cudaStream_t stream, const char** why) {
-  using C = PrefillCfg<D>;
+  using C = PrefillTcCfg<D>;
   const int G = a.num_q_heads / a.num_kv_heads;
   const long long tiles = ((long long)a.max_query_len * G + C::kRows - 1) / C::kRows;
   if (tiles == 0 || a.num_seqs == 0) return cudaSuccess;
@@ -33,7 +34,7 @@ cudaError_t launch_prefill_instance(const PrefillArgs& a, cudaStream_t stream, c
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(attr_done.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(paged_prefill_kernel<D, QT>,
+    e = cudaFuncSetAttribute(paged_prefill_tc_kernel<D, QT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit, std::memory_order_acq_rel);
@@ -66,7 +67,7 @@ cudaError_t launch_prefill_instance(const PrefillArgs& a, cudaStream_t stream, c
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, paged_prefill_kernel<D, QT>, tk, tv, p);
+  return cudaLaunchKernelEx(&cfg, paged_prefill_tc_kernel<D, QT>, tk, tv, p);
 }
 
 }  // namespace

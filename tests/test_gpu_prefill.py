@@ -170,3 +170,26 @@ def test_empty_batch_and_no_queries_are_no_ops():
     W = wl.make_prefill_workload(spec, 9)
     out, _ = gpu_prefill(W)
     assert out.numel() == 0
+
+
+@pytest.mark.parametrize("dtype,head_size", [("f16", 64), ("bf16", 128)])
+def test_growing_logits_rescale_the_accumulator(dtype, head_size):
+    # K grows with the position and q is all ones, so every row's running
+    # maximum keeps rising: the kernel must rescale what it has accumulated
+    # many times over (and the oracle sees the same values).
+    lens, nq = [300, 150, 97], [300, 20, 1]
+    spec = wl.PrefillSpec("growing logits", 3, 4, 2, head_size, dtype, ("fixed", lens),
+                          ("fixed", nq), ("factor", 1.2))
+    W = wl.make_prefill_workload(spec, 17)
+    tables = W.block_tables.numpy()
+    qsl = W.query_start_loc.numpy()
+    slope = 3.2 / head_size                           # log2-scaled logit grows ~0.6 per position
+    for i, L in enumerate(lens):
+        for p in range(L):
+            val = slope * p
+            if p < L - nq[i]:
+                W.pool[tables[i, p // 16], p % 16, 0] = val
+            else:
+                W.k_new[qsl[i] + p - (L - nq[i])] = val
+    W.q.fill_(1.0)
+    full_check(W)
