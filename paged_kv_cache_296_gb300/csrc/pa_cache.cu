@@ -72,7 +72,7 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 bool encode_kv_tensor_map_planes(void* desc, const void* base, int num_blocks, int num_kv_heads,
-                                 int head_size, int elt_bytes, const char** why) {
+                                 int head_size, int elt_bytes, int box_pieces, const char** why) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     *why = "cuTensorMapEncodeTiled is not available from the driver";
@@ -91,7 +91,7 @@ bool encode_kv_tensor_map_planes(void* desc, const void* base, int num_blocks, i
   // a box lands as [piece][token][128 B], each piece a 16-row swizzled tile.
   const cuuint64_t dims[4] = {128ull / elt_bytes, ntok, row / 128, (cuuint64_t)num_kv_heads};
   const cuuint64_t strides[3] = {token_stride, 128ull, row};
-  const cuuint32_t box[4] = {128u / elt_bytes, 16u, (cuuint32_t)(row / 128), 1u};
+  const cuuint32_t box[4] = {128u / elt_bytes, 16u, (cuuint32_t)box_pieces, 1u};
   const cuuint32_t es[4] = {1u, 1u, 1u, 1u};
   const CUresult r = fn(static_cast<CUtensorMap*>(desc), dt, 4, const_cast<void*>(base), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,

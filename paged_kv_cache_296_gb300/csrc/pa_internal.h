@@ -103,11 +103,12 @@ cudaError_t device_status_ptr(unsigned** ptr);
 bool encode_kv_tensor_map(void* desc, const void* base, int num_blocks, int num_kv_heads,
                           int head_size, int elt_bytes, int box_heads, const char** why);
 
-// The same view for rows of a multiple of 128 bytes, but a box (16 tokens x
-// one head) lands piece-major: [row / 128][16 tokens][128 B], so each 128-byte
-// piece of the rows is a 16-row 128B-swizzled tile and 8 consecutive tokens at
-// one column fall in 8 different bank groups.
+// The same view for rows of a multiple of 128 bytes, with the row split into
+// 128-byte pieces as its own dimension: a box of 16 tokens x `box_pieces`
+// pieces x one head lands piece-major, [pieces][16 tokens][128 B], each piece
+// a 16-row 128B-swizzled tile (box_pieces = 1 copies one piece, so a kernel
+// can place each piece of a block where it wants).
 bool encode_kv_tensor_map_planes(void* desc, const void* base, int num_blocks, int num_kv_heads,
-                                 int head_size, int elt_bytes, const char** why);
+                                 int head_size, int elt_bytes, int box_pieces, const char** why);
 
 }  // namespace pa

@@ -15,16 +15,17 @@ template <int D, int QT>
 cudaError_t launch_prefill_instance(const PrefillArgs& a, cudaStream_t stream, const char** why) {
   using C = PrefillTcCfg<D>;
   const int G = a.num_q_heads / a.num_kv_heads;
-  const long long tiles = ((long long)a.max_query_len * G + C::kRows - 1) / C::kRows;
+  const long long tiles =
+      ((long long)a.max_query_len * G + C::kTiles * C::kRows - 1) / (C::kTiles * C::kRows);
   if (tiles == 0 || a.num_seqs == 0) return cudaSuccess;
-  if (tiles > 0x7FFFFFFFll) {
-    *why = "max_query_len * heads per KV head is too large";
+  if (tiles * a.num_kv_heads * a.num_seqs > 0x7FFFFFFFll) {
+    *why = "too many CTAs: max_query_len * heads per KV head * sequences";
     return cudaErrorInvalidValue;
   }
   alignas(64) CUtensorMap tk;
   alignas(64) CUtensorMap tv;
-  if (!encode_kv_tensor_map_planes(&tk, a.k_cache, a.num_blocks, a.num_kv_heads, D, 2, why) ||
-      !encode_kv_tensor_map_planes(&tv, a.v_cache, a.num_blocks, a.num_kv_heads, D, 2, why)) {
+  if (!encode_kv_tensor_map_planes(&tk, a.k_cache, a.num_blocks, a.num_kv_heads, D, 2, 1, why) ||
+      !encode_kv_tensor_map_planes(&tv, a.v_cache, a.num_blocks, a.num_kv_heads, D, 2, 1, why)) {
     return cudaErrorInvalidValue;
   }
   // Opt in to more than 48 KB of dynamic shared memory, once per device.
@@ -61,7 +62,7 @@ cudaError_t launch_prefill_instance(const PrefillArgs& a, cudaStream_t stream, c
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)tiles, (unsigned)a.num_kv_heads, (unsigned)a.num_seqs);
+  cfg.gridDim = dim3((unsigned)(tiles * a.num_kv_heads * a.num_seqs));
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;

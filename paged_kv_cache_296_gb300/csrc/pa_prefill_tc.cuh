@@ -4,24 +4,31 @@
 // query at position p of sequence i, head h, attends to that sequence's tokens
 // 0..p of KV head h / G through its block table.
 //
-// One CTA per (tile of 128 rows, KV head, sequence); a row is one (query token,
-// query head of the KV head's group) pair, token-major.  192 threads:
-//   * warps 0-3 (softmax): thread r owns row r, which is TMEM lane r.  They
+// One CTA per (two tiles of 128 rows, KV head, sequence), one CTA per SM; a
+// row is one (query token, query head of the KV head's group) pair,
+// token-major.  Keys go in chunks of 128 (8 blocks).  320 threads:
+//   * warps 0-3 and 4-7 (softmax, one group per tile): thread r owns row r of
+//     its tile, which is TMEM lane r of the tile's 256 columns.  They
 //     stage Q into shared memory, run the online softmax on each S chunk read
-//     from TMEM, write P (16-bit) back to TMEM, rescale O in TMEM when a row's
+//     from TMEM, write P (16-bit) back over it, rescale O in TMEM when a row's
 //     running maximum grows by more than kRescale (log2 units; otherwise the
 //     exponentials keep the older maximum, so P stays below 2^kRescale), and
 //     finally normalise O and store the rows.
-//   * warp 4 (producer): TMA loads of the sequence's K/V blocks into a ring of
-//     full/empty mbarriers (piece-major 128B-swizzled tiles), and zeroes the
-//     V rows past the context's end in the last block (a P of 0 times a stale
-//     or poisoned V must not reach the sum).
-//   * warp 5 (MMA): owns the TMEM allocation; one thread issues, per chunk of
-//     two blocks (32 keys), S = Q K^T (M = 128, N = 16 per block, K = head
-//     size: kind::f16, A and B from shared memory) into one of two S buffers,
-//     then O += P V for the previous chunk (A = P from TMEM, B = the V tile,
-//     MN-major, N = head size, K = 16 per block), and releases ring stages,
-//     S and P buffers with tcgen05.commit.
+//   * warp 8 (producer): TMA loads of the chunks' K and V blocks into two
+//     rings (K and V, each with full/empty mbarriers per chunk; K is released
+//     as soon as S has read it, V after P V).  The rings are plane-major: each
+//     128-byte piece of the rows has its own plane, 128B-swizzled, so the 8
+//     blocks of a chunk are one 128-row operand.  It also zeroes the V rows
+//     past the context's end in the last block (a P of 0 times a stale or
+//     poisoned V must not reach the sum).
+//   * warp 9 (MMA): owns the TMEM allocation; one thread issues, tile by tile,
+//     O_t += P_t(c) V(c) (A = P from TMEM, B = each block's V rows, MN-major,
+//     N = head size, K = 16) and then S_t(c + 1) = Q_t K(c + 1)^T (M = 128,
+//     N = 128 keys, K = head size, A and B from shared memory) into the
+//     columns P_t(c) occupied.  One thread's MMAs run in order, so P V(c) has
+//     read P(c) before S(c + 1) overwrites it, and a completed S(c + 1) means
+//     P V(c) is done too (the softmax may rescale O then).  The tensor core
+//     works on one tile while the other tile's softmax runs.
 // Accumulation in fp32 throughout; every wait is bounded.
 #pragma once
 
@@ -32,24 +39,37 @@ namespace pa {
 
 template <int D>
 struct PrefillTcCfg {
-  static constexpr int kRows = 128;
+  static constexpr int kRows = 128;                        // rows of one tile (TMEM lanes)
+  static constexpr int kTiles = 2;                         // tiles per CTA, one softmax group each
   static constexpr int kPieces = D * 2 / 128;              // 128-byte pieces of a row
-  static constexpr int kQBytes = kRows * D * 2;            // [pieces][128 rows][128 B]
-  static constexpr int kTileBytes = 16 * D * 2;            // one block of K (or V), one head
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kStages = (kStageBytes >= 8192) ? 8 : 16;  // 64 KB ring
-  static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kBarOff = kQBytes + kRingBytes;
-  // barriers: full, empty per stage; s_full, s_free, p_full, pv_done x2; q_ready, tail, o_done
-  static constexpr int kNumBars = 2 * kStages + 8 + 3;
+  static constexpr int kQTileBytes = kRows * D * 2;        // [pieces][128 rows][128 B]
+  static constexpr int kQBytes = kTiles * kQTileBytes;
+  static constexpr int kBlocksPerChunk = 8;                // 128 keys per S = Q K^T
+  static constexpr int kBlockBytes = 16 * 128;             // one block, one piece: [16][128 B]
+  static constexpr int kChunkBytes = kBlocksPerChunk * kBlockBytes;  // one chunk, one piece
+  static constexpr int kRingBytes = 128 * 1024;            // K and V planes
+  static constexpr int kRing = kRingBytes / (2 * kPieces * kChunkBytes);  // chunks per ring
+  static constexpr int kPlaneBytes = kRing * kChunkBytes;  // one piece plane of K (or V)
+  static constexpr int kKOff = kQBytes;                    // K: [pieces][ring rows][128 B]
+  static constexpr int kVOff = kKOff + kPieces * kPlaneBytes;
+  static constexpr int kBarOff = kVOff + kPieces * kPlaneBytes;
+  // barriers: K full / empty, V full / empty per ring slot; s_full, p_full per
+  // tile; q_ready, tail, o_done
+  static constexpr int kNumBars = 4 * kRing + 2 * kTiles + 3;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
-  static constexpr int kThreads = 192;
-  // TMEM columns: O [0, D), S buffers at kS0 + 32 b, P buffers at kP0 + 16 b
-  static constexpr int kS0 = D;
-  static constexpr int kP0 = D + 64;
-  static constexpr int kTmemCols = 256;
+  static constexpr int kSoftmaxThreads = 128 * kTiles;
+  static constexpr int kProducerWarp = kSoftmaxThreads / 32;
+  static constexpr int kMmaWarp = kProducerWarp + 1;
+  static constexpr int kThreads = kSoftmaxThreads + 64;
+  // TMEM columns of tile t (base 256 t): O [0, D); S(c) in fp32 at [128, 256),
+  // then P(c) (16-bit pairs) over its first 64 columns once the softmax has read it
+  static constexpr int kTileCols = 256;
+  static constexpr int kS0 = 128;
+  static constexpr int kTmemCols = kTileCols * kTiles;
   static constexpr float kRescale = 8.f;
-  static_assert(kP0 + 32 <= kTmemCols, "TMEM layout");
+  static_assert(D <= kS0 && kS0 + 128 <= kTileCols && kTmemCols <= 512, "TMEM layout");
+  static_assert(kRing >= 2, "ring of at least two chunks");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -109,6 +129,54 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 64 consecutive columns of the warp's 32 lanes, and the wait for them, in
+// one statement (no use of a register can be scheduled before the wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Packed pairs of fp32 (the f32x2 forms of fma / add).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t x) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+  return make_float2(lo, hi);
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -136,77 +204,80 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+
 template <int D, int QT>
 __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
   using C = PrefillTcCfg<D>;
+  constexpr unsigned kAll = 0xffffffffu;
+  constexpr int kT = C::kTiles;
+  constexpr int kR = C::kRing;
+  constexpr int kBpc = C::kBlocksPerChunk;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* full_bar = bars;
-  uint64_t* empty_bar = bars + C::kStages;
-  uint64_t* s_full = bars + 2 * C::kStages;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_full + 4;
-  uint64_t* pv_done = s_full + 6;
-  uint64_t* q_ready = s_full + 8;
-  uint64_t* tail_bar = s_full + 9;
-  uint64_t* o_done = s_full + 10;
+  uint64_t* full_k = bars;  // [kR] each
+  uint64_t* empty_k = bars + kR;
+  uint64_t* full_v = bars + 2 * kR;
+  uint64_t* empty_v = bars + 3 * kR;
+  uint64_t* s_full = bars + 4 * kR;  // [kT] each
+  uint64_t* p_full = s_full + kT;
+  uint64_t* q_ready = p_full + kT;
+  uint64_t* tail_bar = q_ready + 1;
+  uint64_t* o_done = q_ready + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 4 * 32) {
+  if (threadIdx.x == C::kProducerWarp * 32) {
     tma_prefetch_desc(&tmap_k);
     tma_prefetch_desc(&tmap_v);
   }
   griddep_wait();
 
-  const int seq = blockIdx.z;
-  const int kvh = blockIdx.y;
-  const int tile = p.tiles - 1 - (int)blockIdx.x;  // heaviest tiles first
+  // one flat grid, KV head fastest and tile slowest, tiles in reverse: every
+  // CTA of the heaviest (last) tile index starts before any lighter one
+  const int kvh = (int)(blockIdx.x % (unsigned)p.num_kv_heads);
+  const int seq = (int)((blockIdx.x / (unsigned)p.num_kv_heads) % (unsigned)p.num_seqs);
+  const int group_tile =
+      p.tiles - 1 - (int)(blockIdx.x / ((unsigned)p.num_kv_heads * (unsigned)p.num_seqs));
   const int r0q = p.query_start_loc[seq];
   const int nq = p.query_start_loc[seq + 1] - r0q;
   const int L = min(p.context_lens[seq], p.max_blocks_per_seq * 16);
   if (nq <= 0) return;
   if (nq > L || nq > p.max_query_len) {
-    if (threadIdx.x == 0 && tile == 0 && kvh == 0) atomicOr(p.status, kErrBadQueryLayout);
+    if (threadIdx.x == 0 && group_tile == 0 && kvh == 0) atomicOr(p.status, kErrBadQueryLayout);
     return;
   }
   const int G = p.group;
   const int rows = nq * G;
-  const int row0 = tile * C::kRows;
+  const int row0 = group_tile * kT * C::kRows;  // the CTA's first row (tile 0), tile t at + 128 t
   if (row0 >= rows) return;
-  const int last_row = min(rows, row0 + C::kRows) - 1;
+  const int last_row = min(rows, row0 + kT * C::kRows) - 1;
   const int last_pos = L - nq + last_row / G;
   const int nkb = last_pos / 16 + 1;
-  const int nchunks = (nkb + 1) / 2;
+  const int nchunks = (nkb + kBpc - 1) / kBpc;
   // The last block holds keys past the context's end when it is the block of
   // position L - 1 and L is not a multiple of 16.
   const bool has_tail = (nkb - 1 == (L - 1) / 16) && (L % 16 != 0);
   const bool bf16 = QT == 1;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+    for (int i = 0; i < 4 * kR; ++i) mbar_init(&bars[i], 1);
+    for (int t = 0; t < kT; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 128);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], 128);
-      mbar_init(&p_full[b], 128);
-      mbar_init(&pv_done[b], 1);
-    }
-    mbar_init(q_ready, 128);
+    mbar_init(q_ready, C::kSoftmaxThreads);
     mbar_init(tail_bar, 1);
     mbar_init(o_done, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 5) {
+  if (warp == C::kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(C::kTmemCols));
@@ -220,219 +291,254 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
   auto fail = [&]() { atomicExch(abort_flag, 1); };
   auto aborted = [&]() { return *reinterpret_cast<volatile int*>(abort_flag) != 0; };
 
-  if (warp == 4) {
+  if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
+    // Chunk c goes to ring slot c % kR: block j of it lands at rows
+    // 16 j .. 16 j + 15 of the slot in each piece's plane, K then V.
     const int32_t* tbl = p.block_tables + (size_t)seq * p.max_blocks_per_seq;
     const int oob_row = p.num_blocks * 16;
     const uint64_t pol = l2_evict_normal_policy();
-    int issued = 0;
-    for (int base = 0; base < nkb; base += 32) {  // warp-uniform bounds (shuffles inside)
-      const int mine = (base + lane < nkb) ? __ldg(tbl + base + lane) : 0;
-      const int cnt = min(32, nkb - base);
-      for (int j = 0; j < cnt; ++j) {
-        const int blk = __shfl_sync(0xffffffffu, mine, j);
-        if (lane == 0 && !aborted()) {
-          const int it = base + j;
-          const int s = it % C::kStages;
-          if (!mbar_wait_bounded(&empty_bar[s], ((uint32_t)(it / C::kStages) & 1u) ^ 1u, p.status)) {
-            fail();
-          } else {
-            const int row = (blk >= 0 && blk < p.num_blocks) ? blk * 16 : oob_row;
-            uint8_t* ks = smem + C::kQBytes + s * C::kStageBytes;
-            mbar_arrive_expect_tx(&full_bar[s], C::kStageBytes);
-            tma_load_4d(ks, &tmap_k, &full_bar[s], 0, row, 0, kvh, pol);
-            tma_load_4d(ks + C::kTileBytes, &tmap_v, &full_bar[s], 0, row, 0, kvh, pol);
-            ++issued;
-          }
-        }
+    int issued = 0;  // chunks whose K and V are both in flight
+    for (int c = 0; c < nchunks; ++c) {
+      // lane j < nblk loads block j of the chunk, once lane 0 holds the slot
+      const int b0 = kBpc * c;
+      const int nblk = min(kBpc, nkb - b0);
+      const int blk = lane < nblk ? __ldg(tbl + b0 + lane) : 0;
+      const int brow = (blk >= 0 && blk < p.num_blocks) ? blk * 16 : oob_row;
+      const int slot = c % kR;
+      const uint32_t ph = ((uint32_t)(c / kR) & 1u) ^ 1u;
+      const uint32_t bytes = (uint32_t)(nblk * C::kPieces * C::kBlockBytes);
+      const uint32_t off = slot * C::kChunkBytes + lane * C::kBlockBytes;
+      int ok = 0;
+      if (lane == 0 && !aborted() && mbar_wait_bounded(&empty_k[slot], ph, p.status)) {
+        mbar_arrive_expect_tx(&full_k[slot], bytes);
+        ok = 1;
       }
+      if (!__shfl_sync(kAll, ok, 0)) break;
+      if (lane < nblk) {
+#pragma unroll
+        for (int pc = 0; pc < C::kPieces; ++pc)
+          tma_load_4d(smem + C::kKOff + pc * C::kPlaneBytes + off, &tmap_k, &full_k[slot], 0, brow,
+                      pc, kvh, pol);
+      }
+      ok = 0;
+      if (lane == 0 && !aborted() && mbar_wait_bounded(&empty_v[slot], ph, p.status)) {
+        mbar_arrive_expect_tx(&full_v[slot], bytes);
+        ok = 1;
+      }
+      if (!__shfl_sync(kAll, ok, 0)) break;
+      if (lane < nblk) {
+#pragma unroll
+        for (int pc = 0; pc < C::kPieces; ++pc)
+          tma_load_4d(smem + C::kVOff + pc * C::kPlaneBytes + off, &tmap_v, &full_v[slot], 0, brow,
+                      pc, kvh, pol);
+      }
+      ++issued;
     }
-    if (lane == 0 && has_tail && !aborted() && issued == nkb) {
-      // zero the V rows of keys L .. 16 * nkb - 1 once the last block has landed
-      const int it = nkb - 1;
-      const int s = it % C::kStages;
-      if (!mbar_wait_bounded(&full_bar[s], (uint32_t)(it / C::kStages) & 1u, p.status)) {
+    if (issued < nchunks && lane == 0) fail();
+    if (lane == 0 && has_tail && !aborted() && issued == nchunks) {
+      // zero the V rows of keys L .. 16 * nkb - 1 once the last chunk's V has landed
+      const int c = nchunks - 1;
+      const int slot = c % kR;
+      const int j = nkb - 1 - kBpc * c;
+      if (!mbar_wait_bounded(&full_v[slot], (uint32_t)(c / kR) & 1u, p.status)) {
         fail();
       } else {
-        uint8_t* vs = smem + C::kQBytes + s * C::kStageBytes + C::kTileBytes;
         for (int key = L % 16; key < 16; ++key) {
-          for (int piece = 0; piece < C::kPieces; ++piece) {
-            uint4* row = reinterpret_cast<uint4*>(vs + piece * 16 * 128 + key * 128);
+          for (int pc = 0; pc < C::kPieces; ++pc) {
+            uint4* row = reinterpret_cast<uint4*>(smem + C::kVOff + pc * C::kPlaneBytes +
+                                                  slot * C::kChunkBytes + j * C::kBlockBytes +
+                                                  key * 128);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+            for (int i = 0; i < 8; ++i) row[i] = make_uint4(0u, 0u, 0u, 0u);
           }
         }
         fence_proxy_async_shared();
         mbar_arrive(tail_bar);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = umma_idesc(bf16, 128, 16, 0);
+      const uint32_t id_s = umma_idesc(bf16, 128, 16 * kBpc, 0);
       const uint32_t id_pv = umma_idesc(bf16, 128, D, 1);
-      bool ok = mbar_wait_bounded(q_ready, 0, p.status);
-      tc_fence_after();
-      auto issue_pv = [&](int c) {  // O += P(c) V(c); release its stages and P buffer
-        const int b = c & 1;
-        if (!mbar_wait_bounded(&p_full[b], (uint32_t)(c >> 1) & 1u, p.status)) return false;
-        tc_fence_after();
-        for (int j = 0; j < 2; ++j) {
-          const int it = 2 * c + j;
-          if (it >= nkb) break;
-          if (has_tail && it == nkb - 1) {
-            if (!mbar_wait_bounded(tail_bar, 0, p.status)) return false;
-            tc_fence_after();
-          }
-          const int s = it % C::kStages;
-          const uint32_t vaddr = sbase + C::kQBytes + s * C::kStageBytes + C::kTileBytes;
-          umma_ts(tmem + 0, tmem + C::kP0 + 16 * b + 8 * j, umma_desc_sw128(vaddr, 2048, 1024),
-                  id_pv, (c > 0 || j > 0) ? 1 : 0);
-          umma_commit(&empty_bar[s]);
-        }
-        umma_commit(&pv_done[b]);
-        return true;
-      };
-      for (int c = 0; c < nchunks && ok; ++c) {
-        const int b = c & 1;
-        if (c >= 2 && !mbar_wait_bounded(&s_free[b], (uint32_t)((c - 2) >> 1) & 1u, p.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        for (int j = 0; j < 2 && ok; ++j) {
-          const int it = 2 * c + j;
-          if (it >= nkb) break;
-          const int s = it % C::kStages;
-          if (!mbar_wait_bounded(&full_bar[s], (uint32_t)(it / C::kStages) & 1u, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t kaddr = sbase + C::kQBytes + s * C::kStageBytes;
+      auto issue_s = [&](int t, int c) {  // S_t(c) = Q_t K(c)^T
+        const int slot = c % kR;
+        const uint32_t dcol = tmem + t * C::kTileCols + C::kS0;
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t qoff = (k / 4) * (C::kRows * 128) + (k % 4) * 32;
-            const uint32_t koff = (k / 4) * (16 * 128) + (k % 4) * 32;
-            umma_ss(tmem + C::kS0 + 32 * b + 16 * j, umma_desc_sw128(sbase + qoff, 16, 1024),
-                    umma_desc_sw128(kaddr + koff, 16, 1024), id_s, k > 0 ? 1 : 0);
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t qoff = t * C::kQTileBytes + (k / 4) * (C::kRows * 128) + (k % 4) * 32;
+          const uint32_t koff =
+              C::kKOff + (k / 4) * C::kPlaneBytes + slot * C::kChunkBytes + (k % 4) * 32;
+          umma_ss(dcol, umma_desc_sw128(sbase + qoff, 16, 1024),
+                  umma_desc_sw128(sbase + koff, 16, 1024), id_s, k > 0 ? 1 : 0);
+        }
+        umma_commit(&s_full[t]);
+      };
+      bool ok = mbar_wait_bounded(q_ready, 0, p.status) &&
+                mbar_wait_bounded(&full_k[0], 0, p.status);
+      tc_fence_after();
+      if (ok) {
+        for (int t = 0; t < kT; ++t) issue_s(t, 0);
+        umma_commit(&empty_k[0]);
+      }
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int slot = c % kR;
+        const int nblk = min(kBpc, nkb - kBpc * c);
+        const bool more = c + 1 < nchunks;
+        ok = mbar_wait_bounded(&full_v[slot], (uint32_t)(c / kR) & 1u, p.status);
+        if (ok && has_tail && !more) ok = mbar_wait_bounded(tail_bar, 0, p.status);
+        for (int t = 0; t < kT && ok; ++t) {
+          // O_t += P_t(c) V(c), then S_t(c + 1) into the same columns
+          ok = mbar_wait_bounded(&p_full[t], (uint32_t)c & 1u, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t pcol = tmem + t * C::kTileCols + C::kS0;
+          for (int j = 0; j < nblk; ++j) {
+            const uint32_t vaddr = sbase + C::kVOff + slot * C::kChunkBytes + j * C::kBlockBytes;
+            umma_ts(tmem + t * C::kTileCols, pcol + 8 * j,
+                    umma_desc_sw128(vaddr, C::kPlaneBytes, 1024), id_pv, (c > 0 || j > 0) ? 1 : 0);
+          }
+          if (t == kT - 1) umma_commit(&empty_v[slot]);
+          if (more) {
+            if (t == 0) {
+              ok = mbar_wait_bounded(&full_k[(c + 1) % kR], (uint32_t)((c + 1) / kR) & 1u,
+                                     p.status);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_s(t, c + 1);
+            if (t == kT - 1) umma_commit(&empty_k[(c + 1) % kR]);
           }
         }
-        if (!ok) break;
-        umma_commit(&s_full[b]);
-        if (c >= 1 && !issue_pv(c - 1)) ok = false;
       }
-      if (ok && !issue_pv(nchunks - 1)) ok = false;
       if (ok) umma_commit(o_done);
       if (!ok) fail();
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax warps
-    const int r = threadIdx.x;  // row of the tile, TMEM lane
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-    const int R = row0 + r;
+    // ------------------------------------------------------------ softmax groups
+    // Group t (warps 4t .. 4t+3) owns tile t; thread r of the group owns row r
+    // of the tile (TMEM lane r).  tcgen05.ld / st are warp-collective: every
+    // decision that guards one is made uniform across the warp first.
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      const bool w = mbar_wait_bounded(bar, parity, p.status);
+      return __all_sync(kAll, w) && !__any_sync(kAll, aborted());
+    };
+    const int t = threadIdx.x >> 7;
+    const int r = threadIdx.x & 127;
+    const uint32_t tcol = tmem + t * C::kTileCols;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t scol = tcol + lane_base + C::kS0;  // S(c), then P(c)
+    const int R = row0 + t * C::kRows + r;
     const bool live = R < rows;
     const int RR = live ? R : rows - 1;
     const int tok = RR / G;
     const int pos = L - nq + tok;
     const size_t qoff = ((size_t)(r0q + tok) * p.num_q_heads + (size_t)kvh * G + (RR - tok * G)) * D;
-    // stage Q: row r, piece-major, 128B-swizzled (zeros for rows past the tile's end)
+    // stage Q: row r of tile t, piece-major, 128B-swizzled (zeros past the rows)
     {
       const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) + qoff);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
         const uint4 v = live ? src[c] : make_uint4(0u, 0u, 0u, 0u);
         const int piece = c / 8, cc = c % 8;
-        *reinterpret_cast<uint4*>(smem + piece * (C::kRows * 128) + r * 128 + ((cc ^ (r & 7)) * 16)) = v;
+        *reinterpret_cast<uint4*>(smem + t * C::kQTileBytes + piece * (C::kRows * 128) + r * 128 +
+                                  ((cc ^ (r & 7)) * 16)) = v;
       }
       fence_proxy_async_shared();
       mbar_arrive(q_ready);
     }
-    // tcgen05.ld / st are warp-collective: every decision that guards one is
-    // made uniform across the warp (vote) before it is acted on.
-    constexpr unsigned kAll = 0xffffffffu;
-    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-      const bool w = mbar_wait_bounded(bar, parity, p.status);
-      return __all_sync(kAll, w) && !__any_sync(kAll, aborted());
-    };
+    const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
     float m_run = -INFINITY, m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int c = 0; c < nchunks; ++c) {
-      const int b = c & 1;
-      if (!wait_all(&s_full[b], (uint32_t)(c >> 1) & 1u)) {
+      if (!wait_all(&s_full[t], (uint32_t)c & 1u)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[32];
-      {
-        float a[16], bb[16];
-        tmem_ld16(tmem + lane_base + C::kS0 + 32 * b, a);
-        tmem_ld16(tmem + lane_base + C::kS0 + 32 * b + 16, bb);
+      float s0[64], s1[64];
+      tmem_ld64(scol, s0);
+      tmem_ld64(scol + 64, s1);
+      const int key0 = 128 * c;
+      if (__any_sync(kAll, key0 + 127 > pos)) {
+        // causal (also covers keys past L and past the last block)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          s[i] = a[i];
-          s[16 + i] = bb[i];
+        for (int i = 0; i < 64; ++i) {
+          if (key0 + i > pos) s0[i] = -INFINITY;
+          if (key0 + 64 + i > pos) s1[i] = -INFINITY;
         }
       }
-      tc_fence_before();
-      mbar_arrive(&s_free[b]);
-      const int key0 = 32 * c;
-      float mx = m_run;
+      // the maximum of the raw scores (the scale is positive, so it commutes)
+      float mq[16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float v = __fmul_rn(s[i], p.scale_log2);
-        if (key0 + i > pos) v = -INFINITY;  // causal (also covers keys past L and a missing block)
-        s[i] = v;
-        mx = fmaxf(mx, v);
+      for (int k = 0; k < 8; ++k) {
+        mq[k] = fmax3(s0[8 * k], s0[8 * k + 1], s0[8 * k + 2]);
+        mq[8 + k] = fmax3(s1[8 * k], s1[8 * k + 1], s1[8 * k + 2]);
       }
-      m_run = mx;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        mq[k] = fmax3(mq[k], s0[8 * k + 3], s0[8 * k + 4]);
+        mq[8 + k] = fmax3(mq[8 + k], s1[8 * k + 3], s1[8 * k + 4]);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        mq[k] = fmax3(mq[k], s0[8 * k + 5], s0[8 * k + 6]);
+        mq[8 + k] = fmax3(mq[8 + k], s1[8 * k + 5], s1[8 * k + 6]);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mq[k] = fmax3(mq[k], s0[8 * k + 7], s1[8 * k + 7]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mq[k] = fmaxf(mq[k], mq[8 + k]);
+      const float mx = fmax3(fmax3(mq[0], mq[1], mq[2]), fmax3(mq[3], mq[4], mq[5]),
+                             fmaxf(mq[6], mq[7]));
+      m_run = fmaxf(m_run, __fmul_rn(mx, p.scale_log2));
       const bool need = m_run > m_used + C::kRescale;
       if (c > 0 && __any_sync(kAll, need)) {
-        // rescale O (and l) of the rows that need it, once every earlier P V
-        // has landed; the warp's other rows take part with a factor of 1
-        if (!wait_all(&pv_done[(c - 1) & 1], (uint32_t)((c - 1) >> 1) & 1u)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        // rescale O (and l) of the rows that need it: S(c) completed after
+        // P V(c - 1), so O holds every earlier chunk; the warp's other rows take
+        // part with a factor of 1
         const float alpha = need ? ex2_approx(__fsub_rn(m_used, m_run)) : 1.f;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 16) {
           float o[16];
-          tmem_ld16(tmem + lane_base + c0, o);
+          tmem_ld16(tcol + lane_base + c0, o);
 #pragma unroll
           for (int i = 0; i < 16; ++i) o[i] = __fmul_rn(o[i], alpha);
-          tmem_st16(tmem + lane_base + c0, o);
+          tmem_st16(tcol + lane_base + c0, o);
         }
-        tmem_wait_st();
         l = __fmul_rn(l, alpha);
       }
       if (need) m_used = m_run;
-      // P buffer b was read by the P V of chunk c - 2: wait until it is done
-      if (c >= 2) {
-        if (!wait_all(&pv_done[b], (uint32_t)((c - 2) >> 1) & 1u)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
-      uint32_t pk[16];
-      float rs = 0.f;
+      // p = 2^(s * scale_log2 - m_used), one rounding per exponent; P(c) goes
+      // over the first 64 columns (half h at 32 h, after all of S(c) was read);
+      // the row sum in fp32 over interleaved partial sums of pairs
+      const uint64_t nm2 = f2_pack(-m_used, -m_used);
+      uint64_t acc0 = 0ull, acc1 = 0ull;
+      auto exp_half = [&](const float (&sh)[64], uint32_t col) {
+        uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float p0 = ex2_approx(__fsub_rn(s[2 * i], m_used));
-        const float p1 = ex2_approx(__fsub_rn(s[2 * i + 1], m_used));
-        pk[i] = pf_pack<QT>(p0, p1);
-        const float2 rr = pf_unpack<QT>(pk[i]);
-        rs = __fadd_rn(rs, __fadd_rn(rr.x, rr.y));
-      }
-      l = __fadd_rn(l, rs);
-      tmem_st16u(tmem + lane_base + C::kP0 + 16 * b, pk);
+        for (int i = 0; i < 32; i += 2) {
+          const float2 x = f2_unpack(f2_fma(f2_pack(sh[2 * i], sh[2 * i + 1]), sc2, nm2));
+          const float2 y = f2_unpack(f2_fma(f2_pack(sh[2 * i + 2], sh[2 * i + 3]), sc2, nm2));
+          const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+          const float p2 = ex2_approx(y.x), p3 = ex2_approx(y.y);
+          pk[i] = pf_pack<QT>(p0, p1);
+          pk[i + 1] = pf_pack<QT>(p2, p3);
+          acc0 = f2_add(acc0, f2_pack(p0, p1));
+          acc1 = f2_add(acc1, f2_pack(p2, p3));
+        }
+        tmem_st16u(col, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+        tmem_st16u(col + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+      };
+      exp_half(s0, scol);
+      exp_half(s1, scol + 32);
+      const float2 a0 = f2_unpack(acc0), a1 = f2_unpack(acc1);
+      l = __fadd_rn(l, __fadd_rn(__fadd_rn(a0.x, a0.y), __fadd_rn(a1.x, a1.y)));
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[b]);
+      mbar_arrive(&p_full[t]);
     }
     if (ok) ok = wait_all(o_done, 0);
     if (!ok) fail();
@@ -443,7 +549,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 16) {
         float o[16];
-        tmem_ld16(tmem + lane_base + c0, o);
+        tmem_ld16(tcol + lane_base + c0, o);
         uint32_t w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -460,7 +566,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == C::kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(C::kTmemCols));
