@@ -85,6 +85,19 @@ __device__ __forceinline__ uint32_t umma_idesc(bool bf16, int m, int n, int b_mn
          ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// The same descriptor split in two words: the low word holds the start address
+// (bits 0-13, in 16-byte units) and the leading byte offset, the high word the
+// stride byte offset, the version bit and the swizzle mode.  Every shared
+// address here is below 2^18, so adding a byte offset / 16 to the low word
+// never carries out of the address field.
+__device__ __forceinline__ uint32_t umma_desc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+constexpr uint32_t kUmmaDescHiSw128 = (1024u >> 4) | (1u << 14) | (2u << 29);  // SBO 1024
+__device__ __forceinline__ uint64_t umma_desc_join(uint32_t lo) {
+  return ((uint64_t)kUmmaDescHiSw128 << 32) | lo;
+}
+
 __device__ __forceinline__ void umma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, int acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -362,16 +375,20 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
     if (lane == 0) {
       const uint32_t id_s = umma_idesc(bf16, 128, 16 * kBpc, 0);
       const uint32_t id_pv = umma_idesc(bf16, 128, D, 1);
+      // descriptors are formed once; an operand's step is a constant added to the low word
+      const uint32_t q_lo = umma_desc_lo(sbase, 16);
+      const uint32_t k_lo = umma_desc_lo(sbase + C::kKOff, 16);
+      const uint32_t v_lo = umma_desc_lo(sbase + C::kVOff, C::kPlaneBytes);
       auto issue_s = [&](int t, int c) {  // S_t(c) = Q_t K(c)^T
-        const int slot = c % kR;
         const uint32_t dcol = tmem + t * C::kTileCols + C::kS0;
+        const uint32_t qa = q_lo + (uint32_t)(t * C::kQTileBytes >> 4);
+        const uint32_t ka = k_lo + (uint32_t)((c % kR) * C::kChunkBytes >> 4);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t qoff = t * C::kQTileBytes + (k / 4) * (C::kRows * 128) + (k % 4) * 32;
-          const uint32_t koff =
-              C::kKOff + (k / 4) * C::kPlaneBytes + slot * C::kChunkBytes + (k % 4) * 32;
-          umma_ss(dcol, umma_desc_sw128(sbase + qoff, 16, 1024),
-                  umma_desc_sw128(sbase + koff, 16, 1024), id_s, k > 0 ? 1 : 0);
+          constexpr int kQStep = C::kRows * 128;
+          const uint32_t qo = (uint32_t)(((k / 4) * kQStep + (k % 4) * 32) >> 4);
+          const uint32_t ko = (uint32_t)(((k / 4) * C::kPlaneBytes + (k % 4) * 32) >> 4);
+          umma_ss(dcol, umma_desc_join(qa + qo), umma_desc_join(ka + ko), id_s, k > 0 ? 1 : 0);
         }
         umma_commit(&s_full[t]);
       };
@@ -394,10 +411,11 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t pcol = tmem + t * C::kTileCols + C::kS0;
+          const uint32_t va = v_lo + (uint32_t)(slot * C::kChunkBytes >> 4);
           for (int j = 0; j < nblk; ++j) {
-            const uint32_t vaddr = sbase + C::kVOff + slot * C::kChunkBytes + j * C::kBlockBytes;
             umma_ts(tmem + t * C::kTileCols, pcol + 8 * j,
-                    umma_desc_sw128(vaddr, C::kPlaneBytes, 1024), id_pv, (c > 0 || j > 0) ? 1 : 0);
+                    umma_desc_join(va + (uint32_t)(j * (C::kBlockBytes >> 4))), id_pv,
+                    (c > 0 || j > 0) ? 1 : 0);
           }
           if (t == kT - 1) umma_commit(&empty_v[slot]);
           if (more) {
