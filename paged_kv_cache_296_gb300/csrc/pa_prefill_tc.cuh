@@ -10,7 +10,8 @@
 //   * warps 0-3 and 4-7 (softmax, one group per tile): thread r owns row r of
 //     its tile, which is TMEM lane r of the tile's 256 columns.  They
 //     stage Q into shared memory, run the online softmax on each S chunk read
-//     from TMEM, write P (16-bit) back over it, rescale O in TMEM when a row's
+//     from TMEM, write P (16-bit) back over it (keys 0..63 at columns 0..31,
+//     keys 64..127 at 64..95), rescale O in TMEM when a row's
 //     running maximum grows by more than kRescale (log2 units; otherwise the
 //     exponentials keep the older maximum, so P stays below 2^kRescale), and
 //     finally normalise O and store the rows.
@@ -62,7 +63,8 @@ struct PrefillTcCfg {
   static constexpr int kMmaWarp = kProducerWarp + 1;
   static constexpr int kThreads = kSoftmaxThreads + 64;
   // TMEM columns of tile t (base 256 t): O [0, D); S(c) in fp32 at [128, 256),
-  // then P(c) (16-bit pairs) over its first 64 columns once the softmax has read it
+  // then P(c) (16-bit pairs) over it once the softmax has read it: keys 0..63
+  // at [128, 160), keys 64..127 at [192, 224)
   static constexpr int kTileCols = 256;
   static constexpr int kS0 = 128;
   static constexpr int kTmemCols = kTileCols * kTiles;
@@ -412,10 +414,16 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
           tc_fence_after();
           const uint32_t pcol = tmem + t * C::kTileCols + C::kS0;
           const uint32_t va = v_lo + (uint32_t)(slot * C::kChunkBytes >> 4);
-          for (int j = 0; j < nblk; ++j) {
-            umma_ts(tmem + t * C::kTileCols, pcol + 8 * j,
+          auto pv = [&](int j) {
+            umma_ts(tmem + t * C::kTileCols, pcol + 64 * (j / 4) + 8 * (j % 4),
                     umma_desc_join(va + (uint32_t)(j * (C::kBlockBytes >> 4))), id_pv,
                     (c > 0 || j > 0) ? 1 : 0);
+          };
+          if (nblk == kBpc) {
+#pragma unroll
+            for (int j = 0; j < kBpc; ++j) pv(j);
+          } else {
+            for (int j = 0; j < nblk; ++j) pv(j);
           }
           if (t == kT - 1) umma_commit(&empty_v[slot]);
           if (more) {
@@ -476,39 +484,43 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         break;
       }
       tc_fence_after();
-      float s0[64], s1[64];
-      tmem_ld64(scol, s0);
-      tmem_ld64(scol + 64, s1);
+      // Two passes over S(c) keep one 64-column half in registers at a time:
+      // the maxima of both halves, then half 1 (P at columns 64..95) and half 0
+      // read again (P at columns 0..31); each P half goes over S values already read.
       const int key0 = 128 * c;
-      if (__any_sync(kAll, key0 + 127 > pos)) {
-        // causal (also covers keys past L and past the last block)
+      const bool diag = __any_sync(kAll, key0 + 127 > pos);
+      auto load_half = [&](float (&sh)[64], int h) {
+        tmem_ld64(scol + 64 * h, sh);
+        if (diag) {
+          // causal (also covers keys past L and past the last block)
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          if (key0 + i > pos) s0[i] = -INFINITY;
-          if (key0 + 64 + i > pos) s1[i] = -INFINITY;
+          for (int i = 0; i < 64; ++i)
+            if (key0 + 64 * h + i > pos) sh[i] = -INFINITY;
         }
+      };
+      float mq[8];
+      {
+        float sh[64];
+        load_half(sh, 0);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mq[k] = fmax3(sh[8 * k], sh[8 * k + 1], sh[8 * k + 2]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mq[k] = fmax3(mq[k], sh[8 * k + 3], sh[8 * k + 4]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mq[k] = fmax3(mq[k], sh[8 * k + 5], sh[8 * k + 6]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mq[k] = fmaxf(mq[k], sh[8 * k + 7]);
       }
-      // the maximum of the raw scores (the scale is positive, so it commutes)
-      float mq[16];
+      float s1[64];
+      load_half(s1, 1);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        mq[k] = fmax3(s0[8 * k], s0[8 * k + 1], s0[8 * k + 2]);
-        mq[8 + k] = fmax3(s1[8 * k], s1[8 * k + 1], s1[8 * k + 2]);
-      }
+      for (int k = 0; k < 8; ++k) mq[k] = fmax3(mq[k], s1[8 * k], s1[8 * k + 1]);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        mq[k] = fmax3(mq[k], s0[8 * k + 3], s0[8 * k + 4]);
-        mq[8 + k] = fmax3(mq[8 + k], s1[8 * k + 3], s1[8 * k + 4]);
-      }
+      for (int k = 0; k < 8; ++k) mq[k] = fmax3(mq[k], s1[8 * k + 2], s1[8 * k + 3]);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        mq[k] = fmax3(mq[k], s0[8 * k + 5], s0[8 * k + 6]);
-        mq[8 + k] = fmax3(mq[8 + k], s1[8 * k + 5], s1[8 * k + 6]);
-      }
+      for (int k = 0; k < 8; ++k) mq[k] = fmax3(mq[k], s1[8 * k + 4], s1[8 * k + 5]);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mq[k] = fmax3(mq[k], s0[8 * k + 7], s1[8 * k + 7]);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mq[k] = fmaxf(mq[k], mq[8 + k]);
+      for (int k = 0; k < 8; ++k) mq[k] = fmax3(mq[k], s1[8 * k + 6], s1[8 * k + 7]);
       const float mx = fmax3(fmax3(mq[0], mq[1], mq[2]), fmax3(mq[3], mq[4], mq[5]),
                              fmaxf(mq[6], mq[7]));
       m_run = fmaxf(m_run, __fmul_rn(mx, p.scale_log2));
@@ -529,9 +541,8 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         l = __fmul_rn(l, alpha);
       }
       if (need) m_used = m_run;
-      // p = 2^(s * scale_log2 - m_used), one rounding per exponent; P(c) goes
-      // over the first 64 columns (half h at 32 h, after all of S(c) was read);
-      // the row sum in fp32 over interleaved partial sums of pairs
+      // p = 2^(s * scale_log2 - m_used), one rounding per exponent; the row
+      // sum in fp32 over interleaved partial sums of pairs
       const uint64_t nm2 = f2_pack(-m_used, -m_used);
       uint64_t acc0 = 0ull, acc1 = 0ull;
       auto exp_half = [&](const float (&sh)[64], uint32_t col) {
@@ -550,8 +561,12 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         tmem_st16u(col, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
         tmem_st16u(col + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
       };
-      exp_half(s0, scol);
-      exp_half(s1, scol + 32);
+      exp_half(s1, scol + 64);
+      {
+        float sh[64];
+        load_half(sh, 0);
+        exp_half(sh, scol);
+      }
       const float2 a0 = f2_unpack(acc0), a1 = f2_unpack(acc1);
       l = __fadd_rn(l, __fadd_rn(__fadd_rn(a0.x, a0.y), __fadd_rn(a1.x, a1.y)));
       tmem_wait_st();
