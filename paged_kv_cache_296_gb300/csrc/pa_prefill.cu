@@ -55,6 +55,11 @@ cudaError_t launch_prefill_instance(const PrefillArgs& a, cudaStream_t stream, c
   p.num_kv_heads = a.num_kv_heads;
   p.group = G;
   p.tiles = (int)tiles;
+  // Tiles of one (sequence, KV head) read the same K/V: when the pool is larger
+  // than half of L2 they run in adjacent bands of 8 so those reads hit in L2;
+  // a smaller pool stays in L2 anyway and the heaviest tiles simply go first.
+  const double pool_bytes = 2.0 * a.num_blocks * 16.0 * a.num_kv_heads * D * 2.0;
+  p.band = pool_bytes > 64.0 * 1024 * 1024 ? 8 : 1;
   p.scale_log2 = (float)((double)a.scale * 1.4426950408889634);
   // Programmatic stream serialisation: the grid may start while the kernel
   // before it drains (every thread waits for it before reading inputs).

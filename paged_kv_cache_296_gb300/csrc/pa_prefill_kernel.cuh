@@ -52,7 +52,8 @@ struct PrefillParams {
   int num_q_heads;
   int num_kv_heads;
   int group;                      // G = Hq / Hkv
-  int tiles;                      // grid.x: tiles of the longest allowed query run
+  int tiles;                      // CTAs per (sequence, KV head): tiles of the longest query run
+  int band;                       // tile indices per grid band (1: heaviest tiles first)
   float scale_log2;               // scale * log2(e)
 };
 

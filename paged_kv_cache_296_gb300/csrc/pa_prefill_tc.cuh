@@ -253,12 +253,32 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
   }
   griddep_wait();
 
-  // one flat grid, KV head fastest and tile slowest, tiles in reverse: every
-  // CTA of the heaviest (last) tile index starts before any lighter one
-  const int kvh = (int)(blockIdx.x % (unsigned)p.num_kv_heads);
-  const int seq = (int)((blockIdx.x / (unsigned)p.num_kv_heads) % (unsigned)p.num_seqs);
-  const int group_tile =
-      p.tiles - 1 - (int)(blockIdx.x / ((unsigned)p.num_kv_heads * (unsigned)p.num_seqs));
+  // One flat grid in bands of p.band tile indices, the heaviest (last) band
+  // first; within a band the tiles of one (sequence, KV head) are adjacent so
+  // that they run together and read its K/V through L2 once.  A band of 1
+  // starts every CTA of a heavier tile index before any lighter one.
+  int kvh, seq, group_tile;
+  {
+    const unsigned kBand = (unsigned)p.band;
+    const unsigned groups = (unsigned)p.num_kv_heads * (unsigned)p.num_seqs;
+    const unsigned full = ((unsigned)p.tiles / kBand) * kBand * groups;  // CTAs in full bands
+    unsigned band, group, in_band;
+    if (blockIdx.x < full) {
+      band = blockIdx.x / (kBand * groups);
+      const unsigned rem = blockIdx.x % (kBand * groups);
+      group = rem / kBand;
+      in_band = rem % kBand;
+    } else {
+      const unsigned tb = (unsigned)p.tiles % kBand;  // tiles of the last, partial band
+      const unsigned rem = blockIdx.x - full;
+      band = (unsigned)p.tiles / kBand;
+      group = rem / tb;
+      in_band = rem % tb;
+    }
+    kvh = (int)(group % (unsigned)p.num_kv_heads);
+    seq = (int)(group / (unsigned)p.num_kv_heads);
+    group_tile = p.tiles - 1 - (int)(band * kBand + in_band);
+  }
   const int r0q = p.query_start_loc[seq];
   const int nq = p.query_start_loc[seq + 1] - r0q;
   const int L = min(p.context_lens[seq], p.max_blocks_per_seq * 16);

@@ -89,12 +89,23 @@ def test_random_shapes(seed):
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("head_size,group", [(128, 1), (128, 4), (64, 8), (128, 6)])
 def test_tile_edges(dtype, head_size, group):
-    # query counts around the 64-row tile and the 16-token block
+    # query counts around the 128-row tile, the 256-row CTA and the 16-token block
     lens = [63, 64, 65, 200, 129, 16, 1]
     nq = [63, 64, 65, 130, 1, 16, 1]
     spec = wl.PrefillSpec("tile edges", len(lens), 2 * group, 2, head_size, dtype,
                           ("fixed", lens), ("fixed", nq), ("factor", 1.3))
     full_check(wl.make_prefill_workload(spec, 71, poison=True))
+
+
+def test_large_pool_runs_in_bands_with_a_partial_last_band():
+    # A pool larger than half of L2 puts the tiles of one (sequence, KV head)
+    # in adjacent bands of 8; 700 queries x 4 heads per KV head are 11 tiles
+    # of 256 rows, so the last band holds 3.
+    spec = wl.PrefillSpec("large pool", 3, 8, 2, 128, "bf16", ("fixed", [900, 1500, 760]),
+                          ("fixed", [700, 300, 650]), ("fixed", 4300))
+    W = wl.make_prefill_workload(spec, 23, poison=True)
+    assert W.pool.numel() * W.pool.element_size() > 64 * 1024 * 1024
+    full_check(W)
 
 
 def test_one_query_per_sequence_matches_decode():
