@@ -622,7 +622,7 @@ def run_prefill(args, world, rank, local):
                    "step": "pa_reshape_and_cache of the query tokens + pa_prefill",
                    "launch": launch, "l2": "K/V re-read by a sequence's tiles comes from L2",
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "tensor", "kernel": "paged_prefill_kernel (mma.sync m16n8k16)",
+        "roofline": {"bound": "tensor", "kernel": "paged_prefill_tc_kernel (tcgen05, S/P/O in TMEM)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "algorithmic_flops_per_launch": flops, "traffic": None},

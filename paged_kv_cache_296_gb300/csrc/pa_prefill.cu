@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "pa_internal.h"
-#include "pa_prefill_kernel.cuh"
+#include "pa_prefill_params.cuh"
 #include "pa_prefill_tc.cuh"
 
 namespace pa {

@@ -1,6 +1,6 @@
 // Paged prefill attention on the 5th-generation tensor cores (tcgen05 + TMEM).
 //
-// What it computes is the causal paged prefill of pa_prefill_kernel.cuh: the
+// What it computes is the causal paged prefill of pa_prefill_params.cuh: the
 // query at position p of sequence i, head h, attends to that sequence's tokens
 // 0..p of KV head h / G through its block table.
 //
@@ -34,7 +34,7 @@
 #pragma once
 
 #include "pa_ptx.cuh"
-#include "pa_prefill_kernel.cuh"
+#include "pa_prefill_params.cuh"
 
 namespace pa {
 
