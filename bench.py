@@ -106,9 +106,13 @@ def tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback bf16"
 
 
-def kernel_source_hash():
+PREFILL_SOURCES = ["pa_prefill_tc.cuh", "pa_prefill_params.cuh", "pa_prefill.cu", "pa_ptx.cuh",
+                   "pa_cache.cu", "pa_api.cu"]
+
+
+def kernel_source_hash(sources=None):
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in (sources or KERNEL_SOURCES):
         with open(os.path.join(ROOT, "paged_kv_cache_296_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -126,6 +130,21 @@ def profiled_traffic(config_id, step_path):
     m_src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     m_tr = re.search(r"dram_bytes_per_decode_call:\s*([0-9.eE+]+)", text)
     if not m_src or not m_tr or m_src.group(1) != kernel_source_hash():
+        return None
+    return float(m_tr.group(1))
+
+
+def profiled_prefill_traffic(n):
+    """DRAM bytes per pa_prefill call from the committed ncu summary of prefill
+    workload ``n``, if it still describes the current kernel source (else None)."""
+    path = os.path.join(PROFILE_DIR, f"paged_prefill_tc_kernel_prefill{n}.md")
+    try:
+        text = open(path, encoding="utf-8").read()
+    except OSError:
+        return None
+    m_src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"dram_bytes_per_prefill_call:\s*([0-9.eE+]+)", text)
+    if not m_src or not m_tr or m_src.group(1) != kernel_source_hash(PREFILL_SOURCES):
         return None
     return float(m_tr.group(1))
 
@@ -625,7 +644,8 @@ def run_prefill(args, world, rank, local):
         "roofline": {"bound": "tensor", "kernel": "paged_prefill_tc_kernel (tcgen05, S/P/O in TMEM)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                     "algorithmic_flops_per_launch": flops, "traffic": None},
+                     "algorithmic_flops_per_launch": flops,
+                     "traffic": profiled_prefill_traffic(args.prefill)},
         "gpu_launches": S.launches_per_step * n,
         "e2e": e2e, "cpu_baseline": cpu,
         "clocks": sampler.summary(t0, t1),
