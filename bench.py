@@ -213,36 +213,56 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle leg
 
-def oracle_sample(W, seconds, pool_cpu_rows):
-    """Time the float64 oracle over whole sequences of W until ``seconds`` pass.
+class OracleSampler:
+    """Times the float64 oracle on bounded samples of a decode workload.
 
-    ``pool_cpu_rows(blocks)`` returns the pool rows of those physical blocks
-    as raw bits on the host.  Returns (attended bytes processed, elapsed s,
-    sequences processed).
+    The unit of work is one sequence, all heads, over the first L' of its L
+    tokens (a decode over a shorter context): the oracle's ``paged_decode`` on
+    that problem.  L' is L when the time budget allows, else the share of it
+    the oracle's measured rate fits into the budget (at least one block), so a
+    sample never runs far past its budget.  Successive calls take the
+    sequences in turn.
     """
-    from oracle import paged_attention as ref  # test infrastructure: only this leg runs it
-    spec = W.spec
-    elt = 1 if spec.kv_dtype == "e4m3" else 2
-    q_bits = W.q.cpu()
-    q_bits = q_bits.view(torch.int16).numpy().view(np.uint16)
-    done_bytes, elapsed, nseq = 0, 0.0, 0
-    lens = W.context_lens.cpu().numpy()
-    tables = W.block_tables.cpu().numpy()
-    for i in range(spec.num_seqs):
-        L = int(lens[i])
-        nblk = -(-L // 16)
-        blocks = tables[i, :nblk].astype(np.int64)
-        pool = pool_cpu_rows(blocks)                      # [nblk, 16, 2, Hkv, D] bits
-        table = np.arange(max(nblk, 1))[None, :]
-        t = time.perf_counter()
-        ref.paged_decode(q_bits[i:i + 1], spec.q_dtype, pool, table, np.array([L]), W.scale,
-                         spec.kv_dtype, W.kv_scale)
-        elapsed += time.perf_counter() - t
-        done_bytes += L * spec.num_kv_heads * spec.head_size * 2 * elt
-        nseq += 1
-        if elapsed >= seconds:
-            break
-    return done_bytes, elapsed, nseq
+
+    def __init__(self, W, pool_cpu_rows):
+        self.W = W
+        self.rows_fn = pool_cpu_rows
+        spec = W.spec
+        elt = 1 if spec.kv_dtype == "e4m3" else 2
+        self.tok_bytes = spec.num_kv_heads * spec.head_size * 2 * elt
+        self.q_bits = W.q.cpu().view(torch.int16).numpy().view(np.uint16)
+        self.lens = W.context_lens.cpu().numpy()
+        self.tables = W.block_tables.cpu().numpy()
+        self.cursor = 0
+        self.rate = None  # attended bytes per oracle second, once measured
+
+    def sample(self, seconds):
+        """Run samples until ``seconds`` of oracle time (at least one).
+        Returns (attended bytes processed, elapsed s, samples)."""
+        from oracle import paged_attention as ref  # test infrastructure: only these legs run it
+        spec = self.W.spec
+        done_bytes, elapsed, n = 0, 0.0, 0
+        while n == 0 or elapsed < seconds:
+            i = self.cursor % spec.num_seqs
+            self.cursor += 1
+            L = int(self.lens[i])
+            budget = max(seconds - elapsed, 0.0)
+            cap = L if self.rate is None else int(self.rate * budget / self.tok_bytes)
+            Lp = min(L, max(16, cap, 0)) if L > 0 else 0
+            nb = -(-Lp // 16)
+            pool = self.rows_fn(self.tables[i, :nb].astype(np.int64))
+            table = np.arange(max(nb, 1))[None, :]
+            t = time.perf_counter()
+            ref.paged_decode(self.q_bits[i:i + 1], spec.q_dtype, pool, table, np.array([Lp]),
+                             self.W.scale, spec.kv_dtype, self.W.kv_scale)
+            dt = time.perf_counter() - t
+            elapsed += dt
+            done_bytes += Lp * self.tok_bytes
+            n += 1
+            if Lp > 0 and dt > 0:
+                r = Lp * self.tok_bytes / dt
+                self.rate = r if self.rate is None else 0.5 * (self.rate + r)
+        return done_bytes, elapsed, n
 
 
 def oracle_rows_fn(W):
@@ -426,10 +446,11 @@ def run_ours(args, world, rank, local):
     # ---- CPU oracle baseline (rank 0, N=1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        b, secs, nseq = oracle_sample(W, args.cpu_seconds, oracle_rows_fn(W))
+        b, secs, nseq = OracleSampler(W, oracle_rows_fn(W)).sample(args.cpu_seconds)
         cpu = {"value": round(b / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"float64 NumPy oracle, {nseq} of {spec.num_seqs} sequences of this "
-                         f"batch (all heads), {secs:.1f} s, 1 BLAS thread"}
+               "sample": f"float64 NumPy oracle, {nseq} sequences of this batch (all heads; a "
+                         f"sequence cut to fewer tokens only if the time budget ends inside it), "
+                         f"{secs:.1f} s, 1 BLAS thread"}
 
     all_kv = sum_over_ranks(kv_bytes, world, device)
     value = all_kv / (ms_step * 1e-3) / 1e9
@@ -483,41 +504,50 @@ def run_ours(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
-def prefill_oracle_sample(W, seconds):
-    """Time the float64 oracle on query rows of a prefill batch (all heads of
-    each row), spread over its sequences, until ``seconds`` of CPU work.
-    Returns (flops, seconds, rows)."""
-    from oracle import paged_attention as ref
-    spec = W.spec
-    dt = spec.dtype
-    lens = W.context_lens.cpu().numpy()
-    qsl = W.query_start_loc.cpu().numpy()
-    tables = W.block_tables.cpu().numpy()
-    q_bits = W.q.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    pool = W.pool.cpu()
-    # the oracle's pool after the step's write
-    pbits = ref.reshape_and_cache(pool.view(torch.int16).numpy().view(np.uint16),
-                                  W.k_new.cpu().view(torch.int16).numpy().view(np.uint16),
-                                  W.v_new.cpu().view(torch.int16).numpy().view(np.uint16),
-                                  W.slot_mapping.cpu().numpy(), dt, dt)
-    rng = np.random.default_rng(0)
-    flops, elapsed, rows = 0, 0.0, 0
-    while elapsed < seconds:
-        i = int(rng.integers(spec.num_seqs))
-        n = int(qsl[i + 1] - qsl[i])
-        if n == 0:
-            continue
-        t_ = int(rng.integers(n))
-        pos = int(lens[i]) - n + t_
-        nb = pos // 16 + 1
-        sub = pbits[tables[i, :nb].astype(np.int64)]
-        t0 = time.perf_counter()
-        ref.paged_prefill(q_bits[qsl[i] + t_:qsl[i] + t_ + 1], dt, sub, np.arange(nb)[None, :],
-                          np.array([pos + 1]), np.array([0, 1]), W.scale, dt)
-        elapsed += time.perf_counter() - t0
-        flops += 4 * spec.head_size * spec.num_q_heads * (pos + 1)
-        rows += 1
-    return flops, elapsed, rows
+class PrefillOracleSampler:
+    """Times the float64 oracle on query rows of a prefill batch (all heads of
+    each row), drawn over its sequences.  The oracle's pool after the step's
+    write is built once."""
+
+    def __init__(self, W):
+        from oracle import paged_attention as ref  # test infrastructure: only these legs run it
+        self.W = W
+        dt = W.spec.dtype
+        self.lens = W.context_lens.cpu().numpy()
+        self.qsl = W.query_start_loc.cpu().numpy()
+        self.tables = W.block_tables.cpu().numpy()
+        self.q_bits = W.q.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+        pool = W.pool.cpu()
+        self.pbits = ref.reshape_and_cache(pool.view(torch.int16).numpy().view(np.uint16),
+                                           W.k_new.cpu().view(torch.int16).numpy().view(np.uint16),
+                                           W.v_new.cpu().view(torch.int16).numpy().view(np.uint16),
+                                           W.slot_mapping.cpu().numpy(), dt, dt)
+        self.rng = np.random.default_rng(0)
+
+    def sample(self, seconds):
+        """Rows until ``seconds`` of oracle time (at least one row).
+        Returns (flops, seconds, rows)."""
+        from oracle import paged_attention as ref
+        spec = self.W.spec
+        dt = spec.dtype
+        flops, elapsed, rows = 0, 0.0, 0
+        while rows == 0 or elapsed < seconds:
+            i = int(self.rng.integers(spec.num_seqs))
+            n = int(self.qsl[i + 1] - self.qsl[i])
+            if n == 0:
+                continue
+            t_ = int(self.rng.integers(n))
+            pos = int(self.lens[i]) - n + t_
+            nb = pos // 16 + 1
+            sub = self.pbits[self.tables[i, :nb].astype(np.int64)]
+            r = int(self.qsl[i]) + t_
+            t0 = time.perf_counter()
+            ref.paged_prefill(self.q_bits[r:r + 1], dt, sub, np.arange(nb)[None, :],
+                              np.array([pos + 1]), np.array([0, 1]), self.W.scale, dt)
+            elapsed += time.perf_counter() - t0
+            flops += 4 * spec.head_size * spec.num_q_heads * (pos + 1)
+            rows += 1
+        return flops, elapsed, rows
 
 
 def run_prefill(args, world, rank, local):
@@ -619,7 +649,7 @@ def run_prefill(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        f, secs, rows = prefill_oracle_sample(W, args.cpu_seconds)
+        f, secs, rows = PrefillOracleSampler(W).sample(args.cpu_seconds)
         cpu = {"value": round(f / secs / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
                "kind": "oracle",
                "sample": f"float64 NumPy oracle, {rows} query rows (all heads) of this batch, "
@@ -869,12 +899,14 @@ def run_reference_prefill(args, world, rank, local):
         return
     spec = wl.PREFILL_SPECS[args.prefill]
     W = wl.make_prefill_workload(spec, 10 + args.prefill, device="cpu")
-    per_step = max(1.0, args.ref_seconds / max(1, args.steps + args.warmup))
+    # the whole run holds about --ref-seconds of oracle time, whatever --steps
+    per_step = args.ref_seconds / max(1, args.steps + args.warmup)
+    sampler = PrefillOracleSampler(W)
     for _ in range(args.warmup):
-        prefill_oracle_sample(W, per_step)
+        sampler.sample(per_step)
     tot_f, tot_s, rows = 0, 0.0, 0
     for _ in range(args.steps):
-        f, sec, r = prefill_oracle_sample(W, per_step)
+        f, sec, r = sampler.sample(per_step)
         tot_f, tot_s, rows = tot_f + f, tot_s + sec, rows + r
     value = tot_f / tot_s / 1e12
     cpu = {"value": round(value, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
@@ -898,19 +930,21 @@ def run_reference(args, world, rank, local):
         return
     spec = wl.SPECS[args.config]
     W = wl.make_workload(spec, args.config, device="cpu")
-    rows = oracle_rows_fn(W)
-    per_step = max(1.0, args.ref_seconds / max(1, args.steps + args.warmup))
+    # the whole run holds about --ref-seconds of oracle time, whatever --steps
+    per_step = args.ref_seconds / max(1, args.steps + args.warmup)
+    sampler = OracleSampler(W, oracle_rows_fn(W))
     for _ in range(args.warmup):
-        oracle_sample(W, per_step, rows)
+        sampler.sample(per_step)
     tot_b, tot_s, nseq = 0, 0.0, 0
     for _ in range(args.steps):
-        b, s, k = oracle_sample(W, per_step, rows)
+        b, s, k = sampler.sample(per_step)
         tot_b += b
         tot_s += s
         nseq += k
     value = tot_b / tot_s / 1e9
     cpu = {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-           "sample": f"float64 NumPy oracle, {nseq} sequences over {args.steps} steps "
+           "sample": f"float64 NumPy oracle, {nseq} sequence samples (all heads, contexts cut to "
+                     f"the per-step time budget) over {args.steps} steps "
                      f"({tot_s:.1f} s), 1 BLAS thread"}
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
