@@ -106,7 +106,8 @@ def tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback bf16"
 
 
-PREFILL_SOURCES = ["pa_prefill_tc.cuh", "pa_prefill_params.cuh", "pa_prefill.cu", "pa_ptx.cuh",
+PREFILL_SOURCES = ["pa_prefill_tc.cuh", "pa_prefill_params.cuh", "pa_prefill_launch.cuh", "pa_prefill.cu",
+                   "pa_prefill_fp8.cu", "pa_ptx.cuh",
                    "pa_cache.cu", "pa_api.cu"]
 
 
@@ -134,10 +135,12 @@ def profiled_traffic(config_id, step_path):
     return float(m_tr.group(1))
 
 
-def profiled_prefill_traffic(n):
+def profiled_prefill_traffic(n, fp8=False):
     """DRAM bytes per pa_prefill call from the committed ncu summary of prefill
-    workload ``n``, if it still describes the current kernel source (else None)."""
-    path = os.path.join(PROFILE_DIR, f"paged_prefill_tc_kernel_prefill{n}.md")
+    workload ``n`` (over an E4M3 cache if ``fp8``), if it still describes the
+    current kernel source (else None)."""
+    path = os.path.join(PROFILE_DIR,
+                        f"paged_prefill_tc_kernel_prefill{n}{'_e4m3' if fp8 else ''}.md")
     try:
         text = open(path, encoding="utf-8").read()
     except OSError:
@@ -562,7 +565,8 @@ def run_prefill(args, world, rank, local):
     pa.load()
     spec = wl.PREFILL_SPECS[args.prefill]
     W = wl.make_prefill_workload(spec, 10 + args.prefill + 1000 * rank, device=str(device))
-    S = PrefillStep(W, device=device)
+    fp8 = args.prefill_kv == "e4m3"
+    S = PrefillStep(W, device=device, kv_dtype=args.prefill_kv)
     flops = prefill_flops(W)
     stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):
@@ -622,7 +626,7 @@ def run_prefill(args, world, rank, local):
     ev[0].record(stream)
     for _ in range(min(n, 50)):
         pa.pa_prefill(S.out, S.q, S.k_cache, S.v_cache, S.block_tables, S.context_lens,
-                      S.query_start_loc, S.max_query_len, S.scale)
+                      S.query_start_loc, S.max_query_len, S.scale, kv_scale=S.kv_scale)
     ev[1].record(stream)
     torch.cuda.synchronize(device)
     attn_ms = ev[0].elapsed_time(ev[1]) / min(n, 50)
@@ -653,7 +657,8 @@ def run_prefill(args, world, rank, local):
         cpu = {"value": round(f / secs / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
                "kind": "oracle",
                "sample": f"float64 NumPy oracle, {rows} query rows (all heads) of this batch, "
-                         f"{secs:.1f} s, 1 BLAS thread"}
+                         f"{secs:.1f} s, 1 BLAS thread"
+                         + (" (on the 16-bit cache values: the same attention work)" if fp8 else "")}
     peak, peak_kind = tensor_peak()
     value = sum_over_ranks(flops, world, device) / (ms_step * 1e-3) / 1e12
     achieved = flops / (attn_ms * 1e-3) / 1e12
@@ -668,6 +673,7 @@ def run_prefill(args, world, rank, local):
                    "head_size": spec.head_size, "block_size": 16,
                    "query_tokens": int(W.q.shape[0]), "max_query_len": S.max_query_len,
                    "mean_context": float(W.context_lens.float().mean()),
+                   "kv_dtype": "e4m3" if fp8 else spec.dtype,
                    "step": "pa_reshape_and_cache of the query tokens + pa_prefill",
                    "launch": launch, "l2": "K/V re-read by a sequence's tiles comes from L2",
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
@@ -675,7 +681,7 @@ def run_prefill(args, world, rank, local):
                      "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "algorithmic_flops_per_launch": flops,
-                     "traffic": profiled_prefill_traffic(args.prefill)},
+                     "traffic": profiled_prefill_traffic(args.prefill, fp8)},
         "gpu_launches": S.launches_per_step * n,
         "e2e": e2e, "cpu_baseline": cpu,
         "clocks": sampler.summary(t0, t1),
@@ -978,6 +984,8 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--prefill", type=int, default=0, choices=[0] + sorted(wl.PREFILL_SPECS),
                    help="time a prefill workload (pa_prefill) instead of the decode step")
+    p.add_argument("--prefill-kv", default="same", choices=["same", "e4m3"],
+                   help="with --prefill: a cache of q's dtype, or E4M3 codes of the same values")
     p.add_argument("--prefix-cache", action="store_true",
                    help="time prefix-cached against full prefill (system-prompt scenario)")
     p.add_argument("--blocks", action="store_true",

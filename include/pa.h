@@ -225,13 +225,18 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const
  * block table as in pa_decode.  A chunk of one token per sequence is a decode
  * step.
  *
- * out, q           [T, num_q_heads, head_size] of dtype, T = query_start_loc[num_seqs];
+ * out, q           [T, num_q_heads, head_size] of q_dtype, T = query_start_loc[num_seqs];
  *                  16-byte aligned, contiguous.
  * query_start_loc  int32 [num_seqs + 1], non-decreasing, query_start_loc[0] = 0.
  * max_query_len    >= every n (sizes the grid; the kernel checks it).
  * block_tables, context_lens, num_blocks  as for pa_decode (n <= L <= max_blocks_per_seq * 16).
- * dtype            PA_F16 or PA_BF16, shared by q, the cache and out (an E4M3
- *                  cache returns PA_ERR_UNSUPPORTED).
+ * q_dtype          PA_F16 or PA_BF16 (q and out).
+ * kv_dtype         q_dtype, or PA_E4M3: the cache holds codes whose values are
+ *                  code * kv_scale (kv_scale finite and > 0, else PA_ERR_INVALID_ARG;
+ *                  ignored for a 16-bit cache).  Over an E4M3 cache the MMAs run in
+ *                  f16: the codes are exact in f16, bf16 queries are rounded to f16
+ *                  (exact for magnitudes in [2^-14, 65504], saturated above), and
+ *                  kv_scale multiplies the logits and the output once each.
  * Rows of sequences whose n exceeds L or max_query_len are not written and the
  * device status bit 2 is raised (pa_device_status).  Asynchronous on `stream`;
  * no workspace.
@@ -240,7 +245,8 @@ pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* 
                      const int32_t* block_tables, const int32_t* context_lens,
                      const int32_t* query_start_loc, int num_seqs, int max_query_len,
                      int max_blocks_per_seq, int num_blocks, int num_q_heads, int num_kv_heads,
-                     int head_size, int block_size, float scale, pa_dtype dtype, void* stream);
+                     int head_size, int block_size, float scale, pa_dtype q_dtype,
+                     pa_dtype kv_dtype, float kv_scale, void* stream);
 
 /*
  * pa_decode_workspace_size -- bytes of workspace pa_decode needs for these

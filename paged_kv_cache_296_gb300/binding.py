@@ -33,7 +33,8 @@ SIGNATURES = {
                               _F, _I, _I, _F, _I, _P, _SZ, _P]),
     "pa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                                _F, _I, _P]),
-    "pa_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "pa_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
+                        _F, _P]),
     "pa_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "pa_decode_partition_size": (_I, [_I, _I, _I, _I, _I]),
     "pa_gather_kv": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
@@ -193,11 +194,12 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, kv_sc
 
 
 def pa_prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
-               max_query_len, scale):
+               max_query_len, scale, kv_scale=1.0):
     """Causal paged prefill into ``out`` ``[T, Hq, D]`` (rows of ``q``).
 
     ``query_start_loc``: int32 ``[B + 1]``; sequence i's queries are rows
-    ``query_start_loc[i] .. query_start_loc[i+1]-1``, its last tokens.
+    ``query_start_loc[i] .. query_start_loc[i+1]-1``, its last tokens.  The
+    cache is of q's dtype, or uint8 E4M3 codes with values ``code * kv_scale``.
     """
     nb, bs, hkv, d = _cache_geometry(k_cache, v_cache)
     T, hq, dq = q.shape
@@ -209,12 +211,12 @@ def pa_prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start
             raise ValueError("block_tables, context_lens and query_start_loc must be contiguous int32")
     if block_tables.dim() != 2 or block_tables.shape[0] != B or query_start_loc.shape != (B + 1,):
         raise ValueError("block_tables must be [B, max_blocks], query_start_loc [B + 1]")
-    if k_cache.dtype != q.dtype:
-        raise ValueError("pa_prefill reads a cache of q's dtype")
+    if k_cache.dtype != q.dtype and k_cache.dtype != torch.uint8:
+        raise ValueError("pa_prefill reads a cache of q's dtype or of E4M3 codes (uint8)")
     st = load().pa_prefill(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         _ptr(query_start_loc), B, int(max_query_len), block_tables.shape[1], nb, hq, hkv, d, bs,
-        float(scale), dtype_code(q.dtype), _stream(q))
+        float(scale), dtype_code(q.dtype), dtype_code(k_cache.dtype), float(kv_scale), _stream(q))
     _check("pa_prefill", st)
 
 

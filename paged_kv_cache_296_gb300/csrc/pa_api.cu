@@ -301,7 +301,8 @@ pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* 
                      const int32_t* block_tables, const int32_t* context_lens,
                      const int32_t* query_start_loc, int num_seqs, int max_query_len,
                      int max_blocks_per_seq, int num_blocks, int num_q_heads, int num_kv_heads,
-                     int head_size, int block_size, float scale, pa_dtype dtype, void* stream) {
+                     int head_size, int block_size, float scale, pa_dtype q_dtype,
+                     pa_dtype kv_dtype, float kv_scale, void* stream) {
   pa_status st;
   if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs must be >= 0 (got %d)", num_seqs);
   if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "num_seqs %d exceeds 65535", num_seqs);
@@ -318,10 +319,12 @@ pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* 
     return fail(PA_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)",
                 num_q_heads, num_kv_heads);
   if (num_kv_heads > 65535) return fail(PA_ERR_UNSUPPORTED, "num_kv_heads exceeds 65535");
-  if (dtype == PA_E4M3)
-    return fail(PA_ERR_UNSUPPORTED, "pa_prefill reads 16-bit caches only (E4M3: not yet)");
-  if (dtype != PA_F16 && dtype != PA_BF16)
-    return fail(PA_ERR_UNSUPPORTED, "dtype must be PA_F16 or PA_BF16");
+  if (q_dtype != PA_F16 && q_dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "q_dtype must be PA_F16 or PA_BF16");
+  if (kv_dtype != q_dtype && kv_dtype != PA_E4M3)
+    return fail(PA_ERR_UNSUPPORTED, "kv_dtype must be q_dtype or PA_E4M3");
+  if (kv_dtype == PA_E4M3 && (!(kv_scale > 0.f) || kv_scale == INFINITY))
+    return fail(PA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an E4M3 cache");
   if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
     return fail(PA_ERR_INVALID_ARG, "scale must be finite");
   if (num_seqs == 0 || max_query_len == 0) return ok();
@@ -351,7 +354,9 @@ pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* 
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = num_kv_heads;
   a.head_size = head_size;
-  a.dtype = dtype == PA_BF16 ? 1 : 0;
+  a.dtype = q_dtype == PA_BF16 ? 1 : 0;
+  a.kv_dtype = kv_dtype == PA_E4M3 ? 2 : a.dtype;
+  a.kv_scale = kv_dtype == PA_E4M3 ? kv_scale : 1.0f;
   a.scale = scale;
   cudaError_t e = pa::device_status_ptr(&a.status);
   if (e != cudaSuccess) return cuda_fail(e, "status word");

@@ -63,12 +63,15 @@ struct PrefillArgs {
   int num_q_heads;
   int num_kv_heads;
   int head_size;
-  int dtype;  // 0 f16, 1 bf16 (q, cache and out)
+  int dtype;     // 0 f16, 1 bf16 (q and out)
+  int kv_dtype;  // the cache: 0 f16, 1 bf16 (q's type), 2 E4M3 codes
+  float kv_scale;
   float scale;
   unsigned* status;
 };
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, const char** why);
+cudaError_t launch_prefill_fp8(const PrefillArgs& a, cudaStream_t stream, const char** why);
 
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
                                      const int64_t* slot_mapping, int64_t n_tokens,

@@ -36,7 +36,8 @@ struct PrefillParams {
   int group;                      // G = Hq / Hkv
   int tiles;                      // CTAs per (sequence, KV head): tiles of the longest query run
   int band;                       // tile indices per grid band (1: heaviest tiles first)
-  float scale_log2;               // scale * log2(e)
+  float scale_log2;               // scale * log2(e) (times kv_scale for an E4M3 cache)
+  float out_scale;                // kv_scale for an E4M3 cache (V holds its codes), else 1
 };
 
 // Two fp32 values rounded to a packed pair of the MMA type (QT: 0 = fp16, 1 = bf16).

@@ -38,30 +38,41 @@
 
 namespace pa {
 
-template <int D>
+// KV8: the cache holds E4M3 codes.  The TMA then loads fp8 rows into rings of
+// their own and two converter warps widen each chunk into 16-bit staging planes
+// laid out like the 16-bit rings (one chunk of K, one of V), which the MMAs
+// read; the MMAs run in f16 (every E4M3 value is exact in f16).
+template <int D, bool KV8>
 struct PrefillTcCfg {
   static constexpr int kRows = 128;                        // rows of one tile (TMEM lanes)
   static constexpr int kTiles = 2;                         // tiles per CTA, one softmax group each
-  static constexpr int kPieces = D * 2 / 128;              // 128-byte pieces of a row
+  static constexpr int kPieces = D * 2 / 128;              // 128-byte pieces of a 16-bit row
   static constexpr int kQTileBytes = kRows * D * 2;        // [pieces][128 rows][128 B]
   static constexpr int kQBytes = kTiles * kQTileBytes;
   static constexpr int kBlocksPerChunk = 8;                // 128 keys per S = Q K^T
   static constexpr int kBlockBytes = 16 * 128;             // one block, one piece: [16][128 B]
   static constexpr int kChunkBytes = kBlocksPerChunk * kBlockBytes;  // one chunk, one piece
-  static constexpr int kRingBytes = 128 * 1024;            // K and V planes
-  static constexpr int kRing = kRingBytes / (2 * kPieces * kChunkBytes);  // chunks per ring
-  static constexpr int kPlaneBytes = kRing * kChunkBytes;  // one piece plane of K (or V)
-  static constexpr int kKOff = kQBytes;                    // K: [pieces][ring rows][128 B]
-  static constexpr int kVOff = kKOff + kPieces * kPlaneBytes;
-  static constexpr int kBarOff = kVOff + kPieces * kPlaneBytes;
+  static constexpr int kChunkBytes8 = kBlocksPerChunk * 16 * D;      // one chunk of fp8 rows
+  static constexpr int kRingBytes = KV8 ? 64 * 1024 : 128 * 1024;    // K and V rings
+  static constexpr int kRing =                                        // chunks per ring
+      KV8 ? kRingBytes / (2 * kChunkBytes8) : kRingBytes / (2 * kPieces * kChunkBytes);
+  // one piece plane of K (or V): the whole ring, or (KV8) the one staged chunk
+  static constexpr int kPlaneBytes = KV8 ? kChunkBytes : kRing * kChunkBytes;
+  static constexpr int kRingPart = KV8 ? kRing * kChunkBytes8 : kPieces * kPlaneBytes;
+  static constexpr int kKOff = kQBytes;                    // K ring
+  static constexpr int kVOff = kKOff + kRingPart;          // V ring
+  static constexpr int kKStOff = kVOff + kRingPart;        // KV8: 16-bit K of one chunk
+  static constexpr int kVStOff = kKStOff + (KV8 ? kPieces * kPlaneBytes : 0);
+  static constexpr int kBarOff = kVStOff + (KV8 ? kPieces * kPlaneBytes : 0);
   // barriers: K full / empty, V full / empty per ring slot; s_full, p_full per
-  // tile; q_ready, tail, o_done
-  static constexpr int kNumBars = 4 * kRing + 2 * kTiles + 3;
+  // tile; q_ready, tail, o_done; KV8: staged K full / empty, staged V full / empty
+  static constexpr int kNumBars = 4 * kRing + 2 * kTiles + 3 + (KV8 ? 4 : 0);
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr int kSoftmaxThreads = 128 * kTiles;
   static constexpr int kProducerWarp = kSoftmaxThreads / 32;
   static constexpr int kMmaWarp = kProducerWarp + 1;
-  static constexpr int kThreads = kSoftmaxThreads + 64;
+  static constexpr int kConvWarp = kMmaWarp + 1;           // KV8: K converter, then V converter
+  static constexpr int kThreads = kSoftmaxThreads + 64 + (KV8 ? 64 : 0);
   // TMEM columns of tile t (base 256 t): O [0, D); S(c) in fp32 at [128, 256),
   // then P(c) (16-bit pairs) over it once the softmax has read it: keys 0..63
   // at [128, 160), keys 64..127 at [192, 224)
@@ -220,11 +231,21 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 
-template <int D, int QT>
-__global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
+// Two floats to two f16 (lo -> low half), round to nearest, saturating to the
+// largest finite f16.
+__device__ __forceinline__ uint32_t pack_f16x2_satfinite(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// QT: 0 = fp16, 1 = bf16 (q and out); KV8: the cache holds E4M3 codes (else q's type).
+template <int D, int QT, bool KV8>
+__global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
-  using C = PrefillTcCfg<D>;
+  using C = PrefillTcCfg<D, KV8>;
+  constexpr int MT = KV8 ? 0 : QT;  // the MMAs' 16-bit type (P, and Q as staged)
   constexpr unsigned kAll = 0xffffffffu;
   constexpr int kT = C::kTiles;
   constexpr int kR = C::kRing;
@@ -243,6 +264,10 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
   uint64_t* q_ready = p_full + kT;
   uint64_t* tail_bar = q_ready + 1;
   uint64_t* o_done = q_ready + 2;
+  uint64_t* kst_full = o_done + 1;  // KV8: the staged 16-bit K / V chunk
+  uint64_t* kst_empty = o_done + 2;
+  uint64_t* vst_full = o_done + 3;
+  uint64_t* vst_empty = o_done + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -298,10 +323,22 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
   // The last block holds keys past the context's end when it is the block of
   // position L - 1 and L is not a multiple of 16.
   const bool has_tail = (nkb - 1 == (L - 1) / 16) && (L % 16 != 0);
-  const bool bf16 = QT == 1;
+  const bool bf16 = MT == 1;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 4 * kR; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < kR; ++i) {
+      // KV8: a ring slot is released by the converter warp's 32 lanes
+      mbar_init(&full_k[i], 1);
+      mbar_init(&empty_k[i], KV8 ? 32 : 1);
+      mbar_init(&full_v[i], 1);
+      mbar_init(&empty_v[i], KV8 ? 32 : 1);
+    }
+    if constexpr (KV8) {
+      mbar_init(kst_full, 32);
+      mbar_init(kst_empty, 1);
+      mbar_init(vst_full, 32);
+      mbar_init(vst_empty, 1);
+    }
     for (int t = 0; t < kT; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 128);
@@ -329,7 +366,8 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
     // Chunk c goes to ring slot c % kR: block j of it lands at rows
-    // 16 j .. 16 j + 15 of the slot in each piece's plane, K then V.
+    // 16 j .. 16 j + 15 of the slot in each piece's plane, K then V (KV8: at
+    // rows 16 j .. of the slot's [128 rows][D bytes] tile, one load per block).
     const int32_t* tbl = p.block_tables + (size_t)seq * p.max_blocks_per_seq;
     const int oob_row = p.num_blocks * 16;
     const uint64_t pol = l2_evict_normal_policy();
@@ -342,8 +380,10 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
       const int brow = (blk >= 0 && blk < p.num_blocks) ? blk * 16 : oob_row;
       const int slot = c % kR;
       const uint32_t ph = ((uint32_t)(c / kR) & 1u) ^ 1u;
-      const uint32_t bytes = (uint32_t)(nblk * C::kPieces * C::kBlockBytes);
-      const uint32_t off = slot * C::kChunkBytes + lane * C::kBlockBytes;
+      const uint32_t bytes =
+          (uint32_t)(KV8 ? nblk * 16 * D : nblk * C::kPieces * C::kBlockBytes);
+      const uint32_t off = KV8 ? slot * C::kChunkBytes8 + lane * 16 * D
+                               : slot * C::kChunkBytes + lane * C::kBlockBytes;
       int ok = 0;
       if (lane == 0 && !aborted() && mbar_wait_bounded(&empty_k[slot], ph, p.status)) {
         mbar_arrive_expect_tx(&full_k[slot], bytes);
@@ -351,10 +391,14 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
       }
       if (!__shfl_sync(kAll, ok, 0)) break;
       if (lane < nblk) {
+        if constexpr (KV8) {
+          tma_load_3d(smem + C::kKOff + off, &tmap_k, &full_k[slot], 0, kvh, brow, pol);
+        } else {
 #pragma unroll
-        for (int pc = 0; pc < C::kPieces; ++pc)
-          tma_load_4d(smem + C::kKOff + pc * C::kPlaneBytes + off, &tmap_k, &full_k[slot], 0, brow,
-                      pc, kvh, pol);
+          for (int pc = 0; pc < C::kPieces; ++pc)
+            tma_load_4d(smem + C::kKOff + pc * C::kPlaneBytes + off, &tmap_k, &full_k[slot], 0,
+                        brow, pc, kvh, pol);
+        }
       }
       ok = 0;
       if (lane == 0 && !aborted() && mbar_wait_bounded(&empty_v[slot], ph, p.status)) {
@@ -363,16 +407,21 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
       }
       if (!__shfl_sync(kAll, ok, 0)) break;
       if (lane < nblk) {
+        if constexpr (KV8) {
+          tma_load_3d(smem + C::kVOff + off, &tmap_v, &full_v[slot], 0, kvh, brow, pol);
+        } else {
 #pragma unroll
-        for (int pc = 0; pc < C::kPieces; ++pc)
-          tma_load_4d(smem + C::kVOff + pc * C::kPlaneBytes + off, &tmap_v, &full_v[slot], 0, brow,
-                      pc, kvh, pol);
+          for (int pc = 0; pc < C::kPieces; ++pc)
+            tma_load_4d(smem + C::kVOff + pc * C::kPlaneBytes + off, &tmap_v, &full_v[slot], 0,
+                        brow, pc, kvh, pol);
+        }
       }
       ++issued;
     }
     if (issued < nchunks && lane == 0) fail();
-    if (lane == 0 && has_tail && !aborted() && issued == nchunks) {
+    if (!KV8 && lane == 0 && has_tail && !aborted() && issued == nchunks) {
       // zero the V rows of keys L .. 16 * nkb - 1 once the last chunk's V has landed
+      // (KV8: the V converter writes zeros for them)
       const int c = nchunks - 1;
       const int slot = c % kR;
       const int j = nkb - 1 - kBpc * c;
@@ -399,12 +448,18 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
       const uint32_t id_pv = umma_idesc(bf16, 128, D, 1);
       // descriptors are formed once; an operand's step is a constant added to the low word
       const uint32_t q_lo = umma_desc_lo(sbase, 16);
-      const uint32_t k_lo = umma_desc_lo(sbase + C::kKOff, 16);
-      const uint32_t v_lo = umma_desc_lo(sbase + C::kVOff, C::kPlaneBytes);
+      const uint32_t k_lo = umma_desc_lo(sbase + (KV8 ? C::kKStOff : C::kKOff), 16);
+      const uint32_t v_lo = umma_desc_lo(sbase + (KV8 ? C::kVStOff : C::kVOff), C::kPlaneBytes);
+      // KV8: one staged chunk of each (released once its MMAs are done), else ring slots
+      auto slot_lo = [&](int c) { return KV8 ? 0u : (uint32_t)((c % kR) * C::kChunkBytes >> 4); };
+      auto wait_k = [&](int c) {
+        return KV8 ? mbar_wait_bounded(kst_full, (uint32_t)c & 1u, p.status)
+                   : mbar_wait_bounded(&full_k[c % kR], (uint32_t)(c / kR) & 1u, p.status);
+      };
       auto issue_s = [&](int t, int c) {  // S_t(c) = Q_t K(c)^T
         const uint32_t dcol = tmem + t * C::kTileCols + C::kS0;
         const uint32_t qa = q_lo + (uint32_t)(t * C::kQTileBytes >> 4);
-        const uint32_t ka = k_lo + (uint32_t)((c % kR) * C::kChunkBytes >> 4);
+        const uint32_t ka = k_lo + slot_lo(c);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           constexpr int kQStep = C::kRows * 128;
@@ -414,26 +469,29 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         }
         umma_commit(&s_full[t]);
       };
-      bool ok = mbar_wait_bounded(q_ready, 0, p.status) &&
-                mbar_wait_bounded(&full_k[0], 0, p.status);
+      bool ok = mbar_wait_bounded(q_ready, 0, p.status) && wait_k(0);
       tc_fence_after();
       if (ok) {
         for (int t = 0; t < kT; ++t) issue_s(t, 0);
-        umma_commit(&empty_k[0]);
+        umma_commit(KV8 ? kst_empty : &empty_k[0]);
       }
       for (int c = 0; c < nchunks && ok; ++c) {
         const int slot = c % kR;
         const int nblk = min(kBpc, nkb - kBpc * c);
         const bool more = c + 1 < nchunks;
-        ok = mbar_wait_bounded(&full_v[slot], (uint32_t)(c / kR) & 1u, p.status);
-        if (ok && has_tail && !more) ok = mbar_wait_bounded(tail_bar, 0, p.status);
+        if constexpr (KV8) {
+          ok = mbar_wait_bounded(vst_full, (uint32_t)c & 1u, p.status);
+        } else {
+          ok = mbar_wait_bounded(&full_v[slot], (uint32_t)(c / kR) & 1u, p.status);
+          if (ok && has_tail && !more) ok = mbar_wait_bounded(tail_bar, 0, p.status);
+        }
         for (int t = 0; t < kT && ok; ++t) {
           // O_t += P_t(c) V(c), then S_t(c + 1) into the same columns
           ok = mbar_wait_bounded(&p_full[t], (uint32_t)c & 1u, p.status);
           if (!ok) break;
           tc_fence_after();
           const uint32_t pcol = tmem + t * C::kTileCols + C::kS0;
-          const uint32_t va = v_lo + (uint32_t)(slot * C::kChunkBytes >> 4);
+          const uint32_t va = v_lo + slot_lo(c);
           auto pv = [&](int j) {
             umma_ts(tmem + t * C::kTileCols, pcol + 64 * (j / 4) + 8 * (j % 4),
                     umma_desc_join(va + (uint32_t)(j * (C::kBlockBytes >> 4))), id_pv,
@@ -445,16 +503,15 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
           } else {
             for (int j = 0; j < nblk; ++j) pv(j);
           }
-          if (t == kT - 1) umma_commit(&empty_v[slot]);
+          if (t == kT - 1) umma_commit(KV8 ? vst_empty : &empty_v[slot]);
           if (more) {
             if (t == 0) {
-              ok = mbar_wait_bounded(&full_k[(c + 1) % kR], (uint32_t)((c + 1) / kR) & 1u,
-                                     p.status);
+              ok = wait_k(c + 1);
               if (!ok) break;
               tc_fence_after();
             }
             issue_s(t, c + 1);
-            if (t == kT - 1) umma_commit(&empty_k[(c + 1) % kR]);
+            if (t == kT - 1) umma_commit(KV8 ? kst_empty : &empty_k[(c + 1) % kR]);
           }
         }
       }
@@ -462,6 +519,53 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
       if (!ok) fail();
     }
     __syncwarp();
+  } else if (KV8 && warp >= C::kConvWarp) {
+    // ------------------------------------------------------------ converters (KV8)
+    // Warp kConvWarp widens K, the next warp V: each 16-byte run of a landed
+    // fp8 row (16 codes) becomes 32 bytes of f16 in the staging planes, at the
+    // positions the TMA would have put a 16-bit row.  V rows of keys at or past
+    // L become zeros (a P of 0 times a stale code must not reach the sum).
+    const bool isv = warp != C::kConvWarp;
+    uint64_t* full = isv ? full_v : full_k;
+    uint64_t* empty = isv ? empty_v : empty_k;
+    uint64_t* st_full = isv ? vst_full : kst_full;
+    uint64_t* st_empty = isv ? vst_empty : kst_empty;
+    const uint8_t* ring = smem + (isv ? C::kVOff : C::kKOff);
+    uint8_t* st = smem + (isv ? C::kVStOff : C::kKStOff);
+    constexpr int kRuns = D / 16;  // 16-byte runs of an fp8 row
+    for (int c = 0; c < nchunks; ++c) {
+      const int slot = c % kR;
+      const bool w = mbar_wait_bounded(&full[slot], (uint32_t)(c / kR) & 1u, p.status) &&
+                     mbar_wait_bounded(st_empty, ((uint32_t)c & 1u) ^ 1u, p.status);
+      if (!__all_sync(kAll, w)) {
+        if (lane == 0) fail();
+        break;
+      }
+      const int nrows = 16 * min(kBpc, nkb - kBpc * c);
+      for (int u = lane; u < nrows * kRuns; u += 32) {
+        const int r = u / kRuns, j = u % kRuns;
+        // the TMA's swizzle of the [16 rows][D bytes] tile of block r / 16
+        const uint32_t o = (uint32_t)((r & 15) * D + j * 16);
+        const uint32_t sw = D == 128 ? (o ^ (((o >> 7) & 7u) << 4)) : (o ^ (((o >> 7) & 3u) << 4));
+        const uint4 x = *reinterpret_cast<const uint4*>(ring + slot * C::kChunkBytes8 +
+                                                        (r >> 4) * (16 * D) + sw);
+        uint4 y0 = make_uint4(0u, 0u, 0u, 0u), y1 = y0;
+        if (!isv || kBpc * 16 * c + r < L) {
+          y0 = make_uint4(e4m3x2_to_f16x2((uint16_t)(x.x & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(x.x >> 16)),
+                          e4m3x2_to_f16x2((uint16_t)(x.y & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(x.y >> 16)));
+          y1 = make_uint4(e4m3x2_to_f16x2((uint16_t)(x.z & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(x.z >> 16)),
+                          e4m3x2_to_f16x2((uint16_t)(x.w & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(x.w >> 16)));
+        }
+        // elements 16 j .. 16 j + 15: piece j / 4, 16-byte chunks 2 (j % 4) and + 1
+        const int cc = 2 * (j % 4);
+        uint8_t* row = st + (j / 4) * C::kPlaneBytes + r * 128;
+        *reinterpret_cast<uint4*>(row + ((cc ^ (r & 7)) << 4)) = y0;
+        *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (r & 7)) << 4)) = y1;
+      }
+      fence_proxy_async_shared();  // the MMAs read the staging through the async proxy
+      mbar_arrive(st_full);
+      mbar_arrive(&empty[slot]);
+    }
   } else {
     // ------------------------------------------------------------ softmax groups
     // Group t (warps 4t .. 4t+3) owns tile t; thread r of the group owns row r
@@ -487,7 +591,14 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
       const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) + qoff);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
-        const uint4 v = live ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+        uint4 v = live ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (KV8 && QT == 1) {
+          // bf16 q to the MMAs' f16 (exact for magnitudes in f16's range, saturated above)
+          auto cv = [](uint32_t x) {
+            return pack_f16x2_satfinite(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+          };
+          v = make_uint4(cv(v.x), cv(v.y), cv(v.z), cv(v.w));
+        }
         const int piece = c / 8, cc = c % 8;
         *reinterpret_cast<uint4*>(smem + t * C::kQTileBytes + piece * (C::kRows * 128) + r * 128 +
                                   ((cc ^ (r & 7)) * 16)) = v;
@@ -573,8 +684,8 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
           const float2 y = f2_unpack(f2_fma(f2_pack(sh[2 * i + 2], sh[2 * i + 3]), sc2, nm2));
           const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
           const float p2 = ex2_approx(y.x), p3 = ex2_approx(y.y);
-          pk[i] = pf_pack<QT>(p0, p1);
-          pk[i + 1] = pf_pack<QT>(p2, p3);
+          pk[i] = pf_pack<MT>(p0, p1);
+          pk[i + 1] = pf_pack<MT>(p2, p3);
           acc0 = f2_add(acc0, f2_pack(p0, p1));
           acc1 = f2_add(acc1, f2_pack(p2, p3));
         }
@@ -606,8 +717,12 @@ __global__ void __launch_bounds__(PrefillTcCfg<D>::kThreads, 1)
         uint32_t w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float a = has ? __fdiv_rn(o[2 * i], l) : 0.f;
-          const float bv = has ? __fdiv_rn(o[2 * i + 1], l) : 0.f;
+          float a = has ? __fdiv_rn(o[2 * i], l) : 0.f;
+          float bv = has ? __fdiv_rn(o[2 * i + 1], l) : 0.f;
+          if constexpr (KV8) {  // V held codes: the dequantised mean is kv_scale times it
+            a = __fmul_rn(a, p.out_scale);
+            bv = __fmul_rn(bv, p.out_scale);
+          }
           w[i] = pf_pack<QT>(a, bv);
         }
         if (live) {

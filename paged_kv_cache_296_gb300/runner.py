@@ -162,13 +162,33 @@ class PrefillStep:
     STEP_INPUTS = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens",
                    "query_start_loc")
 
-    def __init__(self, W, device="cuda"):
+    def __init__(self, W, device="cuda", kv_dtype=None):
+        """``kv_dtype="e4m3"``: an E4M3 cache holding the workload's pool values
+        (written through pa_reshape_and_cache with kv_scale = amax / 448 over
+        them and the step's new K/V); else the workload's 16-bit pool."""
         self.W = W
         self.device = torch.device(device)
-        self.pool = W.pool.to(self.device, copy=True)
-        self.k_cache, self.v_cache = pa.kv_views(self.pool)
         for name in self.STEP_INPUTS:
             setattr(self, name, getattr(W, name).to(self.device))
+        self.kv_scale = 1.0
+        if kv_dtype == "e4m3":
+            src = W.pool.to(self.device).float()
+            amax = float(torch.nan_to_num(src, nan=0.0).abs().max())
+            if self.k_new.numel():
+                amax = max(amax, float(self.k_new.float().abs().max()),
+                           float(self.v_new.float().abs().max()))
+            self.kv_scale = amax / 448.0
+            nb, bs, _, hkv, d = src.shape
+            self.pool = torch.zeros((nb, bs, 2, hkv, d), dtype=torch.uint8, device=self.device)
+            self.k_cache, self.v_cache = pa.kv_views(self.pool)
+            flat = src.reshape(nb * bs, 2, hkv, d)
+            slots = torch.arange(nb * bs, dtype=torch.int64, device=self.device)
+            pa.pa_reshape_and_cache(flat[:, 0].contiguous(), flat[:, 1].contiguous(),
+                                    self.k_cache, self.v_cache, slots, kv_scale=self.kv_scale)
+            del src, flat
+        else:
+            self.pool = W.pool.to(self.device, copy=True)
+            self.k_cache, self.v_cache = pa.kv_views(self.pool)
         self.out = torch.empty_like(self.q)
         self.max_query_len = W.max_query_len
         self.scale = W.scale
@@ -178,9 +198,10 @@ class PrefillStep:
     def step(self):
         if self.q.shape[0]:
             pa.pa_reshape_and_cache(self.k_new, self.v_new, self.k_cache, self.v_cache,
-                                    self.slot_mapping)
+                                    self.slot_mapping, kv_scale=self.kv_scale)
         pa.pa_prefill(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
-                      self.context_lens, self.query_start_loc, self.max_query_len, self.scale)
+                      self.context_lens, self.query_start_loc, self.max_query_len, self.scale,
+                      kv_scale=self.kv_scale)
         return self.out
 
     launches_per_step = 2

@@ -189,10 +189,11 @@ def test_decode_append_requires_token_buffers(lib):
 
 def prefill_args(**over):
     a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, qsl=FAKE, B=4, mq=64, mb=8, nb=64,
-             hq=8, hkv=2, d=128, bs=16, scale=0.1, dt=pa.PA_F16, stream=NULL)
+             hq=8, hkv=2, d=128, bs=16, scale=0.1, dt=pa.PA_F16, kvdt=pa.PA_F16, kvs=1.0,
+             stream=NULL)
     a.update(over)
     return [a[k] for k in ("out", "q", "k", "v", "bt", "cl", "qsl", "B", "mq", "mb", "nb", "hq",
-                           "hkv", "d", "bs", "scale", "dt", "stream")]
+                           "hkv", "d", "bs", "scale", "dt", "kvdt", "kvs", "stream")]
 
 
 @pytest.mark.parametrize("over,status", [
@@ -203,8 +204,12 @@ def prefill_args(**over):
     (dict(d=96), 2),
     (dict(bs=32), 2),
     (dict(hq=6, hkv=4), 1),
-    (dict(dt=pa.PA_E4M3), 2),            # 16-bit caches only
+    (dict(dt=pa.PA_E4M3, kvdt=pa.PA_E4M3), 2),  # q is 16-bit
     (dict(dt=pa.PA_F32), 2),
+    (dict(kvdt=pa.PA_BF16), 2),                 # a 16-bit cache is of q's dtype
+    (dict(kvdt=pa.PA_E4M3, kvs=0.0), 1),        # an E4M3 cache needs a positive finite scale
+    (dict(kvdt=pa.PA_E4M3, kvs=float("inf")), 1),
+    (dict(kvdt=pa.PA_E4M3, kvs=float("nan")), 1),
     (dict(scale=float("inf")), 1),
     (dict(mq=-1), 1),
     (dict(B=-1), 1),

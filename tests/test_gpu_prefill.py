@@ -18,6 +18,7 @@ from paged_kv_cache_296_gb300 import binding as pa
 from paged_kv_cache_296_gb300 import workloads as wl
 
 from harness import ATOL, ULP1, bits_of
+from oracle import e4m3
 
 pytestmark = pytest.mark.gpu
 
@@ -204,3 +205,86 @@ def test_growing_logits_rescale_the_accumulator(dtype, head_size):
                 W.k_new[qsl[i] + p - (L - nq[i])] = val
     W.q.fill_(1.0)
     full_check(W)
+
+
+# ---------------------------------------------------------------- an E4M3 cache
+
+def fp8_check(spec, seed, poison=True):
+    """The spec's pool values as the fp32 sources of an E4M3 cache, with the
+    per-tensor kv_scale = amax / 448 over them and the step's new K/V.  The GPU
+    fills its cache through pa_reshape_and_cache; the oracle quantises the same
+    values by its own rule.  Both caches must agree byte for byte, then
+    pa_prefill must agree with the oracle on the dequantised cache."""
+    W = wl.make_prefill_workload(spec, seed, poison=poison)
+    dev = "cuda"
+    src = W.pool.float()                                  # NaN in unused slots when poisoned
+    amax = float(torch.nan_to_num(src, nan=0.0).abs().max())
+    if W.k_new.numel():
+        amax = max(amax, float(W.k_new.float().abs().max()), float(W.v_new.float().abs().max()))
+    kv_scale = amax / 448.0
+    nb, bs, _, hkv, d = src.shape
+    pool = torch.zeros((nb, bs, 2, hkv, d), dtype=torch.uint8, device=dev)
+    kc, vc = pa.kv_views(pool)
+    flat = src.reshape(nb * bs, 2, hkv, d).to(dev)
+    slots = torch.arange(nb * bs, dtype=torch.int64, device=dev)
+    pa.pa_reshape_and_cache(flat[:, 0].contiguous(), flat[:, 1].contiguous(), kc, vc, slots,
+                            kv_scale=kv_scale)
+    if W.q.shape[0]:
+        pa.pa_reshape_and_cache(W.k_new.to(dev), W.v_new.to(dev), kc, vc, W.slot_mapping.to(dev),
+                                kv_scale=kv_scale)
+    out = torch.full(W.q.shape, float("nan"), dtype=W.q.dtype, device=dev)
+    pa.pa_prefill(out, W.q.to(dev), kc, vc, W.block_tables.to(dev), W.context_lens.to(dev),
+                  W.query_start_loc.to(dev), W.max_query_len, W.scale, kv_scale=kv_scale)
+    dt = W.spec.dtype
+    opool = ref.fp8_quantise(bits_of(src), "f32", kv_scale)
+    opool = ref.reshape_and_cache(opool, bits_of(W.k_new), bits_of(W.v_new),
+                                  W.slot_mapping.numpy(), dt, "e4m3", kv_scale)
+    gpool = bits_of(pool.cpu())
+    assert np.array_equal(e4m3.is_nan_code(gpool), e4m3.is_nan_code(opool))
+    live = ~e4m3.is_nan_code(opool)
+    assert np.array_equal(gpool[live], opool[live]), "E4M3 cache bytes differ from the oracle's"
+    got = ref.widen(bits_of(out.cpu()), dt)
+    assert np.isfinite(got).all(), "NaN output: a slot not yet written or unused was read"
+    want = ref.paged_prefill(bits_of(W.q), dt, opool, W.block_tables.numpy(),
+                             W.context_lens.numpy(), W.query_start_loc.numpy(), W.scale,
+                             "e4m3", kv_scale)
+    bound = np.maximum(ATOL["e4m3"],
+                       ULP1[dt] * np.exp2(np.floor(np.log2(np.maximum(np.abs(want), 1e-30)))))
+    bad = ~(np.abs(got - want) <= bound)
+    assert not bad.any(), (f"{spec.name}: {bad.sum()} of {bad.size} outside tolerance, max err "
+                           f"{np.nanmax(np.abs(got - want)):.3e} at {np.argwhere(bad)[:3].tolist()}")
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_e4m3_cache_random_shapes(seed):
+    spec = random_prefill_spec(100 + seed)
+    fp8_check(spec, 5000 + seed)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("head_size,group", [(128, 4), (64, 8), (128, 1)])
+def test_e4m3_cache_tile_and_chunk_edges(dtype, head_size, group):
+    # query counts around the 128-row tile and the 256-row CTA, contexts around
+    # the 128-key chunk and the 16-token block (V rows past L must read as zero)
+    lens = [127, 128, 129, 300, 16, 1, 257]
+    nq = [127, 64, 129, 200, 16, 1, 3]
+    spec = wl.PrefillSpec("e4m3 edges", len(lens), 2 * group, 2, head_size, dtype,
+                          ("fixed", lens), ("fixed", nq), ("factor", 1.3))
+    fp8_check(spec, 77)
+
+
+def test_e4m3_cache_bad_query_layout_is_reported():
+    spec = wl.PrefillSpec("e4m3 bad layout", 2, 8, 2, 128, "bf16", ("fixed", [30, 10]),
+                          ("fixed", [30, 10]))
+    W = wl.make_prefill_workload(spec, 8)
+    pool = torch.zeros(W.pool.shape, dtype=torch.uint8, device="cuda")
+    kc, vc = pa.kv_views(pool)
+    lens = W.context_lens.clone()
+    lens[1] = 5                                    # 10 queries > 5 tokens
+    out = torch.full(W.q.shape, float("nan"), dtype=W.q.dtype, device="cuda")
+    pa.pa_device_status(clear=True)
+    pa.pa_prefill(out, W.q.cuda(), kc, vc, W.block_tables.cuda(), lens.cuda(),
+                  W.query_start_loc.cuda(), W.max_query_len, W.scale, kv_scale=0.5)
+    assert pa.pa_device_status(clear=True) & 2
+    assert torch.isnan(out[30:].float()).all()
+    assert torch.isfinite(out[:30].float()).all()

@@ -148,3 +148,42 @@ def test_sequences_without_queries_are_skipped():
     one = ref.paged_prefill(q, "f16", pool, tables[1:2], np.array(lens[1:2]),
                             np.array([0, 4]), 0.3, "f16")
     assert np.array_equal(got, one)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (4, 4)])
+def test_e4m3_prefill_equals_sdpa_on_library_dequantised_codes(hq, hkv):
+    # The cache holds E4M3 codes; their values are decoded here by PyTorch's
+    # float8_e4m3fn type (a library routine, not the oracle's decoder) and
+    # scaled by kv_scale, then attended by scaled_dot_product_attention.
+    rng = np.random.default_rng(40 + hq)
+    # a kv_scale exact in fp32: the cache's scale is an fp32 value on both sides
+    lens, nq, d, bs, kv_scale = [40, 17, 33], [40, 3, 16], 16, 16, 0.375
+    nb = [-(-L // bs) for L in lens]
+    nblocks = sum(nb) + 2
+    pool = np.full((nblocks, bs, 2, hkv, d), 0x7F, dtype=np.uint8)  # NaN codes where unused
+    perm = rng.permutation(nblocks)
+    tables = np.full((len(lens), max(nb)), -1, dtype=np.int64)
+    codes = []
+    nxt = 0
+    for i, L in enumerate(lens):
+        # any code but the two NaNs (0x7F, 0xFF)
+        c = (rng.integers(0, 0x7F, (L, 2, hkv, d)) | (rng.integers(0, 2, (L, 2, hkv, d)) << 7))
+        c = c.astype(np.uint8)
+        codes.append(c)
+        tables[i, :nb[i]] = perm[nxt:nxt + nb[i]]
+        nxt += nb[i]
+        for j in range(L):
+            pool[tables[i, j // bs], j % bs] = c[j]
+    qsl = np.concatenate([[0], np.cumsum(nq)]).astype(np.int64)
+    q = _f16_bits(rng.standard_normal((int(qsl[-1]), hq, d)))
+    scale = 1.0 / math.sqrt(d)
+    got = ref.paged_prefill(q, "f16", pool, tables, np.array(lens), qsl, scale, "e4m3", kv_scale)
+    for i, (L, n) in enumerate(zip(lens, nq)):
+        vals = torch.from_numpy(codes[i]).view(torch.float8_e4m3fn).to(torch.float64) * kv_scale
+        kt = vals[:, 0].permute(1, 0, 2)[None]   # [1, Hkv, L, D]
+        vt = vals[:, 1].permute(1, 0, 2)[None]
+        qt = torch.from_numpy(ref.widen(q[qsl[i]:qsl[i + 1]], "f16")).permute(1, 0, 2)[None]
+        allowed = torch.arange(L)[None, :] <= (L - n + torch.arange(n))[:, None]
+        want = torch.nn.functional.scaled_dot_product_attention(
+            qt, kt, vt, attn_mask=allowed, scale=scale, enable_gqa=True)[0].permute(1, 0, 2)
+        np.testing.assert_allclose(got[qsl[i]:qsl[i + 1]], want.numpy(), rtol=0, atol=1e-12)
