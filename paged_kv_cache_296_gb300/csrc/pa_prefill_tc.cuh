@@ -39,9 +39,11 @@
 namespace pa {
 
 // KV8: the cache holds E4M3 codes.  The TMA then loads fp8 rows into rings of
-// their own and two converter warps widen each chunk into 16-bit staging planes
-// laid out like the 16-bit rings (one chunk of K, one of V), which the MMAs
-// read; the MMAs run in f16 (every E4M3 value is exact in f16).
+// their own and six converter warps (three for K, three for V) widen each chunk
+// into 16-bit staging planes laid out like the 16-bit rings (one chunk of K, one
+// of V), which the MMAs read; the MMAs run in f16 (every E4M3 value is exact in
+// f16).  The widening (cvt.f16x2.e4m3x2) is throughput-bound, so it is spread
+// over as many warps as the 128-register budget of 16 warps allows.
 template <int D, bool KV8>
 struct PrefillTcCfg {
   static constexpr int kRows = 128;                        // rows of one tile (TMEM lanes)
@@ -71,8 +73,9 @@ struct PrefillTcCfg {
   static constexpr int kSoftmaxThreads = 128 * kTiles;
   static constexpr int kProducerWarp = kSoftmaxThreads / 32;
   static constexpr int kMmaWarp = kProducerWarp + 1;
-  static constexpr int kConvWarp = kMmaWarp + 1;           // KV8: K converter, then V converter
-  static constexpr int kThreads = kSoftmaxThreads + 64 + (KV8 ? 64 : 0);
+  static constexpr int kConvWarp = kMmaWarp + 1;           // KV8: K converters, then V converters
+  static constexpr int kConvWarps = 3;                     // KV8: warps per operand
+  static constexpr int kThreads = kSoftmaxThreads + 64 + (KV8 ? 64 * kConvWarps : 0);
   // TMEM columns of tile t (base 256 t): O [0, D); S(c) in fp32 at [128, 256),
   // then P(c) (16-bit pairs) over it once the softmax has read it: keys 0..63
   // at [128, 160), keys 64..127 at [192, 224)
@@ -329,14 +332,14 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
     for (int i = 0; i < kR; ++i) {
       // KV8: a ring slot is released by the converter warp's 32 lanes
       mbar_init(&full_k[i], 1);
-      mbar_init(&empty_k[i], KV8 ? 32 : 1);
+      mbar_init(&empty_k[i], KV8 ? 32 * C::kConvWarps : 1);
       mbar_init(&full_v[i], 1);
-      mbar_init(&empty_v[i], KV8 ? 32 : 1);
+      mbar_init(&empty_v[i], KV8 ? 32 * C::kConvWarps : 1);
     }
     if constexpr (KV8) {
-      mbar_init(kst_full, 32);
+      mbar_init(kst_full, 32 * C::kConvWarps);
       mbar_init(kst_empty, 1);
-      mbar_init(vst_full, 32);
+      mbar_init(vst_full, 32 * C::kConvWarps);
       mbar_init(vst_empty, 1);
     }
     for (int t = 0; t < kT; ++t) {
@@ -521,11 +524,14 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
     __syncwarp();
   } else if (KV8 && warp >= C::kConvWarp) {
     // ------------------------------------------------------------ converters (KV8)
-    // Warp kConvWarp widens K, the next warp V: each 16-byte run of a landed
-    // fp8 row (16 codes) becomes 32 bytes of f16 in the staging planes, at the
-    // positions the TMA would have put a 16-bit row.  V rows of keys at or past
+    // Warps kConvWarp .. + kConvWarps - 1 widen K, the next kConvWarps V: each
+    // 16-byte run of a landed fp8 row (16 codes) becomes 32 bytes of f16 in the
+    // staging planes, at the positions the TMA would have put a 16-bit row; a
+    // lane loads kBatch runs before converting them.  V rows of keys at or past
     // L become zeros (a P of 0 times a stale code must not reach the sum).
-    const bool isv = warp != C::kConvWarp;
+    const bool isv = warp >= C::kConvWarp + C::kConvWarps;
+    const int cw = (warp - C::kConvWarp) % C::kConvWarps;  // this warp's share of the runs
+    const int cl = cw * 32 + lane;
     uint64_t* full = isv ? full_v : full_k;
     uint64_t* empty = isv ? empty_v : empty_k;
     uint64_t* st_full = isv ? vst_full : kst_full;
@@ -542,25 +548,44 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
         break;
       }
       const int nrows = 16 * min(kBpc, nkb - kBpc * c);
-      for (int u = lane; u < nrows * kRuns; u += 32) {
-        const int r = u / kRuns, j = u % kRuns;
-        // the TMA's swizzle of the [16 rows][D bytes] tile of block r / 16
-        const uint32_t o = (uint32_t)((r & 15) * D + j * 16);
-        const uint32_t sw = D == 128 ? (o ^ (((o >> 7) & 7u) << 4)) : (o ^ (((o >> 7) & 3u) << 4));
-        const uint4 x = *reinterpret_cast<const uint4*>(ring + slot * C::kChunkBytes8 +
-                                                        (r >> 4) * (16 * D) + sw);
-        uint4 y0 = make_uint4(0u, 0u, 0u, 0u), y1 = y0;
-        if (!isv || kBpc * 16 * c + r < L) {
-          y0 = make_uint4(e4m3x2_to_f16x2((uint16_t)(x.x & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(x.x >> 16)),
-                          e4m3x2_to_f16x2((uint16_t)(x.y & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(x.y >> 16)));
-          y1 = make_uint4(e4m3x2_to_f16x2((uint16_t)(x.z & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(x.z >> 16)),
-                          e4m3x2_to_f16x2((uint16_t)(x.w & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(x.w >> 16)));
+      constexpr int kStride = 32 * C::kConvWarps;  // runs between one lane's consecutive runs
+      constexpr int kBatch = 4;                    // runs loaded before any is converted
+      for (int u0 = cl; u0 < nrows * kRuns; u0 += kBatch * kStride) {
+        uint4 x[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const int u = u0 + b * kStride;
+          const int r = u / kRuns, j = u % kRuns;
+          // the TMA's swizzle of the [16 rows][D bytes] tile of block r / 16
+          const uint32_t o = (uint32_t)((r & 15) * D + j * 16);
+          const uint32_t sw =
+              D == 128 ? (o ^ (((o >> 7) & 7u) << 4)) : (o ^ (((o >> 7) & 3u) << 4));
+          if (u < nrows * kRuns)
+            x[b] = *reinterpret_cast<const uint4*>(ring + slot * C::kChunkBytes8 +
+                                                   (r >> 4) * (16 * D) + sw);
         }
-        // elements 16 j .. 16 j + 15: piece j / 4, 16-byte chunks 2 (j % 4) and + 1
-        const int cc = 2 * (j % 4);
-        uint8_t* row = st + (j / 4) * C::kPlaneBytes + r * 128;
-        *reinterpret_cast<uint4*>(row + ((cc ^ (r & 7)) << 4)) = y0;
-        *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (r & 7)) << 4)) = y1;
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const int u = u0 + b * kStride;
+          if (u >= nrows * kRuns) break;
+          const int r = u / kRuns, j = u % kRuns;
+          uint4 y0 = make_uint4(0u, 0u, 0u, 0u), y1 = y0;
+          if (!isv || kBpc * 16 * c + r < L) {
+            y0 = make_uint4(e4m3x2_to_f16x2((uint16_t)(x[b].x & 0xFFFFu)),
+                            e4m3x2_to_f16x2((uint16_t)(x[b].x >> 16)),
+                            e4m3x2_to_f16x2((uint16_t)(x[b].y & 0xFFFFu)),
+                            e4m3x2_to_f16x2((uint16_t)(x[b].y >> 16)));
+            y1 = make_uint4(e4m3x2_to_f16x2((uint16_t)(x[b].z & 0xFFFFu)),
+                            e4m3x2_to_f16x2((uint16_t)(x[b].z >> 16)),
+                            e4m3x2_to_f16x2((uint16_t)(x[b].w & 0xFFFFu)),
+                            e4m3x2_to_f16x2((uint16_t)(x[b].w >> 16)));
+          }
+          // elements 16 j .. 16 j + 15: piece j / 4, 16-byte chunks 2 (j % 4) and + 1
+          const int cc = 2 * (j % 4);
+          uint8_t* row = st + (j / 4) * C::kPlaneBytes + r * 128;
+          *reinterpret_cast<uint4*>(row + ((cc ^ (r & 7)) << 4)) = y0;
+          *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (r & 7)) << 4)) = y1;
+        }
       }
       fence_proxy_async_shared();  // the MMAs read the staging through the async proxy
       mbar_arrive(st_full);
