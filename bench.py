@@ -47,8 +47,8 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 PREFILL_METRIC = "paged-prefill TFLOP/s (causal attention FLOPs); µs per prefill step"
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-KERNEL_SOURCES = ["pa_decode_kernel.cuh", "pa_ptx.cuh", "pa_decode_launch.cuh", "pa_api.cu",
-                  "pa_cache.cu"]
+KERNEL_SOURCES = ["pa_decode_kernel.cuh", "pa_ptx.cuh", "pa_decode_launch.cuh", "pa_cache.cu",
+                  "pa_decode_f16.cu", "pa_decode_bf16.cu", "pa_decode_e4m3.cu"]
 
 
 # ---------------------------------------------------------------- helpers
@@ -107,8 +107,7 @@ def tensor_peak():
 
 
 PREFILL_SOURCES = ["pa_prefill_tc.cuh", "pa_prefill_params.cuh", "pa_prefill_launch.cuh", "pa_prefill.cu",
-                   "pa_prefill_fp8.cu", "pa_ptx.cuh",
-                   "pa_cache.cu", "pa_api.cu"]
+                   "pa_prefill_fp8.cu", "pa_ptx.cuh", "pa_cache.cu"]
 
 
 def kernel_source_hash(sources=None):
