@@ -9,6 +9,7 @@ import os
 import socket
 import subprocess
 import sys
+import time
 
 import pytest
 import torch
@@ -72,6 +73,18 @@ def test_reference_arm_prints_one_line():
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["steps"] == 2 and d["warmup"] == 3
+
+
+def test_reference_arm_is_bounded_for_many_steps():
+    # the whole run holds about --ref-seconds of oracle time whatever --steps is
+    t0 = time.perf_counter()
+    r = _run_bench(["--impl", "reference", "--config", "2", "--steps", "2000", "--warmup", "20",
+                    "--ref-seconds", "2"], {})
+    wall = time.perf_counter() - t0
+    assert r.returncode == 0, r.stderr
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d["steps"] == 2000 and d["value"] > 0
+    assert wall < 120, f"2000 reference steps took {wall:.0f} s"
 
 
 def test_reference_arm_other_ranks_exit_quietly():
