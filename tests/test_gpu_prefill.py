@@ -288,3 +288,47 @@ def test_e4m3_cache_bad_query_layout_is_reported():
     assert pa.pa_device_status(clear=True) & 2
     assert torch.isnan(out[30:].float()).all()
     assert torch.isfinite(out[:30].float()).all()
+
+
+@pytest.mark.parametrize("n", sorted(wl.PREFILL_SPECS))
+def test_e4m3_cache_full_size_sampled_rows(n):
+    """The prefill workloads over an E4M3 cache, run as bench.py runs them
+    (runner.PrefillStep): for sampled query rows, the oracle quantises the
+    sequence's source values (the step's own K/V at the query positions) by its
+    rule, the GPU cache bytes of those blocks must equal it, and the row's
+    output must match the oracle on the sequence cut to that row."""
+    from paged_kv_cache_296_gb300.runner import PrefillStep
+    W = wl.make_prefill_workload(wl.PREFILL_SPECS[n], 10 + n, device="cuda")
+    S = PrefillStep(W, kv_dtype="e4m3")
+    S.step()
+    assert pa.pa_device_status(clear=True) == 0
+    dt = W.spec.dtype
+    got_all = ref.widen(bits_of(S.out.cpu()), dt)
+    assert np.isfinite(got_all).all()
+    lens = W.context_lens.cpu().numpy()
+    qsl = W.query_start_loc.cpu().numpy()
+    tables = W.block_tables.cpu().numpy()
+    k_new, v_new = W.k_new.cpu().float(), W.v_new.cpu().float()
+    rng = np.random.default_rng(100 + n)
+    for i in rng.choice(W.spec.num_seqs, size=min(4, W.spec.num_seqs), replace=False):
+        nq = int(qsl[i + 1] - qsl[i])
+        L = int(lens[i])
+        t = int(rng.integers(nq))
+        pos = L - nq + t
+        nb = pos // 16 + 1
+        blocks = torch.from_numpy(tables[i, :nb].astype(np.int64))
+        src = W.pool[blocks.cuda()].cpu().float()                   # [nb, 16, 2, Hkv, D]
+        for p in range(L - nq, pos + 1):                             # the step's own tokens
+            src[p // 16, p % 16, 0] = k_new[qsl[i] + p - (L - nq)]
+            src[p // 16, p % 16, 1] = v_new[qsl[i] + p - (L - nq)]
+        opool = ref.fp8_quantise(bits_of(src), "f32", S.kv_scale)
+        gpool = bits_of(S.pool[blocks.cuda()].cpu())
+        # slots past pos in the last block are not part of the cut sequence
+        keep = np.zeros(opool.shape, dtype=bool)
+        keep.reshape(nb * 16, -1)[:pos + 1] = True
+        assert np.array_equal(gpool[keep], opool[keep]), f"seq {i}: cache bytes differ"
+        want = ref.paged_prefill(bits_of(W.q[qsl[i] + t:qsl[i] + t + 1].cpu()), dt, opool,
+                                 np.arange(nb)[None, :], np.array([pos + 1]), np.array([0, 1]),
+                                 W.scale, "e4m3", S.kv_scale)
+        err = np.abs(got_all[qsl[i] + t] - want[0])
+        assert err.max() <= ATOL["e4m3"], f"seq {i} token {t}: max err {err.max():.3e}"
