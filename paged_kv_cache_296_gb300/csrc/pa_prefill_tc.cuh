@@ -734,6 +734,8 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
     tc_fence_after();
     if (ok) {  // every lane loads (warp-collective); only rows of the tile are stored
       const bool has = l > 0.f;
+      // one reciprocal per row, then products: o * (s / l) within an ulp of o * s / l
+      const float inv = has ? (KV8 ? __fdiv_rn(p.out_scale, l) : __frcp_rn(l)) : 0.f;
       uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + qoff;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 16) {
@@ -742,12 +744,9 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
         uint32_t w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          float a = has ? __fdiv_rn(o[2 * i], l) : 0.f;
-          float bv = has ? __fdiv_rn(o[2 * i + 1], l) : 0.f;
-          if constexpr (KV8) {  // V held codes: the dequantised mean is kv_scale times it
-            a = __fmul_rn(a, p.out_scale);
-            bv = __fmul_rn(bv, p.out_scale);
-          }
+          // (KV8: V held codes, so the dequantised mean is out_scale = kv_scale times it)
+          const float a = __fmul_rn(o[2 * i], inv);
+          const float bv = __fmul_rn(o[2 * i + 1], inv);
           w[i] = pf_pack<QT>(a, bv);
         }
         if (live) {
