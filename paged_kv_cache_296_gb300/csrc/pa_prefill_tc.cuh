@@ -88,11 +88,6 @@ struct PrefillTcCfg {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
 // kind::f16 instruction descriptor: f32 accumulator, A/B of type `bf16` (else
 // f16), M, N, A K-major, B K-major (0) or MN-major (1).
 __device__ __forceinline__ uint32_t umma_idesc(bool bf16, int m, int n, int b_mn) {
@@ -101,15 +96,18 @@ __device__ __forceinline__ uint32_t umma_idesc(bool bf16, int m, int n, int b_mn
          ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-// The same descriptor split in two words: the low word holds the start address
-// (bits 0-13, in 16-byte units) and the leading byte offset, the high word the
-// stride byte offset, the version bit and the swizzle mode.  Every shared
-// address here is below 2^18, so adding a byte offset / 16 to the low word
-// never carries out of the address field.
+// Shared-memory matrix descriptor of a 128B-swizzled operand, in two words.
+// The low word holds the start address (bits 0-13, in 16-byte units) and the
+// leading byte offset (bits 16-29, in 16-byte units; 16 bytes for K-major operands, the
+// distance between 64-element pieces for MN-major ones); the high word the
+// stride byte offset (1024: eight 128-byte rows), the version bit (46) and the
+// swizzle mode (bits 61-63 = 2, 128B).  Every shared address here is below
+// 2^18, so adding a byte offset / 16 to the low word never carries out of the
+// address field.
 __device__ __forceinline__ uint32_t umma_desc_lo(uint32_t saddr, uint32_t lbo) {
   return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
-constexpr uint32_t kUmmaDescHiSw128 = (1024u >> 4) | (1u << 14) | (2u << 29);  // SBO 1024
+constexpr uint32_t kUmmaDescHiSw128 = (1024u >> 4) | (1u << 14) | (2u << 29);
 __device__ __forceinline__ uint64_t umma_desc_join(uint32_t lo) {
   return ((uint64_t)kUmmaDescHiSw128 << 32) | lo;
 }
