@@ -2,7 +2,7 @@
 
 This package is the plain, slow, obviously-correct definition of what the
 GPU path computes, in NumPy float64.  It exists so that tests, the smoke
-check and the benchmark's CPU baseline can judge the CUDA library.  The
+check and the benchmark's CPU baseline can test the CUDA library.  The
 product path never imports, calls or links anything here, and nothing here
 imports the product package: the two share no code.  Only the seeded input
 generators (``paged_kv_cache_296_gb300.workloads``) feed both sides.
