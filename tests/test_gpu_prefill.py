@@ -332,3 +332,30 @@ def test_e4m3_cache_full_size_sampled_rows(n):
                                  W.scale, "e4m3", S.kv_scale)
         err = np.abs(got_all[qsl[i] + t] - want[0])
         assert err.max() <= ATOL["e4m3"], f"seq {i} token {t}: max err {err.max():.3e}"
+
+
+def test_context_length_past_the_table_is_cut_to_it():
+    # A context length beyond max_blocks_per_seq * 16 is read as the table's
+    # capacity: no entry past the row is read, and the outputs equal the
+    # oracle's on the cut length (the queries are then the last tokens of it).
+    spec = wl.PrefillSpec("past the table", 2, 8, 2, 64, "f16", ("fixed", [40, 64]),
+                          ("fixed", [8, 16]))
+    W = wl.make_prefill_workload(spec, 31, poison=True)
+    width = W.block_tables.shape[1]
+    lens = W.context_lens.clone()
+    lens[1] = width * 16 + 50                    # past the row's capacity
+    cut = W.context_lens.clone()
+    cut[1] = width * 16
+    dev = "cuda"
+    pool = W.pool.to(dev, copy=True)
+    kc, vc = pa.kv_views(pool)
+    pa.pa_reshape_and_cache(W.k_new.to(dev), W.v_new.to(dev), kc, vc, W.slot_mapping.to(dev))
+    out = torch.full(W.q.shape, float("nan"), dtype=W.q.dtype, device=dev)
+    pa.pa_prefill(out, W.q.to(dev), kc, vc, W.block_tables.to(dev), lens.to(dev),
+                  W.query_start_loc.to(dev), W.max_query_len, W.scale)
+    opool = oracle_pool(W)
+    got = ref.widen(bits_of(out.cpu()), "f16")
+    assert np.isfinite(got).all()
+    want = ref.paged_prefill(bits_of(W.q), "f16", opool, W.block_tables.numpy(), cut.numpy(),
+                             W.query_start_loc.numpy(), W.scale, "f16")
+    check_close(got, want, "f16", "cut length")
