@@ -10,8 +10,9 @@
 //   * warps 0-3 and 4-7 (softmax, one group per tile): thread r owns row r of
 //     its tile, which is TMEM lane r of the tile's 256 columns.  They
 //     stage Q into shared memory, run the online softmax on each S chunk read
-//     from TMEM, write P (16-bit) back over it (keys 0..63 at columns 0..31,
-//     keys 64..127 at 64..95), rescale O in TMEM when a row's
+//     from TMEM (in one load, or in two halves when an E4M3 cache leaves 128
+//     registers a thread), write P (16-bit) back over it (keys 0..63 at columns
+//     0..31, keys 64..127 at 64..95), rescale O in TMEM when a row's
 //     running maximum grows by more than kRescale (log2 units; otherwise the
 //     exponentials keep the older maximum, so P stays below 2^kRescale), and
 //     finally normalise O and store the rows.
@@ -175,6 +176,34 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 128 consecutive columns and the wait for them in one statement.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+  uint32_t r[128];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]),
+        "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]),
+        "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]),
+        "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]),
+        "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]),
+        "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]),
+        "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]),
+        "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]),
+        "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Packed pairs of fp32 (the f32x2 forms of fma / add).
@@ -631,58 +660,63 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
     }
     const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
     float m_run = -INFINITY, m_used = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int c = 0; c < nchunks; ++c) {
-      if (!wait_all(&s_full[t], (uint32_t)c & 1u)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // Two passes over S(c) keep one 64-column half in registers at a time:
-      // the maxima of both halves, then half 1 (P at columns 64..95) and half 0
-      // read again (P at columns 0..31); each P half goes over S values already read.
-      const int key0 = 128 * c;
-      const bool diag = __any_sync(kAll, key0 + 127 > pos);
-      auto load_half = [&](float (&sh)[64], int h) {
-        tmem_ld64(scol + 64 * h, sh);
-        if (diag) {
-          // causal (also covers keys past L and past the last block)
+    // scores of keys past the row's position (also keys past L and past the last block)
+    auto mask_keys = [&](auto& v, int key_base) {
+      constexpr int N = sizeof(v) / sizeof(float);
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (key0 + 64 * h + i > pos) sh[i] = -INFINITY;
-        }
-      };
+      for (int i = 0; i < N; ++i)
+        if (key_base + i > pos) v[i] = -INFINITY;
+    };
+    // the maximum of raw scores (the scale is positive, so it commutes): eight
+    // interleaved chains of 3-input max
+    auto row_max = [&](const auto& v) {
+      constexpr int N = sizeof(v) / sizeof(float);
+      static_assert(N % 16 == 0, "whole 16-key groups");
       float mq[8];
-      {
-        float sh[64];
-        load_half(sh, 0);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mq[k] = fmax3(sh[8 * k], sh[8 * k + 1], sh[8 * k + 2]);
+      for (int k = 0; k < 8; ++k) mq[k] = v[k];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mq[k] = fmax3(mq[k], sh[8 * k + 3], sh[8 * k + 4]);
+      for (int e = 8; e + 16 <= N; e += 16) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mq[k] = fmax3(mq[k], sh[8 * k + 5], sh[8 * k + 6]);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mq[k] = fmaxf(mq[k], sh[8 * k + 7]);
+        for (int k = 0; k < 8; ++k) mq[k] = fmax3(mq[k], v[e + k], v[e + 8 + k]);
       }
-      float s1[64];
-      load_half(s1, 1);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mq[k] = fmax3(mq[k], s1[8 * k], s1[8 * k + 1]);
+      for (int k = 0; k < 8; ++k) mq[k] = fmaxf(mq[k], v[N - 8 + k]);
+      return fmax3(fmax3(mq[0], mq[1], mq[2]), fmax3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
+    };
+    // p = 2^(s * scale_log2 - m_used) for the keys of v (a multiple of 32 from key
+    // 64 h), one rounding per exponent, stored as 16-bit pairs over the scores:
+    // keys 0..63 at columns 0..31, keys 64..127 at 64..95 of the buffer; the
+    // row sum in fp32 over two interleaved partial sums of pairs
+    auto exp_store = [&](const auto& v, uint32_t col, uint64_t nm2, uint64_t& acc0,
+                         uint64_t& acc1) {
+      constexpr int N = sizeof(v) / sizeof(float);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mq[k] = fmax3(mq[k], s1[8 * k + 2], s1[8 * k + 3]);
+      for (int q = 0; q < N / 32; ++q) {
+        uint32_t pk[16];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mq[k] = fmax3(mq[k], s1[8 * k + 4], s1[8 * k + 5]);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mq[k] = fmax3(mq[k], s1[8 * k + 6], s1[8 * k + 7]);
-      const float mx = fmax3(fmax3(mq[0], mq[1], mq[2]), fmax3(mq[3], mq[4], mq[5]),
-                             fmaxf(mq[6], mq[7]));
+        for (int i = 0; i < 16; i += 2) {
+          const int e = 32 * q + 2 * i;
+          const float2 x = f2_unpack(f2_fma(f2_pack(v[e], v[e + 1]), sc2, nm2));
+          const float2 y = f2_unpack(f2_fma(f2_pack(v[e + 2], v[e + 3]), sc2, nm2));
+          const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+          const float p2 = ex2_approx(y.x), p3 = ex2_approx(y.y);
+          pk[i] = pf_pack<MT>(p0, p1);
+          pk[i + 1] = pf_pack<MT>(p2, p3);
+          acc0 = f2_add(acc0, f2_pack(p0, p1));
+          acc1 = f2_add(acc1, f2_pack(p2, p3));
+        }
+        tmem_st16u(col + 64 * (q / 2) + 16 * (q % 2), pk);
+      }
+    };
+    // the running maximum takes the chunk's; O (and l) of the rows whose maximum
+    // grew by more than kRescale are rescaled: S(c) completed after P V(c - 1),
+    // so O holds every earlier chunk (the warp's other rows take part with a
+    // factor of 1); returns -m_used packed for exp_store
+    auto update_max = [&](float mx, int c) {
       m_run = fmaxf(m_run, __fmul_rn(mx, p.scale_log2));
       const bool need = m_run > m_used + C::kRescale;
       if (c > 0 && __any_sync(kAll, need)) {
-        // rescale O (and l) of the rows that need it: S(c) completed after
-        // P V(c - 1), so O holds every earlier chunk; the warp's other rows take
-        // part with a factor of 1
         const float alpha = need ? ex2_approx(__fsub_rn(m_used, m_run)) : 1.f;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 16) {
@@ -695,31 +729,46 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
         l = __fmul_rn(l, alpha);
       }
       if (need) m_used = m_run;
-      // p = 2^(s * scale_log2 - m_used), one rounding per exponent; the row
-      // sum in fp32 over interleaved partial sums of pairs
-      const uint64_t nm2 = f2_pack(-m_used, -m_used);
+      return f2_pack(-m_used, -m_used);
+    };
+    bool ok = true;
+    for (int c = 0; c < nchunks; ++c) {
+      if (!wait_all(&s_full[t], (uint32_t)c & 1u)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int key0 = 128 * c;
+      const bool diag = __any_sync(kAll, key0 + 127 > pos);  // warp-uniform
       uint64_t acc0 = 0ull, acc1 = 0ull;
-      auto exp_half = [&](const float (&sh)[64], uint32_t col) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float2 x = f2_unpack(f2_fma(f2_pack(sh[2 * i], sh[2 * i + 1]), sc2, nm2));
-          const float2 y = f2_unpack(f2_fma(f2_pack(sh[2 * i + 2], sh[2 * i + 3]), sc2, nm2));
-          const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-          const float p2 = ex2_approx(y.x), p3 = ex2_approx(y.y);
-          pk[i] = pf_pack<MT>(p0, p1);
-          pk[i + 1] = pf_pack<MT>(p2, p3);
-          acc0 = f2_add(acc0, f2_pack(p0, p1));
-          acc1 = f2_add(acc1, f2_pack(p2, p3));
+      if constexpr (!KV8) {
+        // all of S(c) in registers: one load, one wait
+        float sv[128];
+        tmem_ld128(scol, sv);
+        if (diag) mask_keys(sv, key0);
+        const uint64_t nm2 = update_max(row_max(sv), c);
+        exp_store(sv, scol, nm2, acc0, acc1);
+      } else {
+        // 128 registers a thread (16 warps): one 64-column half at a time, the
+        // maxima of both, then half 1 and half 0 read again
+        float mx;
+        {
+          float sh[64];
+          tmem_ld64(scol, sh);
+          if (diag) mask_keys(sh, key0);
+          mx = row_max(sh);
         }
-        tmem_st16u(col, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
-        tmem_st16u(col + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
-      };
-      exp_half(s1, scol + 64);
-      {
-        float sh[64];
-        load_half(sh, 0);
-        exp_half(sh, scol);
+        float s1[64];
+        tmem_ld64(scol + 64, s1);
+        if (diag) mask_keys(s1, key0 + 64);
+        const uint64_t nm2 = update_max(fmaxf(mx, row_max(s1)), c);
+        exp_store(s1, scol + 64, nm2, acc0, acc1);
+        {
+          float sh[64];
+          tmem_ld64(scol, sh);
+          if (diag) mask_keys(sh, key0);
+          exp_store(sh, scol, nm2, acc0, acc1);
+        }
       }
       const float2 a0 = f2_unpack(acc0), a1 = f2_unpack(acc1);
       l = __fadd_rn(l, __fadd_rn(__fadd_rn(a0.x, a0.y), __fadd_rn(a1.x, a1.y)));
