@@ -151,6 +151,76 @@ def profiled_prefill_traffic(n, fp8=False):
     return float(m_tr.group(1))
 
 
+def pipelined_e2e(S, step_fn, device):
+    """Steps through the public API with host buffers, as a serving loop runs
+    them: every step copies its inputs in from pinned host memory (one packed
+    buffer) and its output back.  Two device copies of the inputs and of the
+    output let a copy stream move step i+1's inputs in and step i-1's output
+    back while step i computes; each step still makes its own two copies.
+    Returns (enqueue(k): k such steps on the current stream, verify(): the
+    last enqueued step's output as copied back equals a plain step's bit for
+    bit, h2d bytes per step, d2h bytes per step)."""
+    names = list(S.STEP_INPUTS)
+    hosts, devs, sets = [], [], []
+    for _ in range(2):
+        h, d = S.stage_inputs()
+        hosts.append(h)
+        devs.append(d)
+        sets.append({k: getattr(S, k) for k in names})
+    outs = [S.out, torch.empty_like(S.out)]
+    out_host = [torch.empty(S.out.shape, dtype=S.out.dtype).pin_memory() for _ in range(2)]
+    xs = torch.cuda.Stream(device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+
+    last = [0]
+
+    def bind(b):
+        for k, v in sets[b].items():
+            setattr(S, k, v)
+        S.out = outs[b]
+
+    def verify():
+        torch.cuda.synchronize(device)
+        got = out_host[last[0]].clone()
+        bind(0)
+        step_fn()
+        torch.cuda.synchronize(device)
+        want = S.out.cpu()
+        if not torch.equal(got.view(torch.uint8), want.view(torch.uint8)):
+            raise RuntimeError("pipelined e2e output differs from a plain step's")
+
+    def enqueue(k):
+        cs = torch.cuda.current_stream(device)
+        fork, join = torch.cuda.Event(), torch.cuda.Event()
+        fork.record(cs)
+        xs.wait_event(fork)
+        for i in range(k):
+            b = i % 2
+            with torch.cuda.stream(xs):
+                if i >= 2:
+                    xs.wait_event(ev_done[b])        # step i-2 no longer reads buffer b
+                devs[b].copy_(hosts[b], non_blocking=True)
+                ev_in[b].record(xs)
+                if i >= 1:
+                    xs.wait_event(ev_done[1 - b])    # step i-1's output is final
+                    out_host[1 - b].copy_(outs[1 - b], non_blocking=True)
+            cs.wait_event(ev_in[b])
+            bind(b)
+            step_fn()
+            ev_done[b].record(cs)
+        b = (k - 1) % 2
+        last[0] = b
+        with torch.cuda.stream(xs):
+            xs.wait_event(ev_done[b])
+            out_host[b].copy_(outs[b], non_blocking=True)
+            join.record(xs)
+        cs.wait_event(join)
+
+    return (enqueue, verify, hosts[0].numel(),
+            out_host[0].numel() * out_host[0].element_size())
+
+
 class ClockSampler:
     """nvidia-smi SM clock / throttle-reason samples while the timed region runs."""
 
@@ -418,21 +488,26 @@ def run_ours(args, world, rank, local):
     e2e = None
     if not args.no_e2e:
         # the step's inputs live packed in one pinned host buffer (q, new k/v,
-        # slot mapping, block tables, lengths): one host-to-device copy per step
-        host_in, dev_in = S.stage_inputs()
-        out_host = torch.empty(S.out.shape, dtype=S.out.dtype).pin_memory()
-        h2d = host_in.numel()
-        d2h = out_host.numel() * out_host.element_size()
-
-        def e2e_step():
-            dev_in.copy_(host_in, non_blocking=True)
-            step_fn()
-            out_host.copy_(S.out, non_blocking=True)
-
-        for _ in range(args.warmup):
-            e2e_step()
+        # slot mapping, block tables, lengths): one host-to-device copy per
+        # step, overlapped with the previous step's kernels (double buffers)
+        enqueue, verify, h2d, d2h = pipelined_e2e(S, step_fn, device)
+        enqueue(max(2, args.warmup))
         torch.cuda.synchronize(device)
-        run_e2e = make_runner(e2e_step, n)
+        if args.no_graph:
+            def run_e2e():
+                enqueue(n)
+        else:
+            spg = steps_per_graph(n)
+            ge = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(ge):
+                enqueue(spg)
+            ge.replay()
+            torch.cuda.synchronize(device)
+            graphs.append(ge)
+
+            def run_e2e():
+                for _ in range(n // spg):
+                    ge.replay()
         s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         s2.record(stream)
@@ -440,6 +515,7 @@ def run_ours(args, world, rank, local):
         e2.record(stream)
         torch.cuda.synchronize(device)
         barrier(world)
+        verify()
         e2e_ms = max_over_ranks(s2.elapsed_time(e2) / n, world, device)
         e2e_gbs = sum_over_ranks(kv_bytes, world, device) / (e2e_ms * 1e-3) / 1e9
         e2e = {"value": round(e2e_gbs, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
@@ -632,23 +708,32 @@ def run_prefill(args, world, rank, local):
 
     e2e = None
     if not args.no_e2e:
-        host_in, dev_in = S.stage_inputs()
-        out_host = torch.empty(S.out.shape, dtype=S.out.dtype).pin_memory()
+        # inputs copied in and the output back every step, overlapped with the
+        # neighbouring steps' kernels (double buffers)
+        enqueue, verify, h2d, d2h = pipelined_e2e(S, S.step, device)
+        enqueue(max(2, args.warmup))
+        torch.cuda.synchronize(device)
+        if args.no_graph:
+            def run_e2e():
+                enqueue(n)
+        else:
+            spg = max(d for d in range(1, min(n, 20) + 1) if n % d == 0)
+            ge = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(ge):
+                enqueue(spg)
+            ge.replay()
+            torch.cuda.synchronize(device)
+            graphs.append(ge)
 
-        def e2e_step():
-            dev_in.copy_(host_in, non_blocking=True)
-            S.step()
-            out_host.copy_(S.out, non_blocking=True)
-
-        for _ in range(args.warmup):
-            e2e_step()
-        run_e2e, _ = runner(e2e_step)
+            def run_e2e():
+                for _ in range(n // spg):
+                    ge.replay()
         e_ms, _, _ = timed(run_e2e)
+        verify()
         e_ms = max_over_ranks(e_ms, world, device)
         e2e = {"value": round(sum_over_ranks(flops, world, device) / (e_ms * 1e-3) / 1e12, 2),
                "unit": "TFLOP/s", "ms_per_step": round(e_ms, 5),
-               "h2d_bytes_per_step": host_in.numel(),
-               "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
