@@ -155,8 +155,9 @@ def pipelined_e2e(S, step_fn, device):
     """Steps through the public API with host buffers, as a serving loop runs
     them: every step copies its inputs in from pinned host memory (one packed
     buffer) and its output back.  Two device copies of the inputs and of the
-    output let a copy stream move step i+1's inputs in and step i-1's output
-    back while step i computes; each step still makes its own two copies.
+    output let two copy streams (one per direction) move step i+1's inputs in
+    and step i-1's output back while step i computes; each step still makes
+    its own two copies.
     Returns (enqueue(k): k such steps on the current stream, verify(): the
     last enqueued step's output as copied back equals a plain step's bit for
     bit, h2d bytes per step, d2h bytes per step)."""
@@ -169,9 +170,11 @@ def pipelined_e2e(S, step_fn, device):
         sets.append({k: getattr(S, k) for k in names})
     outs = [S.out, torch.empty_like(S.out)]
     out_host = [torch.empty(S.out.shape, dtype=S.out.dtype).pin_memory() for _ in range(2)]
-    xs = torch.cuda.Stream(device)
+    xs = torch.cuda.Stream(device)   # host to device
+    ys = torch.cuda.Stream(device)   # device to host
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
     last = [0]
 
@@ -192,9 +195,10 @@ def pipelined_e2e(S, step_fn, device):
 
     def enqueue(k):
         cs = torch.cuda.current_stream(device)
-        fork, join = torch.cuda.Event(), torch.cuda.Event()
+        fork, join_x, join_y = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
         fork.record(cs)
         xs.wait_event(fork)
+        ys.wait_event(fork)
         for i in range(k):
             b = i % 2
             with torch.cuda.stream(xs):
@@ -202,20 +206,26 @@ def pipelined_e2e(S, step_fn, device):
                     xs.wait_event(ev_done[b])        # step i-2 no longer reads buffer b
                 devs[b].copy_(hosts[b], non_blocking=True)
                 ev_in[b].record(xs)
-                if i >= 1:
-                    xs.wait_event(ev_done[1 - b])    # step i-1's output is final
+            if i >= 1:
+                with torch.cuda.stream(ys):
+                    ys.wait_event(ev_done[1 - b])    # step i-1's output is final
                     out_host[1 - b].copy_(outs[1 - b], non_blocking=True)
+                    ev_out[1 - b].record(ys)
             cs.wait_event(ev_in[b])
+            if i >= 2:
+                cs.wait_event(ev_out[b])             # step i-2's output has been read back
             bind(b)
             step_fn()
             ev_done[b].record(cs)
         b = (k - 1) % 2
         last[0] = b
-        with torch.cuda.stream(xs):
-            xs.wait_event(ev_done[b])
+        with torch.cuda.stream(ys):
+            ys.wait_event(ev_done[b])
             out_host[b].copy_(outs[b], non_blocking=True)
-            join.record(xs)
-        cs.wait_event(join)
+            join_y.record(ys)
+        join_x.record(xs)
+        cs.wait_event(join_x)
+        cs.wait_event(join_y)
 
     return (enqueue, verify, hosts[0].numel(),
             out_host[0].numel() * out_host[0].element_size())
