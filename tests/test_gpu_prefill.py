@@ -359,3 +359,16 @@ def test_context_length_past_the_table_is_cut_to_it():
     want = ref.paged_prefill(bits_of(W.q), "f16", opool, W.block_tables.numpy(), cut.numpy(),
                              W.query_start_loc.numpy(), W.scale, "f16")
     check_close(got, want, "f16", "cut length")
+
+
+def test_e4m3_cache_run_to_run_bitwise_deterministic():
+    # the converters hand staging buffers and ring slots between proxies:
+    # repeated runs at full size must agree bit for bit
+    from paged_kv_cache_296_gb300.runner import PrefillStep
+    W = wl.make_prefill_workload(wl.PREFILL_SPECS[2], 12, device="cuda")
+    S = PrefillStep(W, kv_dtype="e4m3")
+    first = S.step().clone()
+    for _ in range(10):
+        again = S.step()
+        assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+    assert pa.pa_device_status(clear=True) == 0
