@@ -372,3 +372,29 @@ def test_e4m3_cache_run_to_run_bitwise_deterministic():
         again = S.step()
         assert torch.equal(first.view(torch.int16), again.view(torch.int16))
     assert pa.pa_device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_block_permutation_invariance_bitwise(kv):
+    # Paging changes only where K/V live: moving every block to another
+    # physical id (and rewriting the tables and slots to match) leaves every
+    # output bit unchanged.
+    spec = wl.PrefillSpec("permuted", 5, 16, 4, 128, "bf16", ("fixed", [300, 129, 1000, 64, 517]),
+                          ("fixed", [300, 40, 256, 64, 17]), ("factor", 1.4))
+    W = wl.make_prefill_workload(spec, 19)
+
+    def run(pool16, tables, slots):
+        from paged_kv_cache_296_gb300.runner import PrefillStep
+        W.pool, W.block_tables, W.slot_mapping = pool16, tables, slots
+        S = PrefillStep(W, kv_dtype=None if kv == "bf16" else "e4m3")
+        return S.step().cpu()
+
+    pool0, tables0, slots0 = W.pool.clone(), W.block_tables.clone(), W.slot_mapping.clone()
+    a = run(pool0, tables0, slots0)
+    perm = torch.from_numpy(np.random.default_rng(3).permutation(W.num_blocks))  # old id -> new id
+    pool1 = torch.empty_like(pool0)
+    pool1[perm] = pool0
+    tables1 = torch.where(tables0 >= 0, perm[tables0.clamp(min=0).long()].to(torch.int32), tables0)
+    slots1 = perm[slots0 // 16] * 16 + slots0 % 16
+    b = run(pool1, tables1, slots1)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
