@@ -11,9 +11,16 @@ Prints ONE JSON line (rank 0).  ``value`` is attended-KV GB/s of the whole job
 (sum over ranks of sum_i L_i*Hkv*D*2*elt bytes per step / step time, max
 over ranks).  ``roofline`` reports the decode call against the measured HBM
 copy bandwidth.  ``e2e`` repeats the measurement through the public API with
-the step's inputs copied from pinned host memory and the output copied back
-inside the timed region.  ``cpu_baseline`` times the float64 CPU oracle on a
-bounded sample of the same batch.
+every step's inputs copied in from pinned host memory and its output copied
+back inside the timed region (on copy streams that overlap the neighbouring
+steps' kernels, as a serving loop runs).  ``cpu_baseline`` times the float64
+CPU oracle on a bounded sample of the same batch.
+
+Other legs: --prefill N (causal prefill TFLOP/s against the bf16 tensor peak;
+--prefill-kv e4m3 over an E4M3 cache), --prefix-cache (prefix-cached against
+full prefill), --blocks (pa_copy_blocks against the HBM peak and the block
+manager's host step).  --impl reference times the CPU oracle as the
+reference arm, about --ref-seconds of oracle time whatever --steps is.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl reference]
 """
