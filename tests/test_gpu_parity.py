@@ -113,6 +113,65 @@ def test_gather_bit_exact(kv):
                 assert np.array_equal(got, want)
 
 
+def _fp32_rounding_boundaries():
+    """float32 values a few ulps either side of every E4M3 rounding boundary
+    (the midpoints between neighbouring codes, the codes themselves and the
+    saturation edge), both signs, plus random float32 bit patterns (NaNs,
+    infinities and subnormals among them)."""
+    mags = e4m3.decode(np.arange(0x7F, dtype=np.uint8)).astype(np.float64)
+    mids = (mags[:-1] + mags[1:]) / 2
+    edges = np.concatenate([mags, mids, [464.0, 480.0]]).astype(np.float32)
+    pts = [edges]
+    for direction in (np.float32(np.inf), np.float32(-np.inf)):
+        x = edges
+        for _ in range(3):
+            x = np.nextafter(x, direction)
+            pts.append(x)
+    x = np.concatenate(pts)
+    x = np.concatenate([x, -x])
+    rnd = np.random.default_rng(5).integers(0, 1 << 32, 1 << 16, dtype=np.uint64)
+    return np.concatenate([x, rnd.astype(np.uint32).view(np.float32)])
+
+
+@pytest.mark.parametrize("src", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("kv_scale", [1.0, 0.037])
+def test_fp8_write_exhaustive(src, kv_scale):
+    # Every fp16 / bf16 bit pattern (all the write path can see from a 16-bit
+    # source), or float32 around every rounding boundary, through
+    # pa_reshape_and_cache into an E4M3 cache: byte for byte the oracle's
+    # float32 divide then round-to-nearest-even with saturation.  NaN inputs
+    # must give a NaN code; its sign is fixed by neither side.
+    if src == "f32":
+        vals = _fp32_rounding_boundaries()
+        x = torch.from_numpy(vals.copy())
+    else:
+        bits = np.arange(1 << 16, dtype=np.uint16)
+        x = torch.from_numpy(bits.view(np.int16).copy()).view(_torch_dtype(src))
+    hkv, d = 2, 128
+    per_tok = hkv * d
+    n = -(-x.numel() // per_tok)
+    flat = torch.zeros(n * per_tok, dtype=x.dtype)
+    flat[:x.numel()] = x
+    k = flat.view(n, hkv, d)
+    v = flat.flip(0).contiguous().view(n, hkv, d)
+    nb = -(-n // 16)
+    g = torch.Generator().manual_seed(11)
+    pool = torch.randint(0, 256, (nb, 16, 2, hkv, d), generator=g, dtype=torch.uint8)
+    slots = torch.randperm(nb * 16, generator=g)[:n].to(torch.int64)
+
+    dev_pool = pool.cuda()
+    kc, vc = pa.kv_views(dev_pool)
+    pa.pa_reshape_and_cache(k.cuda(), v.cuda(), kc, vc, slots.cuda(), kv_scale=kv_scale)
+    got = H.bits_of(dev_pool.cpu())
+    with np.errstate(over="ignore", invalid="ignore"):
+        want = ref.reshape_and_cache(H.bits_of(pool), H.bits_of(k), H.bits_of(v),
+                                     slots.numpy(), src, "e4m3", kv_scale)
+    nan_w, nan_g = e4m3.is_nan_code(want), e4m3.is_nan_code(got)
+    assert np.array_equal(nan_w, nan_g)
+    bad = np.flatnonzero(got[~nan_w] != want[~nan_w])
+    assert bad.size == 0, f"{bad.size} codes differ, first at {bad[:4]}"
+
+
 def test_fp8_pool_fill_matches_oracle_encoding():
     spec = wl.random_spec(4, head_size=64, group=4, kv_dtype="e4m3", max_len=60)
     W = wl.make_workload(spec, 41, poison=True)
