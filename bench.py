@@ -14,7 +14,10 @@ copy bandwidth.  ``e2e`` repeats the measurement through the public API with
 every step's inputs copied in from pinned host memory and its output copied
 back inside the timed region (on copy streams that overlap the neighbouring
 steps' kernels, as a serving loop runs).  ``cpu_baseline`` times the float64
-CPU oracle on a bounded sample of the same batch.
+CPU oracle on a bounded sample of the same batch.  A workload whose distinct
+bytes per step are under twice the L2 size is timed one step at a time, each
+step after an untimed write of twice the L2 size (the line's config.l2 says
+which); larger ones run back to back.
 
 Other legs: --prefill N (causal prefill TFLOP/s against the bf16 tensor peak;
 --prefill-kv e4m3 over an E4M3 cache), --prefix-cache (prefix-cached against
@@ -156,6 +159,53 @@ def profiled_prefill_traffic(n, fp8=False):
     if not m_src or not m_tr or m_src.group(1) != kernel_source_hash(PREFILL_SOURCES):
         return None
     return float(m_tr.group(1))
+
+
+def l2_plan(device, distinct):
+    """How the timed steps keep L2 from serving one step's inputs to the next.
+
+    ``distinct`` is the bytes one step reads or writes, each byte counted once.
+    At twice the L2 size or more, a step has evicted most of what the step
+    before it left in L2, so steps run back to back; below that, every timed
+    step is preceded by an untimed write of twice the L2 size and timed by its
+    own events.  Returns (flush buffer or None, the line's "l2" text)."""
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 10 ** 6)
+    if distinct >= 2 * l2:
+        return None, (f"inputs larger than L2: {distinct / 1e6:.0f} MB of distinct bytes per "
+                      f"step (L2 {l2 / 1e6:.0f} MB), no flush")
+    buf = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    return buf, (f"L2 flushed before every timed step by an untimed {2 * l2 / 1e6:.0f} MB write "
+                 f"({distinct / 1e6:.1f} MB of distinct bytes per step, L2 {l2 / 1e6:.0f} MB); "
+                 f"each step timed by its own CUDA events")
+
+
+def time_each(run_one, n, flush_buf, stream):
+    """Mean device ms of n steps, each run after a write of ``flush_buf``
+    (larger than L2) and bracketed by its own events on ``stream``."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for i in range(n):
+        flush_buf.fill_(i & 0x7F)
+        ev[i][0].record(stream)
+        run_one()
+        ev[i][1].record(stream)
+    stream.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def one_step_runner(fn, device, graphs, no_graph):
+    """``fn`` as one replay of a CUDA graph of a single step (or a plain call)."""
+    if no_graph:
+        return fn
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize(device)
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()  # one untimed replay
+    torch.cuda.synchronize(device)
+    graphs.append(g)
+    return g.replay
 
 
 def pipelined_e2e(S, step_fn, device):
@@ -404,6 +454,7 @@ def run_ours(args, world, rank, local):
         step_fn()
     torch.cuda.synchronize(device)
     pa.pa_device_status(clear=True)
+    flush_buf, l2_text = l2_plan(device, unique_kv_bytes(W) + (total_bytes - kv_bytes) + new_bytes)
 
     def steps_per_graph(n):
         return max(d for d in range(1, min(n, 20) + 1) if n % d == 0)
@@ -437,10 +488,20 @@ def run_ours(args, world, rank, local):
     graphs = []  # kept alive until the end of the run
 
     def timed(path, n):
-        """Time n steps of `path`: CUDA events only at the ends of the region
-        (an event between kernels would cost time and break their
-        programmatic-launch overlap).  Returns (ms per step, t0, t1)."""
+        """Time n steps of `path`.  With inputs of twice the L2 size or more,
+        CUDA events only at the ends of the region (an event between kernels
+        would cost time and break their programmatic-launch overlap); with
+        smaller ones, each step after an L2 flush, between its own events.
+        Returns (ms per step, t0, t1)."""
         fn = S.append if path == "append" else S.step
+        if flush_buf is not None:
+            one = one_step_runner(fn, device, graphs, args.no_graph)
+            barrier(world)
+            torch.cuda.synchronize(device)
+            t0 = time.time()
+            ms = time_each(one, n, flush_buf, stream)
+            barrier(world)
+            return ms, t0, time.time()
         run = make_runner(fn, n)
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
@@ -460,6 +521,8 @@ def run_ours(args, world, rank, local):
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
         torch.cuda.synchronize(device)
         for i in range(n):
+            if flush_buf is not None:
+                flush_buf.fill_(i & 0x7F)
             ev[i][0].record(stream)
             S.write()
             ev[i][1].record(stream)
@@ -510,7 +573,12 @@ def run_ours(args, world, rank, local):
         enqueue, verify, h2d, d2h = pipelined_e2e(S, step_fn, device)
         enqueue(max(2, args.warmup))
         torch.cuda.synchronize(device)
-        if args.no_graph:
+        if flush_buf is not None:
+            # one step at a time after each flush: its copies in and out are
+            # inside its events, with no overlap from a neighbouring step
+            one = one_step_runner(lambda: enqueue(1), device, graphs, args.no_graph)
+            run_e2e = None
+        elif args.no_graph:
             def run_e2e():
                 enqueue(n)
         else:
@@ -527,13 +595,17 @@ def run_ours(args, world, rank, local):
                     ge.replay()
         s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
-        s2.record(stream)
-        run_e2e()
-        e2.record(stream)
-        torch.cuda.synchronize(device)
+        if run_e2e is None:
+            e_local = time_each(one, n, flush_buf, stream)
+        else:
+            s2.record(stream)
+            run_e2e()
+            e2.record(stream)
+            torch.cuda.synchronize(device)
+            e_local = s2.elapsed_time(e2) / n
         barrier(world)
         verify()
-        e2e_ms = max_over_ranks(s2.elapsed_time(e2) / n, world, device)
+        e2e_ms = max_over_ranks(e_local, world, device)
         e2e_gbs = sum_over_ranks(kv_bytes, world, device) / (e2e_ms * 1e-3) / 1e9
         e2e = {"value": round(e2e_gbs, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
@@ -575,9 +647,10 @@ def run_ours(args, world, rank, local):
         "config": config_block(spec, W, {
             "step": args.path,
             "launch": "stream" if args.no_graph else
+                      "CUDA graph replay, 1 step per graph" if flush_buf is not None else
                       f"CUDA graph replay, {steps_per_graph(n)} steps per graph",
             "partition_tokens": S.partition_tokens,
-            "l2": f"inputs larger than L2: {kv_bytes / 1e9:.3f} GB of KV read per step, no flush",
+            "l2": l2_text,
             "parallelism": f"replicas{world}" if world > 1 else "single GPU"}),
         "roofline": {"bound": "hbm", "kernel": kernel,
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -667,6 +740,13 @@ def run_prefill(args, world, rank, local):
     pa.pa_device_status(clear=True)
     n = args.steps
     graphs = []
+    # distinct bytes per step: the context K/V in the cache, q, out and the
+    # query tokens' K/V sources
+    kv_elt = S.pool.element_size()
+    distinct = (int(W.context_lens.to(torch.int64).sum()) * spec.num_kv_heads * spec.head_size
+                * 2 * kv_elt + 2 * S.q.numel() * S.q.element_size()
+                + 2 * S.k_new.numel() * S.k_new.element_size())
+    flush_buf, l2_text = l2_plan(device, distinct)
 
     def runner(fn):
         if args.no_graph:
@@ -701,27 +781,45 @@ def run_prefill(args, world, rank, local):
         barrier(world)
         return a.elapsed_time(b) / n, t0, time.time()
 
-    run, launch = runner(S.step)
+    if flush_buf is not None:
+        one = one_step_runner(S.step, device, graphs, args.no_graph)
+        launch = "stream" if args.no_graph else "CUDA graph replay, 1 step per graph"
+    else:
+        run, launch = runner(S.step)
     sampler = ClockSampler(device.index)
     sampler.start()
     time.sleep(0.3)
-    ms_local, t0, t1 = timed(run)
+    if flush_buf is not None:
+        barrier(world)
+        torch.cuda.synchronize(device)
+        t0 = time.time()
+        ms_local = time_each(one, n, flush_buf, stream)
+        barrier(world)
+        t1 = time.time()
+    else:
+        ms_local, t0, t1 = timed(run)
     sampler.stop()
     ms_step = max_over_ranks(ms_local, world, device)
     status = pa.pa_device_status(clear=True)
     if status != 0:
         raise RuntimeError(f"device status {status:#x}")
     # the attention kernel alone (the write is a small share of the step)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    S.step()
-    torch.cuda.synchronize(device)
-    ev[0].record(stream)
-    for _ in range(min(n, 50)):
+    def attention_call():
         pa.pa_prefill(S.out, S.q, S.k_cache, S.v_cache, S.block_tables, S.context_lens,
                       S.query_start_loc, S.max_query_len, S.scale, kv_scale=S.kv_scale)
-    ev[1].record(stream)
+
+    S.step()
     torch.cuda.synchronize(device)
-    attn_ms = ev[0].elapsed_time(ev[1]) / min(n, 50)
+    if flush_buf is not None:
+        attn_ms = time_each(attention_call, min(n, 50), flush_buf, stream)
+    else:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record(stream)
+        for _ in range(min(n, 50)):
+            attention_call()
+        ev[1].record(stream)
+        torch.cuda.synchronize(device)
+        attn_ms = ev[0].elapsed_time(ev[1]) / min(n, 50)
 
     e2e = None
     if not args.no_e2e:
@@ -730,22 +828,29 @@ def run_prefill(args, world, rank, local):
         enqueue, verify, h2d, d2h = pipelined_e2e(S, S.step, device)
         enqueue(max(2, args.warmup))
         torch.cuda.synchronize(device)
-        if args.no_graph:
-            def run_e2e():
-                enqueue(n)
+        if flush_buf is not None:
+            # one step at a time after each flush, its copies inside its events
+            one_e2e = one_step_runner(lambda: enqueue(1), device, graphs, args.no_graph)
+            barrier(world)
+            e_ms = time_each(one_e2e, n, flush_buf, stream)
+            barrier(world)
         else:
-            spg = max(d for d in range(1, min(n, 20) + 1) if n % d == 0)
-            ge = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(ge):
-                enqueue(spg)
-            ge.replay()
-            torch.cuda.synchronize(device)
-            graphs.append(ge)
+            if args.no_graph:
+                def run_e2e():
+                    enqueue(n)
+            else:
+                spg = max(d for d in range(1, min(n, 20) + 1) if n % d == 0)
+                ge = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(ge):
+                    enqueue(spg)
+                ge.replay()
+                torch.cuda.synchronize(device)
+                graphs.append(ge)
 
-            def run_e2e():
-                for _ in range(n // spg):
-                    ge.replay()
-        e_ms, _, _ = timed(run_e2e)
+                def run_e2e():
+                    for _ in range(n // spg):
+                        ge.replay()
+            e_ms, _, _ = timed(run_e2e)
         verify()
         e_ms = max_over_ranks(e_ms, world, device)
         e2e = {"value": round(sum_over_ranks(flops, world, device) / (e_ms * 1e-3) / 1e12, 2),
@@ -776,7 +881,8 @@ def run_prefill(args, world, rank, local):
                    "mean_context": float(W.context_lens.float().mean()),
                    "kv_dtype": "e4m3" if fp8 else spec.dtype,
                    "step": "pa_reshape_and_cache of the query tokens + pa_prefill",
-                   "launch": launch, "l2": "K/V re-read by a sequence's tiles comes from L2",
+                   "launch": launch,
+                   "l2": l2_text + "; within a step, K/V re-read by a sequence's tiles comes from L2",
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "kernel": "paged_prefill_tc_kernel (tcgen05, S/P/O in TMEM)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
@@ -945,6 +1051,12 @@ def run_prefix_cache(args, world, rank, local):
     spg = max(k for k in range(1, min(n, 20) + 1) if n % k == 0)
     results = {}
     graphs = []
+    # one L2 plan for both modes, from the cached step's distinct bytes (the
+    # smaller): the prompt's K/V once, the user tokens' K/V, q, out and the
+    # user tokens' K/V sources, all bf16
+    t_c = B * user_len
+    flush_buf, l2_text = l2_plan(device, ((sys_len + t_c) * hkv * d * 2 + 2 * t_c * hq * d
+                                          + 2 * t_c * hkv * d) * 2)
     sampler = ClockSampler(device.index)
     sampler.start()
     time.sleep(0.3)
@@ -954,6 +1066,13 @@ def run_prefix_cache(args, world, rank, local):
         for _ in range(args.warmup):
             step(st)
         torch.cuda.synchronize(device)
+        if flush_buf is not None:
+            one = one_step_runner(lambda st=st: step(st), device, graphs, args.no_graph)
+            barrier(world)
+            ms = time_each(one, n, flush_buf, stream)
+            barrier(world)
+            results[mode] = (max_over_ranks(ms, world, device), st)
+            continue
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr):
             for _ in range(spg):
@@ -987,7 +1106,10 @@ def run_prefix_cache(args, world, rank, local):
         "config": {"workload": f"{B} requests: the same {sys_len}-token system prompt + "
                                f"{user_len} own tokens, 32/8 heads, d128, bf16",
                    "step": "pa_reshape_and_cache of the uncached tokens + pa_prefill of them",
-                   "launch": f"CUDA graph replay, {spg} steps per graph",
+                   "launch": f"CUDA graph replay, {spg} steps per graph" if flush_buf is None
+                             else "stream" if args.no_graph else
+                             "CUDA graph replay, 1 step per graph",
+                   "l2": l2_text,
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
         "pages_context": "the pages quote 4x end-to-end for this scenario (180 ms -> 45 ms, "
                          "serving latency, hardware unstated); this is the attention step alone",
