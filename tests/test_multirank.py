@@ -97,3 +97,19 @@ def test_reference_arm_other_ranks_exit_quietly():
 def test_bench_rejects_short_warmup():
     r = _run_bench(["--impl", "reference", "--warmup", "2"], {})
     assert r.returncode != 0
+
+
+def test_l2_plan_flushes_only_below_twice_l2(monkeypatch):
+    # A step whose distinct bytes are under twice the L2 size gets a flush
+    # buffer of twice the L2 size; at or above it, none.
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class Props:
+        L2_cache_size = 1000
+
+    monkeypatch.setattr(bench.torch.cuda, "get_device_properties", lambda device: Props())
+    buf, text = bench.l2_plan("cpu", 1999)
+    assert buf is not None and buf.numel() == 2000 and "flushed" in text
+    buf, text = bench.l2_plan("cpu", 2000)
+    assert buf is None and "no flush" in text
