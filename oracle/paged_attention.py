@@ -206,31 +206,6 @@ def paged_decode(q_bits, q_dtype, pool, block_tables, context_lens, scale,
     return out
 
 
-def paged_decode_heads(q_bits, q_dtype, pool, block_tables, context_lens, scale,
-                       kv_dtype, kv_scale, pairs):
-    """``paged_decode`` for selected (sequence, query head) pairs only.
-
-    Returns float64 ``[len(pairs), D]``.  Used to check sampled outputs of
-    full-size batches one by one.
-    """
-    block_size = pool.shape[1]
-    hkv = pool.shape[3]
-    out = np.zeros((len(pairs), q_bits.shape[-1]), dtype=np.float64)
-    for n, (i, h) in enumerate(pairs):
-        g = q_bits.shape[1] // hkv
-        L = int(context_lens[i])
-        if L == 0:
-            continue
-        kb, vb = gather_kv(pool, block_tables[i], L, block_size)
-        k = kv_values(kb[:, h // g], kv_dtype, kv_scale)        # [L, D]
-        v = kv_values(vb[:, h // g], kv_dtype, kv_scale)
-        q = widen(q_bits[i, h], q_dtype)
-        s = scale * (k @ q)
-        p = np.exp(s - s.max())
-        out[n] = (p / p.sum()) @ v
-    return out
-
-
 # --------------------------------------------------------------------------
 # Prefill / chunked prefill over the paged cache
 # --------------------------------------------------------------------------

@@ -332,3 +332,51 @@ def test_fp8_decode_uses_dequantised_cache():
     kv = ref.fp8_dequantise(codes, scale)
     want = ref.attention_contiguous(ref.widen(q[0], "f16"), kv, kv, 0.3)
     np.testing.assert_allclose(got[0], want, rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------- small helpers
+
+def test_slot_to_block_offset_fills_each_block_in_order():
+    # Walking the flat slots in order with a counter (no division) must fill
+    # offsets 0..BS-1 of block 0, then of block 1, and so on: the pages'
+    # tokens-fill-a-block-then-spill rule.
+    for bs in (4, 16):
+        blk, off = 0, 0
+        for slot in range(7 * bs + 3):
+            assert ref.slot_to_block_offset(slot, bs) == (blk, off)
+            off += 1
+            if off == bs:
+                blk, off = blk + 1, 0
+
+
+def test_kv_values_match_torch_casts():
+    # 16-bit caches: every bit pattern widens exactly as PyTorch widens it.
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    for name, dt in (("f16", torch.float16), ("bf16", torch.bfloat16)):
+        want = torch.from_numpy(bits.view(np.int16).copy()).view(dt).to(torch.float64).numpy()
+        with np.errstate(invalid="ignore"):   # the NaN patterns
+            got = ref.kv_values(bits, name, 1.0)
+        same = (got == want) | (np.isnan(got) & np.isnan(want))
+        assert same.all(), name
+    # E4M3 cache: every code decoded by PyTorch's float8_e4m3fn, times float32(kv_scale).
+    codes = np.arange(256, dtype=np.uint8)
+    kv_scale = 0.0371
+    dec = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    want = dec * np.float64(np.float32(kv_scale))
+    got = ref.kv_values(codes, "e4m3", kv_scale)
+    finite = np.isfinite(want)
+    assert np.array_equal(got[finite], want[finite])
+    assert np.isnan(got[~finite]).all()
+
+
+def test_narrow_f32_rounds_like_torch():
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.standard_normal(100000) * 10.0 ** rng.integers(-40, 39, 100000),
+                        # exact ties between neighbouring float32 values, both ways
+                        (np.float64(1.0) + np.arange(1, 1001) * 2.0 ** -23) + 2.0 ** -24,
+                        [0.0, -0.0, np.inf, -np.inf, 3.5e38, 1e-46, -1e-46]])
+    want = torch.from_numpy(x).to(torch.float32).numpy()
+    with np.errstate(over="ignore"):          # 3.5e38 rounds to inf
+        got = ref.narrow_f32(x)
+    assert got.dtype == np.float32
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
