@@ -5,8 +5,6 @@ The GPU side calls the C ABI through the Python binding; the oracle side takes
 the CPU copies of the inputs, never a value the GPU produced.
 """
 
-import math
-
 import numpy as np
 import torch
 
@@ -137,7 +135,7 @@ def widen_out(t, dtype):
     return ref.widen(bits_of(t.cpu()), dtype)
 
 
-def tolerance(spec, ref_out, contexts=None):
+def tolerance(spec, ref_out):
     """Per-element bound: the stated tolerance for the cache dtype, widened by
     one output ulp of |ref| where that exceeds it (only large outputs of tiny
     contexts reach that)."""
@@ -157,6 +155,3 @@ def assert_close(got, want, spec, what=""):
             f"{np.nanmax(err):.3e}; first at {idx.tolist()} got {got[bad][:5]} want {want[bad][:5]}")
     return float(err.max()) if err.size else 0.0
 
-
-def scale_for(head_size):
-    return 1.0 / math.sqrt(head_size)
