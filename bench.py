@@ -614,7 +614,8 @@ def run_ours(args, world, rank, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         b, secs, nseq = OracleSampler(W, oracle_rows_fn(W)).sample(args.cpu_seconds)
-        cpu = {"value": round(b / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        cpu = {"value": round(b / secs / 1e9, 4), "unit": "GB/s", "cores": 1,
+               "host_cpus": os.cpu_count(), "kind": "oracle",
                "sample": f"float64 NumPy oracle, {nseq} sequences of this batch (all heads; a "
                          f"sequence cut to fewer tokens only if the time budget ends inside it), "
                          f"{secs:.1f} s, 1 BLAS thread"}
@@ -861,6 +862,7 @@ def run_prefill(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         f, secs, rows = PrefillOracleSampler(W).sample(args.cpu_seconds)
         cpu = {"value": round(f / secs / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+               "host_cpus": os.cpu_count(),
                "kind": "oracle",
                "sample": f"float64 NumPy oracle, {rows} query rows (all heads) of this batch, "
                          f"{secs:.1f} s, 1 BLAS thread"
@@ -1138,7 +1140,8 @@ def run_reference_prefill(args, world, rank, local):
         f, sec, r = sampler.sample(per_step)
         tot_f, tot_s, rows = tot_f + f, tot_s + sec, rows + r
     value = tot_f / tot_s / 1e12
-    cpu = {"value": round(value, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+    cpu = {"value": round(value, 6), "unit": "TFLOP/s", "cores": 1, "host_cpus": os.cpu_count(),
+           "kind": "oracle",
            "sample": f"float64 NumPy oracle, {rows} query rows over {args.steps} steps "
                      f"({tot_s:.1f} s), 1 BLAS thread"}
     print(json.dumps({
@@ -1171,7 +1174,8 @@ def run_reference(args, world, rank, local):
         tot_s += s
         nseq += k
     value = tot_b / tot_s / 1e9
-    cpu = {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    cpu = {"value": round(value, 4), "unit": "GB/s", "cores": 1, "host_cpus": os.cpu_count(),
+           "kind": "oracle",
            "sample": f"float64 NumPy oracle, {nseq} sequence samples (all heads, contexts cut to "
                      f"the per-step time budget) over {args.steps} steps "
                      f"({tot_s:.1f} s), 1 BLAS thread"}
