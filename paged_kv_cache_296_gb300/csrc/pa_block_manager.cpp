@@ -31,7 +31,6 @@
 #include <new>
 #include <string>
 #include <unordered_map>
-#include <unordered_set>
 #include <vector>
 
 #include "../../include/pa.h"
@@ -72,6 +71,7 @@ struct pa_block_manager {
   struct Seq {
     std::vector<int32_t> blocks;
     int64_t len = 0;
+    uint64_t batch = 0;  // the last append batch that named this sequence
   };
   int32_t num_blocks = 0;
   int32_t block_size = 16;
@@ -86,6 +86,8 @@ struct pa_block_manager {
   std::vector<CacheKey> key_of;                    // a cached block's key
   std::vector<uint8_t> cached;
   std::unordered_map<int64_t, Seq> seqs;
+  uint64_t batch_no = 0;       // append batches so far
+  std::vector<Seq*> scratch;   // the sequences of the call in progress
   std::mutex mu;
 
   int64_t blocks_for(int64_t tokens) const { return (tokens + block_size - 1) / block_size; }
@@ -256,13 +258,17 @@ pa_status pa_bm_append_batch(pa_block_manager* bm, const int64_t* seq_ids, const
   // drops while counting.
   int64_t total_blocks = 0, total_slots = 0;
   bool any_cow = false;
-  std::unordered_set<int64_t> seen;
   std::unordered_map<int32_t, int32_t> dropped;  // block -> copies-on-write so far
+  // Each sequence is looked up once; a stamp per batch finds an id named twice.
+  const uint64_t stamp = ++bm->batch_no;
+  bm->scratch.clear();
   for (int32_t i = 0; i < n_seqs; ++i) {
     auto it = bm->seqs.find(seq_ids[i]);
     if (it == bm->seqs.end()) return bm_fail(PA_ERR_INVALID_ARG, "unknown sequence id");
-    if (!seen.insert(seq_ids[i]).second)
+    if (it->second.batch == stamp)
       return bm_fail(PA_ERR_INVALID_ARG, "a sequence id appears twice in one batch");
+    it->second.batch = stamp;
+    bm->scratch.push_back(&it->second);
     if (counts[i] < 0) return bm_fail(PA_ERR_INVALID_ARG, "negative token count");
     const auto& sq = it->second;
     const int64_t L = sq.len;
@@ -284,8 +290,8 @@ pa_status pa_bm_append_batch(pa_block_manager* bm, const int64_t* seq_ids, const
   *n_copies_out = 0;
   int64_t off = 0;
   for (int32_t i = 0; i < n_seqs; ++i) {
-    auto& s = bm->seqs[seq_ids[i]];
-    bm->append_apply(s, counts[i], slots_out + off, copies_out, n_copies_out);
+    bm->append_apply(*bm->scratch[(size_t)i], counts[i], slots_out + off, copies_out,
+                     n_copies_out);
     off += counts[i];
   }
   return bm_ok();
@@ -364,18 +370,20 @@ pa_status pa_bm_block_tables(pa_block_manager* bm, const int64_t* seq_ids, int32
   if (!bm || n_seqs < 0 || width < 0 || (n_seqs > 0 && (!seq_ids || !tables_out || !lens_out)))
     return bm_fail(PA_ERR_INVALID_ARG, "bad manager, size or null pointer");
   std::lock_guard<std::mutex> g(bm->mu);
+  bm->scratch.clear();
   for (int32_t i = 0; i < n_seqs; ++i) {
     auto it = bm->seqs.find(seq_ids[i]);
     if (it == bm->seqs.end()) return bm_fail(PA_ERR_INVALID_ARG, "unknown sequence id");
     if ((int64_t)it->second.blocks.size() > width)
       return bm_fail(PA_ERR_INVALID_ARG, "a block table is wider than width");
     if (it->second.len > 0x7FFFFFFFll) return bm_fail(PA_ERR_UNSUPPORTED, "sequence too long");
+    bm->scratch.push_back(&it->second);
   }
   for (int32_t i = 0; i < n_seqs; ++i) {
-    const auto& s = bm->seqs[seq_ids[i]];
+    const auto& s = *bm->scratch[(size_t)i];
     int32_t* row = tables_out + (size_t)i * (size_t)width;
-    for (int32_t j = 0; j < width; ++j)
-      row[j] = j < (int32_t)s.blocks.size() ? s.blocks[(size_t)j] : -1;
+    std::copy(s.blocks.begin(), s.blocks.end(), row);
+    std::fill(row + s.blocks.size(), row + width, -1);
     lens_out[i] = (int32_t)s.len;
   }
   return bm_ok();

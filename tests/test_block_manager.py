@@ -116,6 +116,26 @@ def test_errors_change_nothing(lib):
     assert t.tolist() == [[0, 1, 2]] and lens.tolist() == [40]
 
 
+def test_a_failed_batch_leaves_its_ids_usable(lib):
+    # A batch that fails after naming some sequences (here: an unknown id
+    # last) changes nothing, and the same sequences append normally next;
+    # a forked child and its parent may appear in one batch.
+    bm = pa.BlockManager(16)
+    bm.allocate(1, 10)
+    bm.allocate(2, 20)
+    with pytest.raises(pa.PagedAttentionError):
+        bm.append_batch([1, 2, 9], [1, 1, 1])
+    assert bm.block_tables([1, 2], 2)[1].tolist() == [10, 20]
+    slots, copies = bm.append_batch([1, 2], [1, 1])
+    assert slots == [10, 2 * 16 + 4] and copies == []   # seq 2 holds blocks 1 and 2
+    bm.fork(1, 3)
+    slots, copies = bm.append_batch([3, 1], [1, 1])
+    assert copies == [(0, 3)]                # the child copies the shared partial block
+    assert slots == [3 * 16 + 11, 11]         # and the parent keeps block 0
+    with pytest.raises(pa.PagedAttentionError):
+        bm.append_batch([2, 3, 2], [1, 1, 1])
+
+
 def test_batch_that_does_not_fit_changes_nothing(lib):
     bm = pa.BlockManager(6)
     bm.allocate(1, 16)
