@@ -223,3 +223,22 @@ def test_prefill_rejects_bad_arguments(lib, over, status):
 def test_prefill_without_queries_is_a_no_op(lib):
     assert lib.pa_prefill(*prefill_args(mq=0, out=NULL, q=NULL)) == 0
     assert lib.pa_prefill(*prefill_args(B=0, out=NULL, q=NULL)) == 0
+
+
+def test_a_plain_c_program_uses_the_library(lib, tmp_path):
+    # The header is valid C99 and the shared library links into a C program
+    # that runs the host-only calls (tests/c_consumer.c states its checks).
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(pa.LIB_PATH)
+    exe = str(tmp_path / "c_consumer")
+    subprocess.run([cc, "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror",
+                    "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c_consumer.c"), "-o", exe,
+                    "-L", libdir, "-lpagedattn", f"-Wl,-rpath,{libdir}"], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == "ok"
