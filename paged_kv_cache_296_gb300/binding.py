@@ -403,17 +403,33 @@ class BlockManager:
     def free(self, seq_id):
         self._check("pa_bm_free", self._lib.pa_bm_free(self._h, int(seq_id)))
 
-    def block_tables(self, seq_ids, width):
-        """int32 tensors (tables [n, width] padded with -1, lengths [n]) on the CPU."""
+    def block_tables(self, seq_ids, width, out=None):
+        """int32 tensors (tables [n, width] padded with -1, lengths [n]) on the CPU.
+
+        ``out``: (tables, lens) to write instead of new tensors, e.g. pinned
+        buffers a serving loop copies to the GPU each step; contiguous int32
+        CPU tensors of at least [n, width] and [n] elements (rows beyond n are
+        left as they are).
+        """
         ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
         n = ids.shape[0]
-        tables = torch.empty((n, width), dtype=torch.int32)
-        lens = torch.empty((n,), dtype=torch.int32)
+        if out is None:
+            tables = torch.empty((n, width), dtype=torch.int32)
+            lens = torch.empty((n,), dtype=torch.int32)
+        else:
+            tables, lens = out
+            for t, need in ((tables, n * width), (lens, n)):
+                if (t.dtype != torch.int32 or t.device.type != "cpu" or not t.is_contiguous()
+                        or t.numel() < need):
+                    raise ValueError("out must be contiguous int32 CPU tensors large enough "
+                                     "for [n, width] and [n]")
+            if tables.dim() != 2 or tables.shape[1] != width:
+                raise ValueError("out tables must be [rows, width]")
         st = self._lib.pa_bm_block_tables(self._h, ids.ctypes.data, n, int(width),
                                           ctypes.c_void_p(tables.data_ptr()),
                                           ctypes.c_void_p(lens.data_ptr()))
         self._check("pa_bm_block_tables", st)
-        return tables, lens
+        return tables[:n], lens[:n]
 
 
 def pa_copy_blocks(pool, pairs):

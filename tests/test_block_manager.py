@@ -8,6 +8,7 @@ free-block counts, reference counts and which requests run out of blocks.
 import random
 
 import pytest
+import torch
 
 from oracle.block_manager import BlockManager as RefManager, OutOfBlocks as RefOOM
 from paged_kv_cache_296_gb300 import binding as pa
@@ -217,3 +218,24 @@ def test_native_prefix_caching_matches_the_oracle(lib, seed):
             ref.free_seq(s)
             bm.free(s)
         _same_state(bm, ref)
+
+
+def test_block_tables_into_caller_buffers(lib):
+    # The export can fill preallocated tensors (a serving loop's pinned
+    # buffers): the same tables as a fresh export, rows past n untouched.
+    bm = pa.BlockManager(32)
+    for s, n in ((1, 40), (2, 5), (3, 33)):
+        bm.allocate(s, n)
+    want_t, want_l = bm.block_tables([3, 1, 2], 4)
+    tables = torch.full((5, 4), 77, dtype=torch.int32)
+    lens = torch.full((5,), 77, dtype=torch.int32)
+    got_t, got_l = bm.block_tables([3, 1, 2], 4, out=(tables, lens))
+    assert torch.equal(got_t, want_t) and torch.equal(got_l, want_l)
+    assert got_t.data_ptr() == tables.data_ptr()
+    assert (tables[3:] == 77).all() and (lens[3:] == 77).all()
+    with pytest.raises(ValueError):
+        bm.block_tables([1], 4, out=(tables.to(torch.int64), lens))
+    with pytest.raises(ValueError):
+        bm.block_tables([1], 4, out=(torch.zeros((5, 3), dtype=torch.int32), lens))
+    with pytest.raises(ValueError):
+        bm.block_tables([1, 2, 3], 4, out=(tables[:2], lens))
