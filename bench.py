@@ -1,4 +1,4 @@
-"""Benchmark of the paged-KV-cache decode hot path on one GB300 (or N replicas).
+"""Benchmark of the paged-KV-cache decode hot path on one GB300 (or N GPUs).
 
 One step = the write of each sequence's new token into the paged pool plus
 decode attention over every sequence, on a seeded synthetic batch whose KV
@@ -6,6 +6,11 @@ cache is already resident in HBM.  By default the step is pa_decode_append
 (write, attention and split-KV merge in one launch); --path separate times
 pa_reshape_and_cache followed by pa_decode.  The other path is timed after
 the headline loop and reported under "other_path".
+
+The headline workload is --config (default 3, the Llama-3-8B GQA batch); the
+--also workloads (default 5, 4, 2: long-context E4M3, shared-prefix sampling,
+Llama-2-7B MHA) are timed in the same process by the same rules and reported
+under "also", each with its own roofline block and clock record.
 
 Prints ONE JSON line (rank 0).  ``value`` is attended-KV GB/s of the whole job
 (sum over ranks of sum_i L_i*Hkv*D*2*elt bytes per step / step time, max
@@ -17,7 +22,13 @@ steps' kernels, as a serving loop runs).  ``cpu_baseline`` times the float64
 CPU oracle on a bounded sample of the same batch.  A workload whose distinct
 bytes per step are under twice the L2 size is timed one step at a time, each
 step after an untimed write of twice the L2 size (the line's config.l2 says
-which); larger ones run back to back.
+which); larger ones run back to back.  ``config`` names the workload only and
+is the same on both arms; how the steps were launched is under ``run``.
+
+N > 1 (torchrun, one rank per GPU): --shard seqs (default) gives every GPU its
+own batch (replicas, weak scaling); --shard heads splits the KV heads of one
+batch over the GPUs, each rank decoding its heads with no collective in
+attention (strong scaling).
 
 Other legs: --prefill N (causal prefill TFLOP/s against the bf16 tensor peak;
 --prefill-kv e4m3 over an E4M3 cache), --prefix-cache (prefix-cached against
@@ -25,7 +36,8 @@ full prefill), --blocks (pa_copy_blocks against the HBM peak and the block
 manager's host step).  --impl reference times the CPU oracle as the
 reference arm, about --ref-seconds of oracle time whatever --steps is.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 3] [--also 5,4,2]
+                    [--shard seqs|heads] [--impl reference]
 """
 
 import argparse
@@ -169,15 +181,10 @@ def l2_plan(device, distinct):
     before it left in L2, so steps run back to back; below that, every timed
     step is preceded by an untimed write of twice the L2 size and timed by its
     own events.  Returns (flush buffer or None, the line's "l2" text)."""
-    props = torch.cuda.get_device_properties(device)
-    l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 10 ** 6)
+    l2 = device_l2_bytes(device)
     if distinct >= 2 * l2:
-        return None, (f"inputs larger than L2: {distinct / 1e6:.0f} MB of distinct bytes per "
-                      f"step (L2 {l2 / 1e6:.0f} MB), no flush")
-    buf = torch.empty(2 * l2, dtype=torch.uint8, device=device)
-    return buf, (f"L2 flushed before every timed step by an untimed {2 * l2 / 1e6:.0f} MB write "
-                 f"({distinct / 1e6:.1f} MB of distinct bytes per step, L2 {l2 / 1e6:.0f} MB); "
-                 f"each step timed by its own CUDA events")
+        return None, l2_text(distinct, l2)
+    return torch.empty(2 * l2, dtype=torch.uint8, device=device), l2_text(distinct, l2)
 
 
 def time_each(run_one, n, flush_buf, stream):
@@ -425,36 +432,85 @@ def oracle_rows_fn(W):
 
 # ---------------------------------------------------------------- main legs
 
-def config_block(spec, W, extra):
-    c = {"workload": spec.name, "num_seqs": spec.num_seqs, "num_q_heads": spec.num_q_heads,
-         "num_kv_heads": spec.num_kv_heads, "head_size": spec.head_size, "block_size": 16,
-         "q_dtype": spec.q_dtype, "kv_dtype": spec.kv_dtype,
-         "mean_context": float(W.context_lens.float().mean()),
-         "num_blocks": W.num_blocks, "seed": W.seed}
-    c.update(extra)
-    return c
+def parallelism(world, shard):
+    """How the job is spread over GPUs, the same words on both arms."""
+    if world <= 1:
+        return "one device"
+    if shard == "heads":
+        return f"kv heads sharded over {world} GPUs (no collective in attention)"
+    return f"replicas{world}"
 
 
-def run_ours(args, world, rank, local):
+def l2_text(distinct, l2_bytes):
+    """The line's config.l2: which L2 rule the timed steps follow (see l2_plan)."""
+    if distinct >= 2 * l2_bytes:
+        return (f"inputs larger than L2: {distinct / 1e6:.0f} MB of distinct bytes per "
+                f"step (L2 {l2_bytes / 1e6:.0f} MB), no flush")
+    return (f"L2 flushed before every timed step by an untimed {2 * l2_bytes / 1e6:.0f} MB write "
+            f"({distinct / 1e6:.1f} MB of distinct bytes per step, L2 {l2_bytes / 1e6:.0f} MB); "
+            f"each step timed by its own CUDA events")
+
+
+def device_l2_bytes(device=None):
+    """L2 size of ``device`` (of GPU 0 if None; the nominal 129 MB where no GPU is visible)."""
+    if device is None and not torch.cuda.is_available():
+        return 129 * 10 ** 6
+    props = torch.cuda.get_device_properties(device if device is not None else 0)
+    return int(getattr(props, "L2_cache_size", 0) or 129 * 10 ** 6)
+
+
+def decode_distinct_bytes(W):
+    """Bytes one decode step reads or writes, each counted once (shared blocks once)."""
+    from paged_kv_cache_296_gb300.runner import step_bytes, unique_kv_bytes
+    total_bytes, kv_bytes, new_bytes = step_bytes(W)
+    return unique_kv_bytes(W) + (total_bytes - kv_bytes) + new_bytes
+
+
+def workload_config(spec, W, l2, world, shard):
+    """The line's ``config``: the workload and the L2 rule only, identical on both
+    arms for the same workload and seed (timing details go under ``run``)."""
+    return {"workload": spec.name, "num_seqs": spec.num_seqs, "num_q_heads": spec.num_q_heads,
+            "num_kv_heads": spec.num_kv_heads, "head_size": spec.head_size, "block_size": 16,
+            "q_dtype": spec.q_dtype, "kv_dtype": spec.kv_dtype,
+            "mean_context": float(W.context_lens.float().mean()),
+            "num_blocks": W.num_blocks, "seed": W.seed, "l2": l2,
+            "parallelism": parallelism(world, shard)}
+
+
+def rank_workload(args, config_id, world, rank, device):
+    """This rank's decode workload: its own batch (replicas, seed + 1000 * rank),
+    or its slice of KV heads of the one shared batch (--shard heads).
+    Returns (the whole workload this rank's slice comes from, the slice)."""
+    spec = wl.SPECS[config_id]
+    if args.shard == "heads" and world > 1:
+        W = wl.make_workload(spec, config_id, device=str(device))
+        return W, wl.shard_heads(W, rank, world)
+    W = wl.make_workload(spec, config_id + 1000 * rank, device=str(device))
+    return W, W
+
+
+def decode_leg(args, config_id, world, rank, device, headline):
+    """Build, warm up and time one decode workload.  The headline leg also times
+    the other step path, the e2e path through host buffers and the CPU oracle;
+    returns the JSON line (headline) or a compact record of the same figures."""
     from paged_kv_cache_296_gb300 import binding as pa
     from paged_kv_cache_296_gb300.runner import DecodeStep, step_bytes, unique_kv_bytes
 
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    init_dist(world, "nccl")
-    pa.load()
-    spec = wl.SPECS[args.config]
-    W = wl.make_workload(spec, args.config + 1000 * rank, device=str(device))
+    spec = wl.SPECS[config_id]
+    W_all, W = rank_workload(args, config_id, world, rank, device)
     S = DecodeStep(W, device=device, partition_size=args.partition_size)
     total_bytes, kv_bytes, new_bytes = step_bytes(W)
     stream = torch.cuda.current_stream(device)
-    step_fn = S.append if args.path == "append" else S.step
+    path = args.path if headline else "append"
+    step_fn = S.append if path == "append" else S.step
 
     for _ in range(args.warmup):
         step_fn()
     torch.cuda.synchronize(device)
     pa.pa_device_status(clear=True)
-    flush_buf, l2_text = l2_plan(device, unique_kv_bytes(W) + (total_bytes - kv_bytes) + new_bytes)
+    flush_buf, _ = l2_plan(device, decode_distinct_bytes(W))
+    l2 = l2_text(decode_distinct_bytes(W_all), device_l2_bytes(device))
+    graphs = []  # kept alive until the leg ends
 
     def steps_per_graph(n):
         return max(d for d in range(1, min(n, 20) + 1) if n % d == 0)
@@ -485,15 +541,13 @@ def run_ours(args, world, rank, local):
                 g.replay()
         return run
 
-    graphs = []  # kept alive until the end of the run
-
-    def timed(path, n):
-        """Time n steps of `path`.  With inputs of twice the L2 size or more,
+    def timed(which, n):
+        """Time n steps of ``which``.  With inputs of twice the L2 size or more,
         CUDA events only at the ends of the region (an event between kernels
         would cost time and break their programmatic-launch overlap); with
         smaller ones, each step after an L2 flush, between its own events.
         Returns (ms per step, t0, t1)."""
-        fn = S.append if path == "append" else S.step
+        fn = S.append if which == "append" else S.step
         if flush_buf is not None:
             one = one_step_runner(fn, device, graphs, args.no_graph)
             barrier(world)
@@ -536,7 +590,7 @@ def run_ours(args, world, rank, local):
     sampler.start()
     time.sleep(0.3)  # let the sampler start before the timed region
     n = args.steps
-    ms_local, t_wall0, t_wall1 = timed(args.path, n)
+    ms_local, t_wall0, t_wall1 = timed(path, n)
     sampler.stop()
     ms_step = max_over_ranks(ms_local, world, device)
     status = pa.pa_device_status(clear=True)
@@ -544,16 +598,55 @@ def run_ours(args, world, rank, local):
         raise RuntimeError(f"device status {status:#x}: a kernel gave up waiting")
     # The step on the append path is one decode call (attention + merge), so
     # its mean duration over the timed region is the call's.
-    if args.path == "append":
-        decode_ms, write_ms = [ms_local], [0.0]
+    if path == "append":
+        dec_ms, write_ms = ms_local, 0.0
     else:
-        w_ms, d_ms = per_call(min(n, 500))
-        decode_ms, write_ms = [d_ms], [w_ms]
+        write_ms, dec_ms = per_call(min(n, 500))
+
+    all_kv = sum_over_ranks(kv_bytes, world, device)
+    value = all_kv / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    if path == "append":
+        call_bytes = total_bytes + new_bytes
+        kernel = "pa_decode_append (token write + attention, then the split-KV merge)"
+    else:
+        call_bytes = total_bytes
+        kernel = "pa_decode (attention + split-KV merge)"
+    achieved = call_bytes / (dec_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(config_id, path) if args.shard != "heads" or world == 1 else None
+    shared = spec.lens[0] == "shared_prefix"
+    roofline = {"bound": "hbm", "kernel": kernel,
+                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                "algorithmic_bytes_per_launch": call_bytes, "traffic": traffic}
+    if shared:
+        # each shared block counted once: the bytes the step must move at least
+        uniq = unique_kv_bytes(W) + (total_bytes - kv_bytes) + (new_bytes if path == "append" else 0)
+        roofline["unique_bytes_per_launch"] = uniq
+        roofline["frac_unique"] = round(uniq / (dec_ms * 1e-3) / 1e9 / peak, 4)
+    run_info = {"step": path,
+                "launch": "stream" if args.no_graph else
+                          "CUDA graph replay, 1 step per graph" if flush_buf is not None else
+                          f"CUDA graph replay, {steps_per_graph(n)} steps per graph",
+                "partition_tokens": S.partition_tokens}
+    clocks = sampler.summary(t_wall0, t_wall1)
+    if not headline:
+        rec = {"workload": spec.name, "config": workload_config(spec, W_all, l2, world, args.shard),
+               "value": round(value, 2), "unit": "GB/s", "us_per_step": round(ms_step * 1e3, 2),
+               "frac_of_hbm_peak": round(value / peak, 4),
+               "seqs_per_s": round(spec.num_seqs * (1 if args.shard == "heads" else world)
+                                   / (ms_step * 1e-3), 1),
+               "roofline": roofline, "run": run_info,
+               "gpu_launches": S.launches_per_step(path) * n, "clocks": clocks}
+        if shared:
+            rec["unique_kv_gbs"] = round(sum_over_ranks(unique_kv_bytes(W), world, device)
+                                         / (ms_step * 1e-3) / 1e9, 2)
+        return rec
 
     # The other way to run the same step, for comparison (not the headline).
     alt = None
     if not args.no_alt:
-        other = "separate" if args.path == "append" else "append"
+        other = "separate" if path == "append" else "append"
         fn = S.append if other == "append" else S.step
         for _ in range(args.warmup):
             fn()
@@ -606,7 +699,7 @@ def run_ours(args, world, rank, local):
         barrier(world)
         verify()
         e2e_ms = max_over_ranks(e_local, world, device)
-        e2e_gbs = sum_over_ranks(kv_bytes, world, device) / (e2e_ms * 1e-3) / 1e9
+        e2e_gbs = all_kv / (e2e_ms * 1e-3) / 1e9
         e2e = {"value": round(e2e_gbs, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
@@ -620,53 +713,57 @@ def run_ours(args, world, rank, local):
                          f"sequence cut to fewer tokens only if the time budget ends inside it), "
                          f"{secs:.1f} s, 1 BLAS thread"}
 
-    all_kv = sum_over_ranks(kv_bytes, world, device)
-    value = all_kv / (ms_step * 1e-3) / 1e9
-    dec_ms = statistics.mean(decode_ms)
-    peak, peak_kind = hbm_peak()
-    if args.path == "append":
-        call_bytes = total_bytes + new_bytes
-        kernel = "pa_decode_append (token write + attention, then the split-KV merge)"
-    else:
-        call_bytes = total_bytes
-        kernel = "pa_decode (attention + split-KV merge)"
-    achieved = call_bytes / (dec_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(args.config, args.path)
-    launches = S.launches_per_step(args.path) * n
-    uniq = unique_kv_bytes(W) if spec.lens[0] == "shared_prefix" else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": n, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "us_per_step": round(ms_step * 1e3, 2),
         "us_decode_call": round(dec_ms * 1e3, 2),
-        "us_write_call": round(statistics.mean(write_ms) * 1e3, 2) if args.path != "append" else None,
+        "us_write_call": round(write_ms * 1e3, 2) if path != "append" else None,
         "frac_of_hbm_peak": round(value / peak, 4),
-        "seqs_per_s": round(spec.num_seqs * world / (ms_step * 1e-3), 1),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "seqs_per_s": round(spec.num_seqs * (1 if args.shard == "heads" else world)
+                            / (ms_step * 1e-3), 1),
+        "higher_is_better": True,
+        "scaling": "strong" if (args.shard == "heads" and world > 1) else "weak",
+        "vs_baseline": None,
         "dtype": spec.kv_dtype if spec.kv_dtype == spec.q_dtype else f"{spec.q_dtype}+{spec.kv_dtype}",
         "data": "synthetic (seeded N(0,1) K/V/q; no model weights)",
-        "config": config_block(spec, W, {
-            "step": args.path,
-            "launch": "stream" if args.no_graph else
-                      "CUDA graph replay, 1 step per graph" if flush_buf is not None else
-                      f"CUDA graph replay, {steps_per_graph(n)} steps per graph",
-            "partition_tokens": S.partition_tokens,
-            "l2": l2_text,
-            "parallelism": f"replicas{world}" if world > 1 else "single GPU"}),
-        "roofline": {"bound": "hbm", "kernel": kernel,
-                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
-                     "algorithmic_bytes_per_launch": call_bytes,
-                     "traffic": traffic},
+        "config": workload_config(spec, W_all, l2, world, args.shard),
+        "run": run_info,
+        "roofline": roofline,
         "other_path": alt,
-        "gpu_launches": launches,
+        "gpu_launches": S.launches_per_step(path) * n,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "clocks": clocks,
     }
-    if uniq is not None:
-        line["unique_kv_gbs"] = round(uniq * world / (ms_step * 1e-3) / 1e9, 2)
-    clocks = sampler.summary(t_wall0, t_wall1)
-    line["clocks"] = clocks
+    if shared:
+        line["unique_kv_gbs"] = round(sum_over_ranks(unique_kv_bytes(W), world, device)
+                                      / (ms_step * 1e-3) / 1e9, 2)
+    return line
+
+
+def run_ours(args, world, rank, local):
+    """The decode headline on --config, then every --also workload in the same
+    process, each timed by the same rules; one JSON line with the others under
+    ``also``."""
+    from paged_kv_cache_296_gb300 import binding as pa
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    pa.load()
+    if args.shard == "heads" and world > 1:
+        for c in [args.config] + args.also:
+            if wl.SPECS[c].num_kv_heads % world:
+                raise SystemExit(f"--shard heads: workload {c} has {wl.SPECS[c].num_kv_heads} "
+                                 f"KV heads, not a multiple of {world}")
+    line = decode_leg(args, args.config, world, rank, device, headline=True)
+    also = {}
+    for c in args.also:
+        if c != args.config:
+            torch.cuda.empty_cache()
+            also[f"config{c}"] = decode_leg(args, c, world, rank, device, headline=False)
+    line["also"] = also or None
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -1179,12 +1276,16 @@ def run_reference(args, world, rank, local):
            "sample": f"float64 NumPy oracle, {nseq} sequence samples (all heads, contexts cut to "
                      f"the per-step time budget) over {args.steps} steps "
                      f"({tot_s:.1f} s), 1 BLAS thread"}
+    # the same config as the GPU arm's line for this workload and seed
+    l2 = l2_text(decode_distinct_bytes(W), device_l2_bytes())
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "scaling": "strong" if (args.shard == "heads" and world > 1) else "weak",
+            "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) K/V/q; no model weights)",
-            "config": config_block(spec, W, {"parallelism": "host cores, one thread"}),
+            "config": workload_config(spec, W, l2, world, args.shard),
+            "run": {"where": "host cores, one thread (rank 0 alone)"},
             "cpu_baseline": cpu,
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -1196,7 +1297,14 @@ def main(argv=None):
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
-    p.add_argument("--config", type=int, default=2, choices=sorted(wl.SPECS))
+    p.add_argument("--config", type=int, default=3, choices=sorted(wl.SPECS),
+                   help="the headline decode workload (default: the Llama-3-8B GQA batch)")
+    p.add_argument("--also", default="5,4,2",
+                   help="other decode workloads timed in the same run, reported under 'also' "
+                        "(comma list; '' for none)")
+    p.add_argument("--shard", default="seqs", choices=["seqs", "heads"],
+                   help="N>1: seqs = one batch per GPU (replicas, weak scaling); heads = the "
+                        "KV heads of one batch split over the GPUs (strong scaling)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--partition-size", type=int, default=0)
     p.add_argument("--path", default="append", choices=["append", "separate"],
@@ -1218,6 +1326,10 @@ def main(argv=None):
     p.add_argument("--blocks", action="store_true",
                    help="time the block manager (pa_copy_blocks; host step of pa_bm_*)")
     args = p.parse_args(argv)
+    args.also = [int(x) for x in args.also.split(",") if x.strip()]
+    for c in args.also:
+        if c not in wl.SPECS:
+            p.error(f"--also: no decode workload {c}")
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
     world, rank, local = dist_env()

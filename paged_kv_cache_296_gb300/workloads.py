@@ -18,7 +18,7 @@ machine; ``device="cuda"`` draws on the GPU instead (faster, different
 numbers) for timing runs that are not compared value by value.
 """
 
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 import math
 
 import numpy as np
@@ -234,6 +234,37 @@ def make_workload(spec, seed, device="cpu", poison=False, table_garbage=False):
         slot_mapping=torch.from_numpy(slots).to(device),
         kv_scale=kv_scale, scale=1.0 / math.sqrt(d), shared_blocks=n_shared,
     )
+
+
+def kv_head_range(num_kv_heads, rank, world):
+    """KV heads ``[h0, h1)`` that rank ``rank`` of ``world`` holds when a batch's
+    KV heads are split over GPUs in equal contiguous slices ("vLLM 部署深度指南",
+    分布式推理: tensor parallelism over the GPUs of one node)."""
+    if world < 1 or not 0 <= rank < world or num_kv_heads % world:
+        raise ValueError(f"{num_kv_heads} KV heads do not split over {world} ranks")
+    per = num_kv_heads // world
+    return rank * per, (rank + 1) * per
+
+
+def shard_heads(W, rank, world):
+    """Rank ``rank``'s part of decode workload ``W`` when its KV heads are split
+    over ``world`` GPUs: KV heads ``[h0, h1)`` of the pool and of the new
+    tokens, and the query heads that read them, ``[h0*G, h1*G)`` (query head h
+    reads KV head h // G).  Lengths, tables, slots and kv_scale are the whole
+    batch's.  Every rank's slice is an independent decode; the outputs
+    concatenated over ranks along the head axis are the whole batch's."""
+    spec = W.spec
+    h0, h1 = kv_head_range(spec.num_kv_heads, rank, world)
+    g = spec.num_q_heads // spec.num_kv_heads
+    sub = replace(spec, name=f"{spec.name} [kv heads {h0}..{h1 - 1}]",
+                  num_q_heads=(h1 - h0) * g, num_kv_heads=h1 - h0)
+    part = lambda t: None if t is None else t[:, :, :, h0:h1, :].contiguous()
+    return replace(W, spec=sub,
+                   pool=part(W.pool), pool_src=part(W.pool_src),
+                   q=W.q[:, h0 * g:h1 * g, :].contiguous(),
+                   k_new=W.k_new[:, h0:h1, :].contiguous(),
+                   v_new=W.v_new[:, h0:h1, :].contiguous(),
+                   extra=dict(W.extra, kv_heads=(h0, h1)))
 
 
 def _randn(shape, dtype, gen, device):

@@ -113,3 +113,76 @@ def test_l2_plan_flushes_only_below_twice_l2(monkeypatch):
     assert buf is not None and buf.numel() == 2000 and "flushed" in text
     buf, text = bench.l2_plan("cpu", 2000)
     assert buf is None and "no flush" in text
+
+
+def test_reference_arm_config_is_the_workload_config():
+    # The reference arm's config is exactly the dict the GPU arm prints for the
+    # same workload and seed: the workload, the L2 rule and the parallelism.
+    sys.path.insert(0, ROOT)
+    import bench
+    from paged_kv_cache_296_gb300 import workloads as wl
+    r = _run_bench(["--impl", "reference", "--config", "1", "--steps", "2", "--warmup", "3",
+                    "--ref-seconds", "1"], {"CUDA_VISIBLE_DEVICES": ""})
+    assert r.returncode == 0, r.stderr
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    W = wl.make_workload(wl.SPECS[1], 1)
+    want = bench.workload_config(wl.SPECS[1], W, bench.l2_text(bench.decode_distinct_bytes(W),
+                                                             129 * 10 ** 6), 1, "seqs")
+    assert d["config"] == json.loads(json.dumps(want))
+
+
+def _shard_rank_main(rank, world, port, out_q):
+    import numpy as np
+    from oracle import paged_attention as ref
+    from paged_kv_cache_296_gb300 import workloads as wl
+    torch.distributed.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}",
+                                         rank=rank, world_size=world)
+    spec = wl.Spec("gqa tiny", 3, 8, 4, 64, "bf16", "bf16", ("fixed", [5, 40, 17]))
+    W = wl.make_workload(spec, 77)                  # every rank draws the same whole batch
+    P = wl.shard_heads(W, rank, world)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    out = ref.paged_decode(bits(P.q), "bf16", bits(P.pool), P.block_tables.numpy(),
+                           P.context_lens.numpy(), P.scale, "bf16")
+    parts = [torch.zeros((3, 8 // world, 64), dtype=torch.float64) for _ in range(world)]
+    torch.distributed.all_gather(parts, torch.from_numpy(np.ascontiguousarray(out)))
+    if rank == 0:
+        whole = ref.paged_decode(bits(W.q), "bf16", bits(W.pool), W.block_tables.numpy(),
+                                 W.context_lens.numpy(), W.scale, "bf16")
+        out_q.put((torch.cat(parts, dim=1).numpy(), whole, P.spec.num_kv_heads))
+    torch.distributed.barrier()
+    torch.distributed.destroy_process_group()
+
+
+def test_kv_head_sharding_gloo_world2():
+    # Each rank decodes its slice of KV heads (and the query heads that read
+    # them) of one batch with no exchange; the slices, gathered along the head
+    # axis, are the whole batch's output exactly.
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_shard_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got, want, hkv_rank = q.get(timeout=300)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert hkv_rank == 2
+    assert got.shape == want.shape == (3, 8, 64)
+    assert (got == want).all()
+
+
+def test_kv_head_ranges_partition_the_heads():
+    from paged_kv_cache_296_gb300 import workloads as wl
+    for hkv in (1, 2, 4, 8, 32):
+        for world in (1, 2, 4, 8):
+            if hkv % world:
+                with pytest.raises(ValueError):
+                    wl.kv_head_range(hkv, 0, world)
+                continue
+            covered = []
+            for r in range(world):
+                h0, h1 = wl.kv_head_range(hkv, r, world)
+                assert h1 - h0 == hkv // world
+                covered.extend(range(h0, h1))
+            assert covered == list(range(hkv))
