@@ -225,7 +225,7 @@ def pipelined_e2e(S, step_fn, device):
     Returns (enqueue(k): k such steps on the current stream, verify(): the
     last enqueued step's output as copied back equals a plain step's bit for
     bit, h2d bytes per step, d2h bytes per step)."""
-    names = list(S.STEP_INPUTS)
+    names = list(getattr(S, "step_inputs", S.STEP_INPUTS))
     hosts, devs, sets = [], [], []
     for _ in range(2):
         h, d = S.stage_inputs()

@@ -172,6 +172,95 @@ pa_status pa_decode_append(void* out, const void* q, const void* k_new, const vo
                            size_t workspace_bytes, void* stream);
 
 /*
+ * pa_decode_shared -- pa_decode for a batch in which groups of sequences share
+ * the leading blocks of their block tables: each shared block is read once
+ * per call for all its sequences.
+ *
+ * Parallel sampling and beam search fork several sequences from one prompt;
+ * their block tables point at the same physical blocks for the prompt, and
+ * block-level sharing avoids storing (and, here, reading) that prefix again
+ * ("vLLM GitHub 项目：探索高效 LLM 推理服务", section 二 item 4; "vLLM 部署深度指南",
+ * section 代码层面理解, where several sequences' tables may name one block).
+ * The result is exactly what pa_decode defines for the same tables (up to
+ * fp32 rounding order): sharing changes only which CTA reads a block.
+ *
+ * Groups, as device int32 arrays in CSR form: group g's members are the
+ * sequence indices group_seqs[group_offsets[g] .. group_offsets[g+1]), and
+ * each member's table holds the same physical block at every entry j <
+ * group_blocks[g].  group_offsets has num_groups + 1 non-decreasing entries,
+ * group_offsets[0] = 0, and group_seqs has group_offsets[num_groups] entries.
+ * A sequence belongs to at most one group.  A member shorter than its group's
+ * shared blocks is handled exactly (it attends only its own tokens).  Per KV
+ * head, a group's members times the query heads per KV head are served as the
+ * columns of one tensor-core tile: at most 32 / (num_q_heads / num_kv_heads)
+ * members share; members past that count are decoded as unshared sequences.
+ * pa_find_shared_prefixes() builds the arrays from the tables.
+ *
+ * Limits: num_seqs <= 1024, num_groups <= 1024, and num_seqs *
+ * max_blocks_per_seq * num_kv_heads < 2^31 (else PA_ERR_UNSUPPORTED).
+ * The split of the work over CTAs is the library's (partition_size has no
+ * counterpart).  workspace: at least pa_decode_shared_workspace_size(...)
+ * bytes, 256-byte aligned, no initialisation needed.  Every other argument
+ * is pa_decode's.
+ */
+pa_status pa_decode_shared(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                           int max_blocks_per_seq, int num_blocks, int num_q_heads,
+                           int num_kv_heads, int head_size, int block_size, float scale,
+                           pa_dtype q_dtype, pa_dtype kv_dtype, float kv_scale,
+                           const int32_t* group_offsets, const int32_t* group_seqs,
+                           const int32_t* group_blocks, int num_groups, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
+ * pa_decode_append_shared -- pa_decode_append with shared-prefix groups: one
+ * launch appends each sequence's new token and attends as pa_decode_shared.
+ * A new token must land in a block that no other sequence of the batch reads
+ * (copy-on-write gives a forked sequence a private block before it writes);
+ * a member whose new token falls inside its group's shared blocks is not
+ * written.  Arguments: pa_decode_append's plus the group arrays.
+ */
+pa_status pa_decode_append_shared(void* out, const void* q, const void* k_new, const void* v_new,
+                                  const int64_t* slot_mapping, int64_t src_token_stride,
+                                  void* k_cache, void* v_cache, const int32_t* block_tables,
+                                  const int32_t* context_lens, int num_seqs,
+                                  int max_blocks_per_seq, int num_blocks, int num_q_heads,
+                                  int num_kv_heads, int head_size, int block_size, float scale,
+                                  pa_dtype q_dtype, pa_dtype kv_dtype, float kv_scale,
+                                  const int32_t* group_offsets, const int32_t* group_seqs,
+                                  const int32_t* group_blocks, int num_groups, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
+ * pa_decode_shared_workspace_size -- bytes of workspace pa_decode_shared and
+ * pa_decode_append_shared need (host only; 0 with pa_last_error() set for
+ * invalid arguments).
+ */
+size_t pa_decode_shared_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                       int head_size, int max_blocks_per_seq, int block_size,
+                                       int num_groups);
+
+/*
+ * pa_find_shared_prefixes -- build pa_decode_shared's group arrays from block
+ * tables held in HOST memory (host only, no GPU).
+ *
+ * Sequences whose tables start with the same physical block are grouped (in
+ * index order, at most 32 / (num_q_heads / num_kv_heads) per group); a group's
+ * shared length is the number of leading entries, within every member's
+ * ceil(L / block_size) blocks, on which all members' tables agree.  Groups of
+ * one sequence, or sharing fewer than min_blocks blocks, are dropped.
+ * block_tables int32 [num_seqs, max_blocks_per_seq] and context_lens int32
+ * [num_seqs] are host arrays; the outputs are host arrays with room for
+ * num_seqs + 1 (group_offsets) and num_seqs (group_seqs, group_blocks)
+ * entries; *num_groups_out receives the group count.
+ */
+pa_status pa_find_shared_prefixes(const int32_t* block_tables, const int32_t* context_lens,
+                                  int num_seqs, int max_blocks_per_seq, int block_size,
+                                  int num_q_heads, int num_kv_heads, int min_blocks,
+                                  int32_t* group_offsets, int32_t* group_seqs,
+                                  int32_t* group_blocks, int32_t* num_groups_out);
+
+/*
  * pa_decode_noalloc -- pa_decode for callers that cannot allocate device memory.
  *
  * The pages have no counterpart to this call: it exists for callers with no
@@ -261,10 +350,11 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
  * partition_size.  A positive request is used as given.  0 asks for the
  * library's choice, made from the batch shape: with num_seqs*num_kv_heads >=
  * 512 no split (partitions capped at 8192 tokens; a sequence no longer than
- * 512 tokens is never split either); otherwise a balanced split, returned as
- * 0: the decode kernel reads the context lengths and takes the smallest
- * partition size (>= 512 tokens) whose partitions over all sequences and KV
- * heads run in one wave of resident CTAs on this GPU.
+ * 512 tokens is never split either); otherwise a stream-K split, returned as
+ * 0: the decode kernel reads the context lengths and gives each CTA of one
+ * wave of resident CTAs on this GPU an equal range (at least 512 tokens) of
+ * the batch's (sequence, KV head, block) units, a range crossing from one
+ * sequence into the next where it ends.
  * Host only; -1 on invalid input.
  */
 int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_blocks_per_seq,

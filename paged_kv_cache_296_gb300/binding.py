@@ -33,6 +33,12 @@ SIGNATURES = {
                               _F, _I, _I, _F, _I, _P, _SZ, _P]),
     "pa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                                _F, _I, _P]),
+    "pa_decode_shared": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I, _F,
+                              _P, _P, _P, _I, _P, _SZ, _P]),
+    "pa_decode_append_shared": (_I, [_P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I, _I, _I, _I,
+                                     _I, _I, _I, _F, _I, _I, _F, _P, _P, _P, _I, _P, _SZ, _P]),
+    "pa_decode_shared_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "pa_find_shared_prefixes": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "pa_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                         _F, _P]),
     "pa_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
@@ -248,6 +254,108 @@ def pa_decode_append(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block
         d, bs, float(scale), dtype_code(q.dtype), dtype_code(k_cache.dtype), float(kv_scale),
         int(partition_size), _ptr(workspace), wbytes, _stream(q))
     _check("pa_decode_append", st)
+
+
+def pa_decode_shared_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size,
+                                    max_blocks_per_seq, block_size=16, num_groups=0):
+    return int(load().pa_decode_shared_workspace_size(num_seqs, num_q_heads, num_kv_heads,
+                                                      head_size, max_blocks_per_seq, block_size,
+                                                      num_groups))
+
+
+class SharedGroups:
+    """pa_decode_shared's group arrays (device int32 tensors, CSR over sequences)."""
+
+    def __init__(self, offsets, seqs, blocks):
+        self.offsets, self.seqs, self.blocks = offsets, seqs, blocks
+
+    @property
+    def num_groups(self):
+        return self.offsets.numel() - 1
+
+    def to(self, device):
+        return SharedGroups(self.offsets.to(device), self.seqs.to(device), self.blocks.to(device))
+
+
+def pa_find_shared_prefixes(block_tables, context_lens, num_q_heads, num_kv_heads, min_blocks=1,
+                            block_size=16):
+    """Groups of sequences whose (host) tables start with the same blocks, as
+    :class:`SharedGroups` of CPU tensors (``.to(device)`` for the decode)."""
+    bt = block_tables.to("cpu", torch.int32).contiguous()
+    cl = context_lens.to("cpu", torch.int32).contiguous()
+    B = cl.shape[0]
+    if bt.dim() != 2 or bt.shape[0] != B:
+        raise ValueError("block_tables must be [B, max_blocks], context_lens [B]")
+    offs = torch.zeros(B + 1, dtype=torch.int32)
+    seqs = torch.zeros(max(B, 1), dtype=torch.int32)
+    blks = torch.zeros(max(B, 1), dtype=torch.int32)
+    ng = ctypes.c_int32(0)
+    st = load().pa_find_shared_prefixes(_ptr(bt), _ptr(cl), B, bt.shape[1], block_size,
+                                        num_q_heads, num_kv_heads, int(min_blocks), _ptr(offs),
+                                        _ptr(seqs), _ptr(blks), ctypes.byref(ng))
+    _check("pa_find_shared_prefixes", st)
+    n = ng.value
+    nm = int(offs[n])
+    return SharedGroups(offs[:n + 1].clone(), seqs[:max(nm, 1)].clone(), blks[:max(n, 1)].clone())
+
+
+def _shared_args(groups):
+    if groups.offsets.dtype != torch.int32 or groups.seqs.dtype != torch.int32 \
+            or groups.blocks.dtype != torch.int32:
+        raise ValueError("group arrays must be int32")
+    return _ptr(groups.offsets), _ptr(groups.seqs), _ptr(groups.blocks), groups.num_groups
+
+
+def pa_decode_shared(out, q, k_cache, v_cache, block_tables, context_lens, scale, groups,
+                     kv_scale=1.0, workspace=None):
+    """pa_decode with shared-prefix ``groups`` (:class:`SharedGroups` on q's device)."""
+    nb, bs, hkv, d = _cache_geometry(k_cache, v_cache)
+    B, hq, dq = q.shape
+    if dq != d or out.shape != q.shape or not q.is_contiguous() or not out.is_contiguous():
+        raise ValueError("q and out must be contiguous [B, Hq, D] tensors")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 \
+            or not block_tables.is_contiguous() or not context_lens.is_contiguous():
+        raise ValueError("block_tables and context_lens must be contiguous int32 tensors")
+    mb = block_tables.shape[1]
+    if workspace is None:
+        workspace = alloc_workspace(
+            pa_decode_shared_workspace_size(B, hq, hkv, d, mb, bs, groups.num_groups), q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().pa_decode_shared(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        B, mb, nb, hq, hkv, d, bs, float(scale), dtype_code(q.dtype), dtype_code(k_cache.dtype),
+        float(kv_scale), *_shared_args(groups), _ptr(workspace), wbytes, _stream(q))
+    _check("pa_decode_shared", st)
+
+
+def pa_decode_append_shared(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                            context_lens, scale, groups, kv_scale=1.0, workspace=None):
+    """pa_decode_append with shared-prefix ``groups``: write each new token, then decode."""
+    nb, bs, hkv, d = _cache_geometry(k_cache, v_cache)
+    B, hq, dq = q.shape
+    if dq != d or out.shape != q.shape or not q.is_contiguous() or not out.is_contiguous():
+        raise ValueError("q and out must be contiguous [B, Hq, D] tensors")
+    if k_new.shape != (B, hkv, d) or v_new.shape != k_new.shape or k_new.stride() != v_new.stride() \
+            or k_new.stride(1) != d or k_new.stride(2) != 1 or k_new.dtype != q.dtype \
+            or v_new.dtype != q.dtype:
+        raise ValueError("k_new and v_new must be [B, Hkv, D] of q's dtype with unit inner strides")
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_contiguous() \
+            or slot_mapping.shape != (B,):
+        raise ValueError("slot_mapping must be a contiguous int64 [B] tensor")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 \
+            or not block_tables.is_contiguous() or not context_lens.is_contiguous():
+        raise ValueError("block_tables and context_lens must be contiguous int32 tensors")
+    mb = block_tables.shape[1]
+    if workspace is None:
+        workspace = alloc_workspace(
+            pa_decode_shared_workspace_size(B, hq, hkv, d, mb, bs, groups.num_groups), q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().pa_decode_append_shared(
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), k_new.stride(0),
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), B, mb, nb, hq, hkv,
+        d, bs, float(scale), dtype_code(q.dtype), dtype_code(k_cache.dtype), float(kv_scale),
+        *_shared_args(groups), _ptr(workspace), wbytes, _stream(q))
+    _check("pa_decode_append_shared", st)
 
 
 #: Bytes of the library's fixed split-KV scratch used by pa_decode_noalloc.

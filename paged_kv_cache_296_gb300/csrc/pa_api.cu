@@ -58,17 +58,25 @@ int elt_bytes(pa_dtype d) {
   return 0;
 }
 
-// Split-KV partition size (tokens), 0 for a balanced split, or -1 when the
+// Whether the stream-K kernel can plan this batch: its per-CTA plan holds
+// every sequence and group, and unit counts stay below 2^31.
+bool split_fits(int num_seqs, int num_kv_heads, int max_blocks_per_seq, int num_groups) {
+  return num_seqs <= pa::kMaxPlanSeqs && num_groups <= pa::kMaxPlanGroups &&
+         2 * num_kv_heads <= pa::kMaxSplitCtas &&  // two CTAs per KV head group at least
+         ((long long)num_seqs + num_groups) * max_blocks_per_seq * std::max(1, num_kv_heads) <
+             (1LL << 31);
+}
+
+// Split-KV partition size (tokens), 0 for the stream-K split, or -1 when the
 // request is invalid.  A request of 0 decides from the batch shape alone (no
 // device query, so the host-side sizing calls agree with pa_decode everywhere):
 //   * with >= kTargetPairs (sequence, KV head) pairs there are enough CTAs
 //     already: no split, except that no partition exceeds kMaxPartitionTokens
 //     (bounds the slowest CTA);
-//   * otherwise a balanced split (returned as 0): the decode kernel reads the
-//     actual context lengths and picks the smallest partition size, at least
-//     kMinPartitionTokens, whose partitions over all sequences and KV heads
-//     fit in one wave of resident CTAs, so every SM streams from the start to
-//     the end and the longest CTA is as short as that allows.
+//   * otherwise the stream-K split (returned as 0): the decode kernel reads the
+//     actual context lengths and gives every CTA of one wave an equal range
+//     of (sequence, KV head group, block) units, at least kMinPartitionTokens
+//     of them, so every SM streams from the start to the end.
 // Measured on GB300: a CTA streams about its ring (64 KB) per loaded memory
 // latency (~3.5 us), so a batch of a few long sequences must be split, and a
 // split that spills into a second wave leaves a long tail.
@@ -77,39 +85,63 @@ int partition_tokens(int num_seqs, int num_kv_heads, int max_blocks_per_seq, int
   if (requested > 0) return requested;
   const long long max_tokens = (long long)max_blocks_per_seq * kBlockSize;
   const long long pairs = std::max(1LL, (long long)num_seqs * std::max(1, num_kv_heads));
-  if (pairs >= kTargetPairs) {
+  if (pairs >= kTargetPairs || !split_fits(num_seqs, num_kv_heads, max_blocks_per_seq, 0)) {
     return (int)std::max<long long>(kBlockSize, std::min<long long>(max_tokens, kMaxPartitionTokens));
   }
   if (max_tokens <= kMinPartitionTokens) return (int)std::max<long long>(kBlockSize, max_tokens);
   return 0;
 }
 
-// Partitions of the grid (per sequence and KV head) for a partition size from
-// partition_tokens(); for a balanced split, enough for its smallest size.
+// Partitions of the grid (per sequence and KV head) for a fixed partition size.
 int num_partitions(int max_blocks_per_seq, int part_tokens) {
+  if (part_tokens <= 0) return 0;  // stream-K: no per-sequence partitions
   const long long max_tokens = (long long)max_blocks_per_seq * kBlockSize;
-  const long long unit = part_tokens > 0 ? part_tokens : kMinPartitionTokens;
-  const long long p = (max_tokens + unit - 1) / unit;
+  const long long p = (max_tokens + part_tokens - 1) / part_tokens;
   return (int)(p < 1 ? 1 : p);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Split-KV workspace: partial m, l, O per (sequence, query head, partition),
-// then 256 bytes where a balanced split records its partition size.
+// Split-KV workspace.  Fixed partitions: partial m, l, O per (sequence, query
+// head, partition).  Stream-K: "cut" partials per (CTA, slot, column) for at
+// most kMaxSplitCtas CTAs of up to kMaxSplitHeads KV heads (columns: the
+// heads' query heads, or kPrefixCols per head with shared-prefix groups),
+// "whole" partials per (sequence, query head) for the prefix and the suffix
+// of group members, and the kernel's plan for the merge kernel.
 struct WorkspaceLayout {
-  size_t m_off, l_off, o_off, plan_off, total;
+  size_t m_off, l_off, o_off;              // fixed partitions or cut partials
+  size_t wm_off, wl_off, wo_off;           // whole partials (groups only)
+  size_t plan_off, total;
+  int cut_cols;
 };
 
-WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_size, int nparts) {
-  WorkspaceLayout w{0, 0, 0, 0, 0};
-  if (nparts <= 1) return w;
-  const size_t rows = (size_t)num_seqs * num_q_heads * nparts;
+WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
+                                 int nparts, bool split, int num_groups) {
+  WorkspaceLayout w{0, 0, 0, 0, 0, 0, 0, 0, 0};
+  size_t rows = 0;
+  if (split) {
+    const int g = num_q_heads / std::max(1, num_kv_heads);
+    w.cut_cols = pa::kMaxSplitHeads * (num_groups > 0 ? pa::kPrefixCols : g);
+    rows = (size_t)pa::kMaxSplitCtas * 2 * w.cut_cols;
+  } else {
+    if (nparts <= 1) return w;
+    rows = (size_t)num_seqs * num_q_heads * nparts;
+  }
   w.m_off = 0;
   w.l_off = align256(rows * sizeof(float));
   w.o_off = w.l_off + align256(rows * sizeof(float));
-  w.plan_off = w.o_off + align256(rows * head_size * sizeof(float));
-  w.total = w.plan_off + 256;
+  size_t end = w.o_off + align256(rows * head_size * sizeof(float));
+  if (split && num_groups > 0) {
+    const size_t wrows = 2 * (size_t)num_seqs * num_q_heads;
+    w.wm_off = end;
+    w.wl_off = w.wm_off + align256(wrows * sizeof(float));
+    w.wo_off = w.wl_off + align256(wrows * sizeof(float));
+    end = w.wo_off + align256(wrows * head_size * sizeof(float));
+  }
+  w.plan_off = end;
+  const size_t plan_ints =
+      split ? (size_t)pa::kPlanHeader + 4 * (size_t)num_seqs + 2 * (size_t)num_groups : 64;
+  w.total = w.plan_off + align256(plan_ints * sizeof(int));
   return w;
 }
 
@@ -135,8 +167,17 @@ pa_status check_pool(int num_blocks, int num_kv_heads) {
   return PA_OK;
 }
 
-// Shared by pa_decode and pa_decode_append (`fn` names the caller in messages;
-// `k_new` == NULL means no fused write).
+// Shared-prefix groups of one call (device arrays; see pa_decode_shared).
+struct Groups {
+  const int32_t* offsets;   // [num_groups + 1]
+  const int32_t* seqs;      // [offsets[num_groups]]
+  const int32_t* blocks;    // [num_groups]
+  int num_groups;
+};
+
+// Shared by pa_decode, pa_decode_append and their shared-prefix forms (`fn`
+// names the caller in messages; `k_new` == NULL means no fused write; `grp` ==
+// NULL means no shared-prefix groups).
 pa_status decode_impl(const char* fn, void* out, const void* q, const void* k_cache,
                       const void* v_cache, const int32_t* block_tables,
                       const int32_t* context_lens, int num_seqs, int max_blocks_per_seq,
@@ -144,7 +185,8 @@ pa_status decode_impl(const char* fn, void* out, const void* q, const void* k_ca
                       int block_size, float scale, pa_dtype q_dtype, pa_dtype kv_dtype,
                       float kv_scale, int partition_size, void* workspace,
                       size_t workspace_bytes, void* stream, const void* k_new,
-                      const void* v_new, const int64_t* slot_mapping, int64_t src_token_stride) {
+                      const void* v_new, const int64_t* slot_mapping, int64_t src_token_stride,
+                      const Groups* grp) {
   pa_status st;
   if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs must be >= 0 (got %d)", num_seqs);
   if (num_seqs > 65535) return fail(PA_ERR_UNSUPPORTED, "num_seqs %d exceeds 65535", num_seqs);
@@ -170,13 +212,33 @@ pa_status decode_impl(const char* fn, void* out, const void* q, const void* k_ca
     return fail(PA_ERR_INVALID_ARG, "scale must be finite");
   if (kv_dtype == PA_E4M3 && (!(kv_scale > 0.f) || kv_scale == INFINITY))
     return fail(PA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an E4M3 cache");
-  const int part = partition_tokens(num_seqs, num_kv_heads, max_blocks_per_seq, partition_size);
-  if (part < 0)
-    return fail(PA_ERR_INVALID_ARG, "partition_size must be 0 or a positive multiple of 16 (got %d)",
-                partition_size);
+  int part;
+  int num_groups = 0;
+  if (grp) {
+    num_groups = grp->num_groups;
+    if (num_groups < 0) return fail(PA_ERR_INVALID_ARG, "num_groups must be >= 0 (got %d)", num_groups);
+    if (!split_fits(num_seqs, num_kv_heads, max_blocks_per_seq, num_groups))
+      return fail(PA_ERR_UNSUPPORTED,
+                  "%s: at most %d sequences and %d groups, and fewer than 2^31 blocks over all "
+                  "sequences and KV heads",
+                  fn, pa::kMaxPlanSeqs, pa::kMaxPlanGroups);
+    if (num_groups > 0 && (!grp->offsets || !grp->seqs || !grp->blocks))
+      return fail(PA_ERR_INVALID_ARG, "null group array");
+    if ((reinterpret_cast<uintptr_t>(grp->offsets) | reinterpret_cast<uintptr_t>(grp->seqs) |
+         reinterpret_cast<uintptr_t>(grp->blocks)) & 3u)
+      return fail(PA_ERR_INVALID_ARG, "group arrays must be 4-byte aligned");
+    part = 0;  // the stream-K kernel serves the groups
+  } else {
+    part = partition_tokens(num_seqs, num_kv_heads, max_blocks_per_seq, partition_size);
+    if (part < 0)
+      return fail(PA_ERR_INVALID_ARG,
+                  "partition_size must be 0 or a positive multiple of 16 (got %d)", partition_size);
+  }
   const int np = num_partitions(max_blocks_per_seq, part);
   if (np > 65535) return fail(PA_ERR_UNSUPPORTED, "too many partitions (%d)", np);
-  const WorkspaceLayout ws = workspace_layout(num_seqs, num_q_heads, head_size, np);
+  const bool split = part == 0;
+  const WorkspaceLayout ws =
+      workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_size, np, split, num_groups);
   if (num_seqs == 0) return ok();
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
     return fail(PA_ERR_INVALID_ARG, "null pointer argument");
@@ -225,10 +287,22 @@ pa_status decode_impl(const char* fn, void* out, const void* q, const void* k_ca
   a.min_partition_tokens = (int)kMinPartitionTokens;
   a.num_partitions = np;
   auto* wsb = static_cast<uint8_t*>(workspace);
-  a.part_m = ws.total ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
-  a.part_l = ws.total ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
-  a.part_o = ws.total ? reinterpret_cast<float*>(wsb + ws.o_off) : nullptr;
-  a.plan = ws.total ? reinterpret_cast<int*>(wsb + ws.plan_off) : nullptr;
+  auto at = [&](size_t off) { return ws.total ? reinterpret_cast<float*>(wsb + off) : nullptr; };
+  a.part_m = split ? nullptr : at(ws.m_off);
+  a.part_l = split ? nullptr : at(ws.l_off);
+  a.part_o = split ? nullptr : at(ws.o_off);
+  a.cut_m = split ? at(ws.m_off) : nullptr;
+  a.cut_l = split ? at(ws.l_off) : nullptr;
+  a.cut_o = split ? at(ws.o_off) : nullptr;
+  a.cut_cols = ws.cut_cols;
+  a.whole_m = split && num_groups ? at(ws.wm_off) : nullptr;
+  a.whole_l = split && num_groups ? at(ws.wl_off) : nullptr;
+  a.whole_o = split && num_groups ? at(ws.wo_off) : nullptr;
+  a.plan = split ? reinterpret_cast<int*>(wsb + ws.plan_off) : nullptr;
+  a.grp_off = grp && num_groups ? grp->offsets : nullptr;
+  a.grp_seq = grp && num_groups ? grp->seqs : nullptr;
+  a.grp_blocks = grp && num_groups ? grp->blocks : nullptr;
+  a.num_groups = num_groups;
   a.append = k_new != nullptr;
   a.k_new = k_new;
   a.v_new = v_new;
@@ -264,7 +338,7 @@ extern "C" {
 
 const char* pa_last_error(void) { return g_last_error.c_str(); }
 
-int pa_version(void) { return 110; }
+int pa_version(void) { return 120; }
 
 uint32_t pa_device_status(int clear) {
   unsigned* p = nullptr;
@@ -426,7 +500,20 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
     return 0;
   }
   const int np = num_partitions(max_blocks_per_seq, part);
-  return workspace_layout(num_seqs, num_q_heads, head_size, np).total;
+  return workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_size, np, part == 0, 0).total;
+}
+
+size_t pa_decode_shared_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                       int head_size, int max_blocks_per_seq, int block_size,
+                                       int num_groups) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 ||
+      block_size != kBlockSize || (head_size != 64 && head_size != 128) || num_groups < 0 ||
+      !split_fits(num_seqs, num_kv_heads, max_blocks_per_seq, num_groups)) {
+    fail(PA_ERR_INVALID_ARG, "invalid arguments to pa_decode_shared_workspace_size");
+    return 0;
+  }
+  return workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_size, 0, true, num_groups)
+      .total;
 }
 
 int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_blocks_per_seq,
@@ -444,7 +531,7 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
   return decode_impl("pa_decode", out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
                      max_blocks_per_seq, num_blocks, num_q_heads, num_kv_heads, head_size,
                      block_size, scale, q_dtype, kv_dtype, kv_scale, partition_size, workspace,
-                     workspace_bytes, stream, nullptr, nullptr, nullptr, 0);
+                     workspace_bytes, stream, nullptr, nullptr, nullptr, 0, nullptr);
 }
 
 pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
@@ -461,7 +548,43 @@ pa_status pa_decode_append(void* out, const void* q, const void* k_new, const vo
                      num_seqs, max_blocks_per_seq, num_blocks, num_q_heads, num_kv_heads,
                      head_size, block_size, scale, q_dtype, kv_dtype, kv_scale, partition_size,
                      workspace, workspace_bytes, stream, k_new, v_new, slot_mapping,
-                     src_token_stride);
+                     src_token_stride, nullptr);
+}
+
+pa_status pa_decode_shared(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                           int max_blocks_per_seq, int num_blocks, int num_q_heads,
+                           int num_kv_heads, int head_size, int block_size, float scale,
+                           pa_dtype q_dtype, pa_dtype kv_dtype, float kv_scale,
+                           const int32_t* group_offsets, const int32_t* group_seqs,
+                           const int32_t* group_blocks, int num_groups, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  const Groups grp{group_offsets, group_seqs, group_blocks, num_groups};
+  return decode_impl("pa_decode_shared", out, q, k_cache, v_cache, block_tables, context_lens,
+                     num_seqs, max_blocks_per_seq, num_blocks, num_q_heads, num_kv_heads,
+                     head_size, block_size, scale, q_dtype, kv_dtype, kv_scale, 0, workspace,
+                     workspace_bytes, stream, nullptr, nullptr, nullptr, 0, &grp);
+}
+
+pa_status pa_decode_append_shared(void* out, const void* q, const void* k_new, const void* v_new,
+                                  const int64_t* slot_mapping, int64_t src_token_stride,
+                                  void* k_cache, void* v_cache, const int32_t* block_tables,
+                                  const int32_t* context_lens, int num_seqs,
+                                  int max_blocks_per_seq, int num_blocks, int num_q_heads,
+                                  int num_kv_heads, int head_size, int block_size, float scale,
+                                  pa_dtype q_dtype, pa_dtype kv_dtype, float kv_scale,
+                                  const int32_t* group_offsets, const int32_t* group_seqs,
+                                  const int32_t* group_blocks, int num_groups, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (num_seqs > 0 && (!k_new || !v_new || !slot_mapping))
+    return fail(PA_ERR_INVALID_ARG,
+                "pa_decode_append_shared: k_new, v_new and slot_mapping are required");
+  const Groups grp{group_offsets, group_seqs, group_blocks, num_groups};
+  return decode_impl("pa_decode_append_shared", out, q, k_cache, v_cache, block_tables,
+                     context_lens, num_seqs, max_blocks_per_seq, num_blocks, num_q_heads,
+                     num_kv_heads, head_size, block_size, scale, q_dtype, kv_dtype, kv_scale, 0,
+                     workspace, workspace_bytes, stream, k_new, v_new, slot_mapping,
+                     src_token_stride, &grp);
 }
 
 pa_status pa_gather_kv(void* k_out, void* v_out, const void* k_cache, const void* v_cache,

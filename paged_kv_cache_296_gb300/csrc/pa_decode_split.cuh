@@ -1,0 +1,715 @@
+// Stream-K split of paged decode, with optional shared-prefix groups.
+//
+// The work is laid out as lines of units, one unit = one 16-token block, two
+// lines per KV head group (the same units for every group), and every CTA
+// takes an equal range of one line:
+//   * the suffix line: for each sequence i in order, the blocks of its own
+//     part of the context, [P_i, ceil(L_i / 16)), where P_i is the length in
+//     blocks of the shared prefix it belongs to (0 if none);
+//   * the prefix line: for each shared-prefix group, the blocks [0, n_g) that
+//     every member's table holds.  Parallel sampling forks several sequences
+//     from one prompt, and their tables point at the same physical blocks
+//     ("vLLM GitHub 项目…", section 二 item 4: block-level sharing, so shared
+//     storage is not repeated); a prefix CTA streams each such block once and
+//     computes the logits of all members' query heads against it, the
+//     members x G heads forming up to 32 MMA columns (four n-tiles, one per
+//     consumer warp of each head).
+// CTA c serves KV head group c % kvgc, so the CTAs reading the adjacent head
+// slices of the same blocks run side by side.  A CTA's range may end inside
+// a row or span several rows; each stretch of a row it covers is a segment.
+// A segment that covers a whole row of a sequence with no shared prefix
+// writes the normalised output; every other segment writes an fp32 partial
+// (m, l, O): "whole" partials per (sequence, query head), "cut" partials per
+// (CTA, slot), slot 0 for the CTA's first segment and 1 for its last (a cut
+// row is always one of the two).  The merge kernel finds, for every
+// (sequence, query head), the partials that cover its context from the same
+// plan and combines them by log-sum-exp.
+//
+// The plan is computed by every CTA from the context lengths (no host sync):
+// prefix sums of row lengths, the number of CTAs each line gets (in
+// proportion to its units, prefix units counted double) and the range width
+// W = ceil(units / CTAs) of each line (at least min_units).  CTA 0 stores it
+// for the merge kernel.
+//
+// Inside a CTA the ring, the producer and the per-block step are the fixed
+// kernel's.  On the suffix line warp 4j + w of head j consumes blocks
+// w, w+4, ... of the CTA's range (stage ownership never changes across
+// segments), and at each segment end the four warps' states are merged through
+// a buffer outside the ring (the producer keeps filling the ring meanwhile).
+// On the prefix line every consumer warp reads every block for its own n-tile
+// of columns and writes its columns' partials itself.
+#pragma once
+
+#include "pa_decode_kernel.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+// Plan record in the workspace (ints): [0] CTAs on each group's prefix line,
+// [1] its range width, [2] the suffix line's width, [3] KV head groups; from
+// kPlanHeader, per sequence i four ints: U_i (suffix blocks before i), n_i
+// (its suffix blocks), g_i (its group or -1), j_i (its index among the
+// group's members); then per group g two ints: Up_g, n_g.  CTA c of line
+// position k serves KV head group c % kvgc with k = c / kvgc (prefix line
+// first).
+__host__ __device__ constexpr size_t split_plan_ints(int num_seqs, int num_groups) {
+  return (size_t)kPlanHeader + 4 * (size_t)num_seqs + 2 * (size_t)num_groups;
+}
+
+// Shared-memory plan arrays (ints): sU[B+1], sP[B], sG[B], sJ[B], sUp[NG+1].
+__host__ __device__ constexpr size_t split_smem_plan_bytes(int num_seqs, int num_groups) {
+  return (4 * (size_t)num_seqs + (size_t)num_groups + 2) * 4;
+}
+
+template <int D, int KV>
+struct SplitCfg {
+  using C = DecodeCfg<D, KV>;
+  // Two CTAs per SM (shared memory allows no more).  The register cap this implies
+  // is per SM sub-partition: 2 x 9 warps of the E4M3 CTA put 5 warps on one of
+  // the four 16K-register files, so at most 96 registers a thread.
+  static constexpr int kMinCtasPerSm = 2;
+  // ring (1024-aligned) | merge buffer | full and empty barriers | plan arrays
+  static constexpr int kRedOffset = C::kRingBytes;
+  static constexpr int kBarOffset = kRedOffset + C::kRedBytes;
+  static constexpr int kPlanOffset = kBarOffset + 2 * C::kStages * 8;
+  __host__ __device__ static constexpr size_t smem_bytes(int num_seqs, int num_groups) {
+    return 1024 + (size_t)kPlanOffset + split_smem_plan_bytes(num_seqs, num_groups);
+  }
+};
+
+// Exclusive scan in place: on entry a[1..n] hold counts, on exit a[i] is the
+// sum of the first i counts (a[0] = 0).  One warp.
+__device__ __forceinline__ void warp_scan_counts(int* a, int n) {
+  const int lane = threadIdx.x & 31;
+  int carry = 0;
+  for (int base = 1; base <= n; base += 32) {
+    const int i = base + lane;
+    int v = i <= n ? a[i] : 0;
+#pragma unroll
+    for (int x = 1; x < 32; x <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, v, x);
+      if (lane >= x) v += o;
+    }
+    if (i <= n) a[i] = v + carry;
+    carry += __shfl_sync(0xffffffffu, v, 31);
+  }
+  if (lane == 0) a[0] = 0;
+}
+
+// The segment of a line that starts at unit u (u inside the line, u < end).
+struct Segment {
+  int row;            // sequence (suffix line) or group (prefix line)
+  int kvg;            // KV head group
+  int b0;             // first block, counted from the row's first (shared) block
+  int nblk;           // blocks in the segment
+  bool whole;         // the segment is its row's whole range
+  bool first;         // the segment starts the CTA's range (cut slot 0, else 1)
+  bool row_end;       // the segment reaches its row's last block
+};
+
+// The segment of a KV head group's line that starts at unit u (u < u_end).
+// Unit counts fit in 32 bits: the host admits a call only if (sequences +
+// groups) x max_blocks_per_seq x num_kv_heads < 2^31.
+__device__ __forceinline__ Segment segment_at(int u, int u_begin, int u_end, const int* base,
+                                              int nrows, const int* first_blk) {
+  // the row r with base[r] <= u < base[r + 1] (rows of no units skipped)
+  int lo = 0, hi = nrows - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (base[mid + 1] > u) hi = mid; else lo = mid + 1;
+  }
+  Segment s;
+  s.row = lo;
+  s.kvg = 0;  // set by the caller: a CTA's line belongs to one KV head group
+  const int row_start = base[lo];
+  const int row_stop = base[lo + 1];
+  const int seg_end = min(row_stop, u_end);
+  s.b0 = (first_blk ? first_blk[lo] : 0) + (u - row_start);
+  s.nblk = seg_end - u;
+  s.whole = (u == row_start) && (seg_end == row_stop);
+  s.first = (u == u_begin);
+  s.row_end = (seg_end == row_stop);
+  return s;
+}
+
+__device__ __forceinline__ void consumer_bar(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// kShared: the call has shared-prefix groups (else the prefix line, its plan
+// and its consumer path are compiled out).
+template <int D, int KV, int QT, bool kAppend, bool kShared>
+__global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::kMinCtasPerSm)
+    paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                              const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
+  using C = DecodeCfg<D, KV>;
+  using SC = SplitCfg<D, KV>;
+  constexpr int kT = C::kThreads;
+  constexpr int kConsumerThreads = C::kConsumerWarps * 32;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
+  float* red_o = reinterpret_cast<float*>(smem + SC::kRedOffset);    // [warps][8][D+4]
+  float* red_m = red_o + C::kConsumerWarps * 8 * C::kRedStride;       // [warps][8]
+  float* red_l = red_m + C::kConsumerWarps * 8;                       // [warps][8]
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + SC::kBarOffset);
+  uint64_t* empty_bar = full_bar + C::kStages;
+  __shared__ int abort_flag;
+
+  const int B = p.num_seqs;
+  const int NG = kShared ? p.num_groups : 0;
+  const int kvgc = p.kv_groups;
+  const int cap = p.max_blocks_per_seq * 16;
+  int* sU = reinterpret_cast<int*>(smem + SC::kPlanOffset);  // [B+1]
+  int* sP = sU + B + 1;                                      // [B]
+  int* sG = sP + B;                                          // [B]
+  int* sJ = sG + B;                                          // [B]
+  int* sUp = sJ + B;                                         // [NG+1]
+
+  if (threadIdx.x == C::kConsumerWarps * 32) {
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+  }
+  // Every input may come from the kernel before this one on the stream.
+  griddep_wait();
+
+  // ------------------------------------------------------------------ plan
+  const int tid = threadIdx.x;
+  for (int i = tid; i < B; i += kT) {
+    sP[i] = 0;
+    sG[i] = -1;
+    sJ[i] = 0;
+  }
+  if (tid == 0) abort_flag = 0;
+  __syncthreads();
+  // Groups: each member's suffix starts after the group's shared blocks.  A
+  // group's prefix row has n_g = min(shared blocks, the longest member's
+  // blocks) units.  Members past the columns a prefix CTA has (32 / G per KV
+  // head) are left out of the group: their whole context is suffix.
+  const int max_members = kPrefixCols / p.group;
+  const int n_members = (kShared && NG > 0) ? max(0, p.grp_off[NG]) : 0;
+  for (int g = tid; g < NG; g += kT) {
+    const int o0 = min(max(p.grp_off[g], 0), n_members);
+    const int o1 = min(max(p.grp_off[g + 1], o0), min(n_members, o0 + max_members));
+    const int pg = min(max(p.grp_blocks[g], 0), p.max_blocks_per_seq);
+    int maxnb = 0;
+    for (int k = o0; k < o1; ++k) {
+      const int s = p.grp_seq[k];
+      if (s < 0 || s >= B) continue;
+      const int L = min(max(p.context_lens[s], 0), cap);
+      maxnb = max(maxnb, (L + 15) >> 4);
+      sP[s] = pg;
+      sG[s] = g;
+      sJ[s] = k - o0;
+    }
+    sUp[g + 1] = min(pg, maxnb);
+  }
+  __syncthreads();
+  for (int i = tid; i < B; i += kT) {
+    const int L = min(max(p.context_lens[i], 0), cap);
+    sU[i + 1] = max(0, ((L + 15) >> 4) - sP[i]);
+  }
+  __syncthreads();
+  if (tid < 32) warp_scan_counts(sU, B);
+  else if (tid < 64) warp_scan_counts(sUp, NG);
+  __syncthreads();
+
+  // Each KV head group has its own two lines (the units are the same for every
+  // group); CTA c serves group c % kvgc, so the kvgc CTAs that read the same
+  // blocks' adjacent head slices run side by side (DRAM pages are opened once
+  // for all of them).  Prefix units count double in the split of a group's
+  // CTAs between its lines: a prefix CTA's warps each run every block.
+  const int Tp = sUp[NG];
+  const int Ts = sU[B];
+  const int Skv = (int)gridDim.x / kvgc;  // >= 2 (the launcher's rule)
+  int n_pre;
+  if (Tp == 0) {
+    n_pre = 0;
+  } else if (Ts == 0) {
+    n_pre = Skv;
+  } else {
+    const long long wp = 2LL * Tp;
+    n_pre = (int)(((long long)Skv * wp + (wp + Ts) / 2) / (wp + Ts));
+    n_pre = min(max(n_pre, 1), Skv - 1);
+  }
+  const int Wp = n_pre ? max(p.min_units, (Tp + n_pre - 1) / n_pre) : 1;
+  const int Ws = (Skv - n_pre) ? max(p.min_units, (Ts + (Skv - n_pre) - 1) / (Skv - n_pre)) : 1;
+  if (blockIdx.x == 0) {
+    if (tid == 0) {
+      p.plan[0] = n_pre;
+      p.plan[1] = Wp;
+      p.plan[2] = Ws;
+      p.plan[3] = kvgc;
+    }
+    for (int i = tid; i < B; i += kT) {
+      int* r = p.plan + kPlanHeader + 4 * i;
+      r[0] = sU[i];
+      r[1] = sU[i + 1] - sU[i];
+      r[2] = sG[i];
+      r[3] = sJ[i];
+    }
+    for (int g = tid; g < NG; g += kT) {
+      int* r = p.plan + kPlanHeader + 4 * B + 2 * g;
+      r[0] = sUp[g];
+      r[1] = sUp[g + 1] - sUp[g];
+    }
+  }
+  const int my_kvg = (int)blockIdx.x % kvgc;
+  const int ci = (int)blockIdx.x / kvgc;
+  if (ci >= Skv) return;  // past the last whole set of kvgc CTAs
+  const bool pre = kShared && ci < n_pre;
+  const int cidx = pre ? ci : ci - n_pre;
+  const int W = pre ? Wp : Ws;
+  const int T = pre ? Tp : Ts;
+  if ((long long)cidx * W >= T) return;  // no work for this CTA
+  const int u_begin = cidx * W;
+  const int u_end = (int)min((long long)T, (long long)u_begin + W);
+  const int* line_base = pre ? sUp : sU;
+  const int line_rows = pre ? NG : B;
+  const int* line_first = pre ? nullptr : sP;
+
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      // suffix line: one consumer warp per head reads a stage; prefix line: all
+      mbar_init(&empty_bar[s], pre ? C::kConsumerWarps : C::kHeads);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == C::kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    const uint64_t kv_policy = l2_evict_first_policy();  // the KV stream is read once
+    bool ok = true;
+    int issued = 0;
+    int it = 0;
+    for (int u = u_begin; u < u_end && ok;) {
+      Segment sg = segment_at(u, u_begin, u_end, line_base, line_rows, line_first);
+      sg.kvg = my_kvg;
+      int seq = sg.row;
+      if (pre) {
+        // the table of the group's first listed sequence (all members share these blocks)
+        const int o0 = min(max(p.grp_off[sg.row], 0), n_members);
+        const int o1 = min(max(p.grp_off[sg.row + 1], o0), min(n_members, o0 + max_members));
+        seq = -1;
+        for (int k = o0; k < o1 && seq < 0; ++k) {
+          const int s = p.grp_seq[k];
+          if (s >= 0 && s < B) seq = s;
+        }
+      } else if constexpr (kAppend) {
+        // append_kv for this sequence's new token: written by the CTA that
+        // reads the row's last block, before it loads it.
+        if (sg.row_end) {
+          const int L = min(max(p.context_lens[seq], 0), cap);
+          const int64_t slot = L > 0 ? p.slot_mapping[seq] : -1;
+          append_token<D, KV, QT>(p, seq, sg.kvg * C::kHeads, slot);
+        }
+      }
+      const int32_t* tbl = p.block_tables + (size_t)max(seq, 0) * p.max_blocks_per_seq + sg.b0;
+      const int kv0 = sg.kvg * C::kHeads;
+      for (int base = 0; base < sg.nblk; base += 32) {
+        const int mine = (base + lane < sg.nblk) ? __ldg(tbl + base + lane) : 0;
+        const int cnt = min(32, sg.nblk - base);
+        for (int j = 0; j < cnt; ++j) {
+          const int blk = __shfl_sync(0xffffffffu, mine, j);
+          if (lane == 0 && ok) {
+            const int s = it % C::kStages;
+            const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
+            if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u, p.status)) {
+              ok = false;
+              abort_flag = 1;
+            } else {
+              load_block<D, KV>(smem + s * C::kStageBytes, &tmap_k, &tmap_v, &full_bar[s], blk,
+                                p.num_blocks, kv0, kv_policy);
+              ++issued;
+            }
+          }
+          ++it;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+      u += sg.nblk;
+    }
+    griddep_launch_dependents();
+    // Never leave the CTA with copies in flight.
+    if (lane == 0) {
+      const int first = max(0, issued - C::kStages);
+      for (int k = first; k < issued; ++k) {
+        mbar_wait_bounded(&full_bar[k % C::kStages], (uint32_t)(k / C::kStages) & 1u, p.status);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int hsel = warp / C::kWarpsPerHead;
+  const int wq = warp % C::kWarpsPerHead;  // block phase (suffix) or n-tile (prefix)
+  const int g = lane >> 2;
+  const int t = lane & 3;
+  float* my_o = red_o + warp * 8 * C::kRedStride;
+  float* my_m = red_m + warp * 8;
+  float* my_l = red_l + warp * 8;
+  WarpState<D> st;
+  uint32_t qb[C::kMTiles][2];
+  int it0 = 0;
+
+  for (int u = u_begin; u < u_end;) {
+    Segment sg = segment_at(u, u_begin, u_end, line_base, line_rows, line_first);
+    sg.kvg = my_kvg;
+    const int kvh = sg.kvg * C::kHeads + hsel;
+    st.reset();
+    if (!pre) {
+      // ------------------------------------------------ suffix line
+      const int seq = sg.row;
+      const bool live = kvh < p.num_kv_heads && g < p.group;
+      load_q_frag<D, KV, QT>(qb, p.q,
+                             ((size_t)seq * p.num_q_heads + kvh * p.group + (live ? g : 0)) * D,
+                             live);
+      // tokens from the segment's first block to the context's end (the last
+      // block of a row may be partial)
+      const int seg_ntok = min(max(p.context_lens[seq], 0), cap) - 16 * sg.b0;
+      // block k of the segment sits at ring position it0 + k; this warp takes
+      // the positions that are wq mod 4, as in the fixed kernel
+      const bool aborted = *reinterpret_cast<volatile int*>(&abort_flag) != 0;
+      for (int k = (wq - it0) & (C::kWarpsPerHead - 1); k < sg.nblk && !aborted;
+           k += C::kWarpsPerHead) {
+        const int it = it0 + k;
+        const int s = it % C::kStages;
+        if (!mbar_wait_bounded(&full_bar[s], (uint32_t)(it / C::kStages) & 1u, p.status)) {
+          abort_flag = 1;
+          break;
+        }
+        const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
+        decode_block<D, KV, false>(st, qb, kbase, kbase + C::kTileBytes, hsel,
+                                   min(16, seg_ntok - 16 * k), p.scale_log2, 16, 16);
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+      }
+      finish_row_sums(st);
+      dump_state<D, KV>(st, my_o, my_m, my_l);
+      consumer_bar(kConsumerThreads);
+      // Merge each head's four warp states and write the segment's result.
+      const bool direct = sg.whole && sG[seq] < 0;
+      constexpr int kQuads = D / 4;
+      const int per_head = p.group * kQuads;
+      for (int idx = tid; idx < C::kHeads * per_head; idx += kConsumerThreads) {
+        const int hs = idx / per_head;
+        const int rem = idx - hs * per_head;
+        const int h = rem / kQuads;
+        const int d = (rem - h * kQuads) * 4;
+        const int kvh2 = sg.kvg * C::kHeads + hs;
+        if (kvh2 >= p.num_kv_heads) break;
+        const int w0 = hs * C::kWarpsPerHead;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = w0; w < w0 + C::kWarpsPerHead; ++w) M = fmaxf(M, red_m[w * 8 + h]);
+        float num[4] = {0.f, 0.f, 0.f, 0.f}, den = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = w0; w < w0 + C::kWarpsPerHead; ++w) {
+            const float wt = ex2_approx(__fsub_rn(red_m[w * 8 + h], M));
+            const float4 ov =
+                *reinterpret_cast<const float4*>(&red_o[(w * 8 + h) * C::kRedStride + d]);
+            num[0] = __fmaf_rn(wt, ov.x, num[0]);
+            num[1] = __fmaf_rn(wt, ov.y, num[1]);
+            num[2] = __fmaf_rn(wt, ov.z, num[2]);
+            num[3] = __fmaf_rn(wt, ov.w, num[3]);
+            den = __fmaf_rn(wt, red_l[w * 8 + h], den);
+          }
+        }
+        const int qh = kvh2 * p.group + h;
+        if (direct) {
+          float v[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            v[k] = (den > 0.f) ? __fmul_rn(__fdiv_rn(num[k], den), p.out_scale) : 0.f;
+          uint2 pk;
+          if constexpr (QT == kKvF16) {
+            pk.x = pack_f16x2(v[0], v[1]);
+            pk.y = pack_f16x2(v[2], v[3]);
+          } else {
+            pk.x = pack_bf16x2(v[0], v[1]);
+            pk.y = pack_bf16x2(v[2], v[3]);
+          }
+          *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) +
+                                    ((size_t)seq * p.num_q_heads + qh) * D + d) = pk;
+        } else {
+          size_t pi;
+          float *pm, *pl, *po;
+          if (sg.whole) {  // a member's whole suffix
+            pi = (size_t)B * p.num_q_heads + (size_t)seq * p.num_q_heads + qh;
+            pm = p.whole_m; pl = p.whole_l; po = p.whole_o;
+          } else {
+            pi = ((size_t)blockIdx.x * 2 + (sg.first ? 0 : 1)) * p.cut_cols + hs * p.group + h;
+            pm = p.cut_m; pl = p.cut_l; po = p.cut_o;
+          }
+          *reinterpret_cast<float4*>(po + pi * D + d) = make_float4(num[0], num[1], num[2], num[3]);
+          if (d == 0) {
+            pm[pi] = M;
+            pl[pi] = den;
+          }
+        }
+      }
+      consumer_bar(kConsumerThreads);  // the buffer is free for the next segment
+    } else {
+      // ------------------------------------------------ prefix line
+      const int o0 = min(max(p.grp_off[sg.row], 0), n_members);
+      const int o1 = min(max(p.grp_off[sg.row + 1], o0), min(n_members, o0 + max_members));
+      const int mcnt = o1 - o0;
+      const bool kv_live = kvh < p.num_kv_heads;
+      // B operand: this lane's column 8 wq + g -> member, query head of the group
+      const int cb = 8 * wq + g;
+      const int jb = cb / p.group;
+      const int sb = (jb < mcnt) ? p.grp_seq[o0 + jb] : -1;
+      const bool bl = kv_live && sb >= 0 && sb < B;
+      load_q_frag<D, KV, QT>(
+          qb, p.q, ((size_t)(bl ? sb : 0) * p.num_q_heads + kvh * p.group + cb % p.group) * D, bl);
+      // C columns 2t, 2t+1 of the n-tile: their members' context lengths
+      int lim[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int j = (8 * wq + 2 * t + c) / p.group;
+        const int s = (j < mcnt) ? p.grp_seq[o0 + j] : -1;
+        lim[c] = (s >= 0 && s < B && kv_live) ? min(max(p.context_lens[s], 0), cap) : -1;
+      }
+      // tokens past every live column's length are masked for the whole warp
+      int vmax = max(lim[0], lim[1]);
+#pragma unroll
+      for (int x = 1; x < 32; x <<= 1) vmax = max(vmax, __shfl_xor_sync(0xffffffffu, vmax, x));
+      const int seg_tok_end = 16 * (sg.b0 + sg.nblk);
+      // a dead column (no member) keeps q = 0 and is never stored: no mask needed
+      const int l0c = lim[0] < 0 ? (1 << 30) : lim[0];
+      const int l1c = lim[1] < 0 ? (1 << 30) : lim[1];
+      const bool need_mask = __any_sync(0xffffffffu, l0c < seg_tok_end || l1c < seg_tok_end);
+      const bool aborted = *reinterpret_cast<volatile int*>(&abort_flag) != 0;
+      for (int k = 0; k < sg.nblk && !aborted; ++k) {
+        const int it = it0 + k;
+        const int s = it % C::kStages;
+        if (!mbar_wait_bounded(&full_bar[s], (uint32_t)(it / C::kStages) & 1u, p.status)) {
+          abort_flag = 1;
+          break;
+        }
+        const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
+        const int tok0 = 16 * (sg.b0 + k);
+        const int valid = min(16, vmax - tok0);
+        if (need_mask) {
+          decode_block<D, KV, true>(st, qb, kbase, kbase + C::kTileBytes, hsel, valid,
+                                    p.scale_log2, l0c - tok0, l1c - tok0);
+        } else {
+          decode_block<D, KV, false>(st, qb, kbase, kbase + C::kTileBytes, hsel, valid,
+                                     p.scale_log2, 16, 16);
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+      }
+      finish_row_sums(st);
+      // this warp's 8 columns -> their members' partials
+      dump_state<D, KV>(st, my_o, my_m, my_l);
+      __syncwarp();
+      for (int c = 0; c < 8; ++c) {
+        const int col = 8 * wq + c;
+        const int j = col / p.group;
+        if (j >= mcnt || !kv_live) break;  // later columns are past the members too
+        const int s = p.grp_seq[o0 + j];
+        if (s < 0 || s >= B) continue;
+        const int qh = kvh * p.group + col % p.group;
+        size_t pi;
+        float *pm, *pl, *po;
+        if (sg.whole) {
+          pi = (size_t)s * p.num_q_heads + qh;
+          pm = p.whole_m; pl = p.whole_l; po = p.whole_o;
+        } else {
+          pi = ((size_t)blockIdx.x * 2 + (sg.first ? 0 : 1)) * p.cut_cols + hsel * kPrefixCols + col;
+          pm = p.cut_m; pl = p.cut_l; po = p.cut_o;
+        }
+        if (lane < D / 4) {
+          const float4 ov = *reinterpret_cast<const float4*>(&my_o[c * C::kRedStride + 4 * lane]);
+          *reinterpret_cast<float4*>(po + pi * D + 4 * lane) = ov;
+        }
+        if (lane == 0) {
+          pm[pi] = my_m[c];
+          pl[pi] = my_l[c];
+        }
+      }
+      __syncwarp();
+    }
+    it0 += sg.nblk;
+    u += sg.nblk;
+  }
+  griddep_launch_dependents();
+}
+
+// Log-sum-exp merge for the stream-K split: one warp per (sequence, query
+// head), kSplitMergeWarps of them per CTA.  From the plan it lists the
+// partials covering the sequence's context (its suffix: one whole partial, or
+// the cut partials of the CTAs whose ranges meet its row; its shared prefix,
+// if any, the same way on the prefix line).  Lanes resolve and load 32 of the
+// partials' (m, l) at once; every lane then folds its D/32 head_size elements
+// of each partial's O row (coalesced loads) into a running maximum, in list
+// order, so the result does not depend on timing.  A sequence whose whole
+// context one CTA wrote directly is skipped.
+constexpr int kSplitMergeWarps = 8;
+
+template <int D, int QT, int H>
+__global__ void __launch_bounds__(kSplitMergeWarps * 32)
+    paged_decode_split_merge_kernel(const DecodeParams p) {
+  constexpr int kPer = D / 32;  // head_size elements per lane
+  const int lane = threadIdx.x & 31;
+  const int idx = blockIdx.x * kSplitMergeWarps + (threadIdx.x >> 5);  // sequence * Hq + head
+  if (idx >= p.num_seqs * p.num_q_heads) return;
+  const int seq = idx / p.num_q_heads;
+  const int h = idx - seq * p.num_q_heads;
+  griddep_wait();  // the plan and the partials come from the attention kernel
+  const int* plan = p.plan;
+  const int n_pre = plan[0];
+  const int Wp = plan[1], Ws = plan[2];
+  const int kvgc = plan[3];
+  const int* rec = plan + kPlanHeader + 4 * seq;
+  const int U = rec[0], nsuf = rec[1], grp = rec[2], mem = rec[3];
+  const int G = p.group;
+  const int kvh = h / G;
+  const int kvg = kvh / H;
+  const int hs = kvh - kvg * H;
+  const int gh = h - kvh * G;
+
+  // suffix partials
+  const int s_start = U;
+  int ns = 0, s_c0 = 0;
+  bool s_whole = false;
+  if (nsuf > 0) {
+    s_c0 = s_start / Ws;
+    const int c1 = (s_start + nsuf - 1) / Ws;
+    if (s_c0 == c1) {
+      if (grp < 0) return;  // written directly by the attention kernel
+      s_whole = true;
+      ns = 1;
+    } else {
+      ns = c1 - s_c0 + 1;
+    }
+  }
+  // shared-prefix partials
+  int np = 0, p_start = 0, p_c0 = 0;
+  bool p_whole = false;
+  if (grp >= 0) {
+    const int* grec = plan + kPlanHeader + 4 * p.num_seqs + 2 * grp;
+    const int npre = grec[1];
+    if (npre > 0) {
+      p_start = grec[0];
+      p_c0 = p_start / Wp;
+      const int c1 = (p_start + npre - 1) / Wp;
+      if (p_c0 == c1) {
+        p_whole = true;
+        np = 1;
+      } else {
+        np = c1 - p_c0 + 1;
+      }
+    }
+  }
+  const size_t BH = (size_t)p.num_seqs * p.num_q_heads;
+  const int K = ns + np;
+  float M = -INFINITY, den = 0.f;
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  for (int base = 0; base < K; base += 32) {
+    // lane k of this chunk: partial base + k -> its (m, l) and O row
+    const int k = base + lane;
+    float mk = -INFINITY, lk = 0.f;
+    const float* ok = p.cut_o;
+    if (k < K) {
+      const float *pm, *pl, *po;
+      size_t pi;
+      if (k < ns) {
+        if (s_whole) {
+          pi = BH + (size_t)seq * p.num_q_heads + h;
+          pm = p.whole_m; pl = p.whole_l; po = p.whole_o;
+        } else {
+          const int c = s_c0 + k;
+          const int slot = (c * Ws >= s_start) ? 0 : 1;
+          pi = (((size_t)(n_pre + c) * kvgc + kvg) * 2 + slot) * p.cut_cols + hs * G + gh;
+          pm = p.cut_m; pl = p.cut_l; po = p.cut_o;
+        }
+      } else if (p_whole) {
+        pi = (size_t)seq * p.num_q_heads + h;
+        pm = p.whole_m; pl = p.whole_l; po = p.whole_o;
+      } else {
+        const int c = p_c0 + (k - ns);
+        const int slot = (c * Wp >= p_start) ? 0 : 1;
+        pi = (((size_t)c * kvgc + kvg) * 2 + slot) * p.cut_cols + hs * kPrefixCols + mem * G + gh;
+        pm = p.cut_m; pl = p.cut_l; po = p.cut_o;
+      }
+      mk = pm[pi];
+      lk = pl[pi];
+      ok = po + pi * D;
+    }
+    float cmax = mk;
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, x));
+    const float Mn = fmaxf(M, cmax);
+    if (Mn == -INFINITY) continue;  // nothing but empty partials so far
+    const float sc = ex2_approx(__fsub_rn(M, Mn));  // 0 while M is -inf
+    den = __fmul_rn(den, sc);
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = __fmul_rn(acc[e], sc);
+    const float wk = ex2_approx(__fsub_rn(mk, Mn));  // 0 for lanes past K
+    float dl = __fmul_rn(wk, lk);
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) dl = __fadd_rn(dl, __shfl_xor_sync(0xffffffffu, dl, x));
+    den = __fadd_rn(den, dl);
+    // O rows 8 at a time: all eight loads are issued before any is used
+    const int cnt = min(32, K - base);
+    for (int j0 = 0; j0 < cnt; j0 += 8) {
+      float w8[8];
+      float row8[8][kPer];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int jj = min(j0 + j, cnt - 1);
+        w8[j] = (j0 + j < cnt) ? __shfl_sync(0xffffffffu, wk, jj) : 0.f;
+        const float* row = reinterpret_cast<const float*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(ok), jj));
+        if constexpr (kPer == 4) {
+          const float4 v = reinterpret_cast<const float4*>(row)[lane];
+          row8[j][0] = v.x; row8[j][1] = v.y; row8[j][2] = v.z; row8[j][3] = v.w;
+        } else {
+          const float2 v = reinterpret_cast<const float2*>(row)[lane];
+          row8[j][0] = v.x; row8[j][1] = v.y;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j0 + j < cnt) {
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) acc[e] = __fmaf_rn(w8[j], row8[j][e], acc[e]);
+        }
+      }
+    }
+    M = Mn;
+  }
+  float v[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e)
+    v[e] = (den > 0.f) ? __fmul_rn(__fdiv_rn(acc[e], den), p.out_scale) : 0.f;
+  uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + (size_t)idx * D + lane * kPer;
+  if constexpr (kPer == 4) {
+    uint2 pk;
+    if constexpr (QT == kKvF16) {
+      pk.x = pack_f16x2(v[0], v[1]);
+      pk.y = pack_f16x2(v[2], v[3]);
+    } else {
+      pk.x = pack_bf16x2(v[0], v[1]);
+      pk.y = pack_bf16x2(v[2], v[3]);
+    }
+    *reinterpret_cast<uint2*>(dst) = pk;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) =
+        (QT == kKvF16) ? pack_f16x2(v[0], v[1]) : pack_bf16x2(v[0], v[1]);
+  }
+}
+
+}  // namespace pa

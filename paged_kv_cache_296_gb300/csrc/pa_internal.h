@@ -8,6 +8,14 @@
 
 namespace pa {
 
+// Stream-K split (pa_decode_split.cuh): limits the host checks before choosing it.
+constexpr int kMaxSplitCtas = 1024;   // grid cap; cut partials are sized for it
+constexpr int kMaxPlanSeqs = 1024;    // sequences in one stream-K call
+constexpr int kMaxPlanGroups = 1024;  // shared-prefix groups in one call
+constexpr int kPrefixCols = 32;       // MMA columns per KV head on the prefix line
+constexpr int kPlanHeader = 8;        // ints before the per-sequence plan records
+constexpr int kMaxSplitHeads = 2;     // KV heads per CTA of any instantiation (E4M3)
+
 // Everything one pa_decode launch needs, already validated by the caller.
 struct DecodeArgs {
   void* out;
@@ -26,11 +34,10 @@ struct DecodeArgs {
   int kv_dtype;  // 0 f16, 1 bf16, 2 e4m3
   float scale;
   float kv_scale;
-  int partition_tokens;      // 0: balanced split chosen in the kernel (>= min_partition_tokens)
-  int min_partition_tokens;
-  int num_partitions;        // grid partitions: an upper bound in the balanced mode
-  int* plan;                 // balanced mode: where the kernel records its choice
-  float* part_m;
+  int partition_tokens;      // > 0: fixed partitions; 0: stream-K split chosen in the kernel
+  int min_partition_tokens;  // stream-K: the smallest range a CTA takes
+  int num_partitions;        // fixed partitions: grid partitions per sequence
+  float* part_m;             // fixed partitions: partials [B, Hq, P]
   float* part_l;
   float* part_o;
   unsigned* status;
@@ -40,6 +47,19 @@ struct DecodeArgs {
   const void* v_new;
   const int64_t* slot_mapping;
   int64_t src_stride_bytes;
+  // stream-K: shared-prefix groups (num_groups == 0: none) and the partials
+  const int32_t* grp_off;
+  const int32_t* grp_seq;
+  const int32_t* grp_blocks;
+  int num_groups;
+  int cut_cols;
+  float* cut_m;
+  float* cut_l;
+  float* cut_o;
+  float* whole_m;
+  float* whole_l;
+  float* whole_o;
+  int* plan;
 };
 
 // Per-dtype decode launchers (one translation unit each, compiled in parallel).

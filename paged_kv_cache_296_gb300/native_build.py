@@ -20,7 +20,8 @@ LIB = os.path.join(LIBDIR, "libpagedattn.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["pa_api.cu", "pa_cache.cu", "pa_decode_f16.cu", "pa_decode_bf16.cu", "pa_decode_e4m3.cu",
-           "pa_noalloc.cu", "pa_prefill.cu", "pa_prefill_fp8.cu", "pa_block_manager.cpp"]
+           "pa_noalloc.cu", "pa_prefill.cu", "pa_prefill_fp8.cu", "pa_block_manager.cpp",
+           "pa_shared.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

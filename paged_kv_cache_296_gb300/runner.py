@@ -28,9 +28,15 @@ def fill_fp8_pool(pool_src, kv_scale, device, rows_per_call=1 << 16):
 
 
 class DecodeStep:
-    """Device buffers for one workload plus the step that runs on them."""
+    """Device buffers for one workload plus the step that runs on them.
 
-    def __init__(self, W, device="cuda", partition_size=0):
+    ``shared``: decode with shared-prefix groups (pa_decode_shared /
+    pa_decode_append_shared), each shared block read once for all the
+    sequences whose tables hold it.  "auto" (the default) uses them when the
+    tables have any (pa_find_shared_prefixes on the host copy of the tables).
+    """
+
+    def __init__(self, W, device="cuda", partition_size=0, shared="auto"):
         self.W = W
         self.device = torch.device(device)
         spec = W.spec
@@ -49,16 +55,42 @@ class DecodeStep:
         self.out = torch.empty_like(self.q)
         self.partition_size = partition_size
         B, hq, d = self.q.shape
-        self.partition_tokens = pa.pa_decode_partition_size(
-            B, spec.num_kv_heads, W.max_blocks_per_seq, BLOCK_SIZE, partition_size)
-        self.workspace = pa.alloc_workspace(
-            pa.pa_decode_workspace_size(B, hq, spec.num_kv_heads, d, W.max_blocks_per_seq,
-                                        BLOCK_SIZE, partition_size), self.device)
+        groups = None
+        if shared:
+            groups = pa.pa_find_shared_prefixes(W.block_tables, W.context_lens, hq,
+                                                spec.num_kv_heads)
+            if groups.num_groups == 0:
+                if shared != "auto":
+                    raise ValueError("shared=True but the tables share no leading blocks")
+                groups = None
+        self.shared = groups is not None
+        self.step_inputs = self.STEP_INPUTS
+        if self.shared:
+            self.grp_off = groups.offsets.to(self.device)
+            self.grp_seq = groups.seqs.to(self.device)
+            self.grp_blocks = groups.blocks.to(self.device)
+            self.num_groups = groups.num_groups
+            self.step_inputs = self.STEP_INPUTS + ("grp_off", "grp_seq", "grp_blocks")
+            self.partition_tokens = 0
+            nbytes = pa.pa_decode_shared_workspace_size(B, hq, spec.num_kv_heads, d,
+                                                        W.max_blocks_per_seq, BLOCK_SIZE,
+                                                        self.num_groups)
+        else:
+            self.partition_tokens = pa.pa_decode_partition_size(
+                B, spec.num_kv_heads, W.max_blocks_per_seq, BLOCK_SIZE, partition_size)
+            nbytes = pa.pa_decode_workspace_size(B, hq, spec.num_kv_heads, d,
+                                                 W.max_blocks_per_seq, BLOCK_SIZE, partition_size)
+        self.workspace = pa.alloc_workspace(nbytes, self.device)
         self.kv_scale = W.kv_scale
         self.scale = W.scale
 
-    #: The step's per-call inputs, in the order they are packed by :meth:`stage_inputs`.
+    #: The step's per-call inputs, in the order they are packed by :meth:`stage_inputs`
+    #: (a shared-prefix step adds its three group arrays).
     STEP_INPUTS = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+
+    @property
+    def groups(self):
+        return pa.SharedGroups(self.grp_off, self.grp_seq, self.grp_blocks) if self.shared else None
 
     def stage_inputs(self):
         """Pack the per-step inputs into one device buffer and a pinned host twin.
@@ -70,13 +102,14 @@ class DecodeStep:
         already holds the current inputs.
         """
         align = lambda n: (n + 255) // 256 * 256
-        tensors = [getattr(self, k) for k in self.STEP_INPUTS]
+        names = getattr(self, "step_inputs", self.STEP_INPUTS)
+        tensors = [getattr(self, k) for k in names]
         sizes = [t.numel() * t.element_size() for t in tensors]
         total = sum(align(n) for n in sizes)
         dev = torch.empty(total, dtype=torch.uint8, device=self.device)
         host = torch.empty(total, dtype=torch.uint8).pin_memory()
         off = 0
-        for name, t, n in zip(self.STEP_INPUTS, tensors, sizes):
+        for name, t, n in zip(names, tensors, sizes):
             view = dev[off:off + n].view(t.dtype).view(t.shape)
             view.copy_(t)
             host[off:off + n].copy_(view.view(torch.uint8).reshape(-1).cpu())
@@ -88,16 +121,23 @@ class DecodeStep:
         """Kernels one step enqueues.
 
         "append": one (token write + attention), plus the merge kernel when a
-        sequence can span more than one partition.  "separate": the write
-        kernel, then the same.
+        sequence can span more than one partition (always with the stream-K
+        split).  "separate": the write kernel, then the same.
         """
         max_tokens = self.W.max_blocks_per_seq * BLOCK_SIZE
-        split = self.partition_tokens == 0 or max_tokens > self.partition_tokens   # 0: balanced
+        split = self.partition_tokens == 0 or max_tokens > self.partition_tokens   # 0: stream-K
         n = 1 + (1 if split else 0)
         return n + (1 if path == "separate" else 0)
 
     def append(self):
-        """The whole step in one call: pa_decode_append."""
+        """The whole step in one call: pa_decode_append (or its shared-prefix form)."""
+        if self.shared:
+            pa.pa_decode_append_shared(self.out, self.q, self.k_new, self.v_new,
+                                       self.slot_mapping, self.k_cache, self.v_cache,
+                                       self.block_tables, self.context_lens, self.scale,
+                                       self.groups, kv_scale=self.kv_scale,
+                                       workspace=self.workspace)
+            return self.out
         pa.pa_decode_append(self.out, self.q, self.k_new, self.v_new, self.slot_mapping,
                             self.k_cache, self.v_cache, self.block_tables, self.context_lens,
                             self.scale, kv_scale=self.kv_scale,
@@ -109,6 +149,11 @@ class DecodeStep:
                                 self.slot_mapping, kv_scale=self.kv_scale)
 
     def decode(self):
+        if self.shared:
+            pa.pa_decode_shared(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
+                                self.context_lens, self.scale, self.groups,
+                                kv_scale=self.kv_scale, workspace=self.workspace)
+            return
         pa.pa_decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
                      self.context_lens, self.scale, kv_scale=self.kv_scale,
                      partition_size=self.partition_size, workspace=self.workspace)

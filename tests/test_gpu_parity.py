@@ -349,7 +349,7 @@ def test_shared_prefix_equals_private_copies_bitwise():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-@pytest.mark.parametrize("n", [2, 3, 5])
+@pytest.mark.parametrize("n", [2, 3, 4, 5])
 def test_run_to_run_bitwise_deterministic(n):
     """Repeated decodes of one device state give identical bits, the first run
     after set-up included (a stage refilled by TMA while still being read
@@ -401,7 +401,7 @@ def test_check_tables_counts_bad_indices():
 def _append_step(W, partition_size=0, workspace=None):
     """pa_decode_append on a fresh device copy of W; returns (out, pool)."""
     from paged_kv_cache_296_gb300.runner import DecodeStep
-    S = DecodeStep(W, device="cuda", partition_size=partition_size)
+    S = DecodeStep(W, device="cuda", partition_size=partition_size, shared=False)
     pa.pa_decode_append(S.out, S.q, S.k_new, S.v_new, S.slot_mapping, S.k_cache, S.v_cache,
                         S.block_tables, S.context_lens, S.scale, kv_scale=S.kv_scale,
                         partition_size=partition_size,
@@ -410,8 +410,9 @@ def _append_step(W, partition_size=0, workspace=None):
 
 
 def _separate_step(W, partition_size=0):
+    """pa_reshape_and_cache then pa_decode (no shared-prefix groups); returns (out, pool)."""
     from paged_kv_cache_296_gb300.runner import DecodeStep
-    S = DecodeStep(W, device="cuda", partition_size=partition_size)
+    S = DecodeStep(W, device="cuda", partition_size=partition_size, shared=False)
     S.write()
     S.decode()
     return S.out, S.pool
