@@ -67,16 +67,17 @@ bool split_fits(int num_seqs, int num_kv_heads, int max_blocks_per_seq, int num_
              (1LL << 31);
 }
 
-// Split-KV partition size (tokens), 0 for the stream-K split, or -1 when the
+// Split-KV partition size (tokens), 0 for a balanced split, or -1 when the
 // request is invalid.  A request of 0 decides from the batch shape alone (no
 // device query, so the host-side sizing calls agree with pa_decode everywhere):
 //   * with >= kTargetPairs (sequence, KV head) pairs there are enough CTAs
 //     already: no split, except that no partition exceeds kMaxPartitionTokens
 //     (bounds the slowest CTA);
-//   * otherwise the stream-K split (returned as 0): the decode kernel reads the
-//     actual context lengths and gives every CTA of one wave an equal range
-//     of (sequence, KV head group, block) units, at least kMinPartitionTokens
-//     of them, so every SM streams from the start to the end.
+//   * otherwise a balanced split (returned as 0): the decode kernel reads the
+//     actual context lengths and picks the smallest partition size, at least
+//     kMinPartitionTokens, whose partitions over all sequences and KV heads
+//     fit in one wave of resident CTAs, so every SM streams from the start to
+//     the end and the longest CTA is as short as that allows.
 // Measured on GB300: a CTA streams about its ring (64 KB) per loaded memory
 // latency (~3.5 us), so a batch of a few long sequences must be split, and a
 // split that spills into a second wave leaves a long tail.
@@ -85,29 +86,31 @@ int partition_tokens(int num_seqs, int num_kv_heads, int max_blocks_per_seq, int
   if (requested > 0) return requested;
   const long long max_tokens = (long long)max_blocks_per_seq * kBlockSize;
   const long long pairs = std::max(1LL, (long long)num_seqs * std::max(1, num_kv_heads));
-  if (pairs >= kTargetPairs || !split_fits(num_seqs, num_kv_heads, max_blocks_per_seq, 0)) {
+  if (pairs >= kTargetPairs) {
     return (int)std::max<long long>(kBlockSize, std::min<long long>(max_tokens, kMaxPartitionTokens));
   }
   if (max_tokens <= kMinPartitionTokens) return (int)std::max<long long>(kBlockSize, max_tokens);
   return 0;
 }
 
-// Partitions of the grid (per sequence and KV head) for a fixed partition size.
+// Partitions of the grid (per sequence and KV head) for a partition size from
+// partition_tokens(); for a balanced split, enough for its smallest size.
 int num_partitions(int max_blocks_per_seq, int part_tokens) {
-  if (part_tokens <= 0) return 0;  // stream-K: no per-sequence partitions
   const long long max_tokens = (long long)max_blocks_per_seq * kBlockSize;
-  const long long p = (max_tokens + part_tokens - 1) / part_tokens;
+  const long long unit = part_tokens > 0 ? part_tokens : kMinPartitionTokens;
+  const long long p = (max_tokens + unit - 1) / unit;
   return (int)(p < 1 ? 1 : p);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Split-KV workspace.  Fixed partitions: partial m, l, O per (sequence, query
-// head, partition).  Stream-K: "cut" partials per (CTA, slot, column) for at
-// most kMaxSplitCtas CTAs of up to kMaxSplitHeads KV heads (columns: the
-// heads' query heads, or kPrefixCols per head with shared-prefix groups),
-// "whole" partials per (sequence, query head) for the prefix and the suffix
-// of group members, and the kernel's plan for the merge kernel.
+// Split-KV workspace.  Partitions (given or balanced): partial m, l, O per
+// (sequence, query head, partition), then 256 bytes where a balanced split
+// records its partition size.  Shared prefixes (the stream-K kernel): "cut"
+// partials per (CTA, slot, column) for at most kMaxSplitCtas CTAs of up to
+// kMaxSplitHeads KV heads (kPrefixCols columns per head), "whole" partials per
+// (sequence, query head) for the prefix and the suffix of group members, and
+// the kernel's plan for the merge kernel.
 struct WorkspaceLayout {
   size_t m_off, l_off, o_off;              // fixed partitions or cut partials
   size_t wm_off, wl_off, wo_off;           // whole partials (groups only)
@@ -115,13 +118,12 @@ struct WorkspaceLayout {
   int cut_cols;
 };
 
-WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
-                                 int nparts, bool split, int num_groups) {
+WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_size, int nparts,
+                                 bool split, int num_groups) {
   WorkspaceLayout w{0, 0, 0, 0, 0, 0, 0, 0, 0};
   size_t rows = 0;
   if (split) {
-    const int g = num_q_heads / std::max(1, num_kv_heads);
-    w.cut_cols = pa::kMaxSplitHeads * (num_groups > 0 ? pa::kPrefixCols : g);
+    w.cut_cols = pa::kMaxSplitHeads * pa::kPrefixCols;
     rows = (size_t)pa::kMaxSplitCtas * 2 * w.cut_cols;
   } else {
     if (nparts <= 1) return w;
@@ -131,7 +133,7 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads
   w.l_off = align256(rows * sizeof(float));
   w.o_off = w.l_off + align256(rows * sizeof(float));
   size_t end = w.o_off + align256(rows * head_size * sizeof(float));
-  if (split && num_groups > 0) {
+  if (split) {
     const size_t wrows = 2 * (size_t)num_seqs * num_q_heads;
     w.wm_off = end;
     w.wl_off = w.wm_off + align256(wrows * sizeof(float));
@@ -140,7 +142,7 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads
   }
   w.plan_off = end;
   const size_t plan_ints =
-      split ? (size_t)pa::kPlanHeader + 4 * (size_t)num_seqs + 2 * (size_t)num_groups : 64;
+      split ? (size_t)pa::kPlanHeader + pa::kPlanSeqInts * (size_t)num_seqs : 64;
   w.total = w.plan_off + align256(plan_ints * sizeof(int));
   return w;
 }
@@ -214,9 +216,10 @@ pa_status decode_impl(const char* fn, void* out, const void* q, const void* k_ca
     return fail(PA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an E4M3 cache");
   int part;
   int num_groups = 0;
-  if (grp) {
+  if (grp && grp->num_groups < 0)
+    return fail(PA_ERR_INVALID_ARG, "num_groups must be >= 0 (got %d)", grp->num_groups);
+  if (grp && grp->num_groups > 0) {
     num_groups = grp->num_groups;
-    if (num_groups < 0) return fail(PA_ERR_INVALID_ARG, "num_groups must be >= 0 (got %d)", num_groups);
     if (!split_fits(num_seqs, num_kv_heads, max_blocks_per_seq, num_groups))
       return fail(PA_ERR_UNSUPPORTED,
                   "%s: at most %d sequences and %d groups, and fewer than 2^31 blocks over all "
@@ -227,7 +230,7 @@ pa_status decode_impl(const char* fn, void* out, const void* q, const void* k_ca
     if ((reinterpret_cast<uintptr_t>(grp->offsets) | reinterpret_cast<uintptr_t>(grp->seqs) |
          reinterpret_cast<uintptr_t>(grp->blocks)) & 3u)
       return fail(PA_ERR_INVALID_ARG, "group arrays must be 4-byte aligned");
-    part = 0;  // the stream-K kernel serves the groups
+    part = 0;  // the shared-prefix (stream-K) kernel serves the groups
   } else {
     part = partition_tokens(num_seqs, num_kv_heads, max_blocks_per_seq, partition_size);
     if (part < 0)
@@ -236,9 +239,8 @@ pa_status decode_impl(const char* fn, void* out, const void* q, const void* k_ca
   }
   const int np = num_partitions(max_blocks_per_seq, part);
   if (np > 65535) return fail(PA_ERR_UNSUPPORTED, "too many partitions (%d)", np);
-  const bool split = part == 0;
-  const WorkspaceLayout ws =
-      workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_size, np, split, num_groups);
+  const bool split = num_groups > 0;  // the shared-prefix kernel
+  const WorkspaceLayout ws = workspace_layout(num_seqs, num_q_heads, head_size, np, split, num_groups);
   if (num_seqs == 0) return ok();
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
     return fail(PA_ERR_INVALID_ARG, "null pointer argument");
@@ -295,10 +297,10 @@ pa_status decode_impl(const char* fn, void* out, const void* q, const void* k_ca
   a.cut_l = split ? at(ws.l_off) : nullptr;
   a.cut_o = split ? at(ws.o_off) : nullptr;
   a.cut_cols = ws.cut_cols;
-  a.whole_m = split && num_groups ? at(ws.wm_off) : nullptr;
-  a.whole_l = split && num_groups ? at(ws.wl_off) : nullptr;
-  a.whole_o = split && num_groups ? at(ws.wo_off) : nullptr;
-  a.plan = split ? reinterpret_cast<int*>(wsb + ws.plan_off) : nullptr;
+  a.whole_m = split ? at(ws.wm_off) : nullptr;
+  a.whole_l = split ? at(ws.wl_off) : nullptr;
+  a.whole_o = split ? at(ws.wo_off) : nullptr;
+  a.plan = ws.total ? reinterpret_cast<int*>(wsb + ws.plan_off) : nullptr;
   a.grp_off = grp && num_groups ? grp->offsets : nullptr;
   a.grp_seq = grp && num_groups ? grp->seqs : nullptr;
   a.grp_blocks = grp && num_groups ? grp->blocks : nullptr;
@@ -500,7 +502,7 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
     return 0;
   }
   const int np = num_partitions(max_blocks_per_seq, part);
-  return workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_size, np, part == 0, 0).total;
+  return workspace_layout(num_seqs, num_q_heads, head_size, np, false, 0).total;
 }
 
 size_t pa_decode_shared_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
@@ -512,8 +514,10 @@ size_t pa_decode_shared_workspace_size(int num_seqs, int num_q_heads, int num_kv
     fail(PA_ERR_INVALID_ARG, "invalid arguments to pa_decode_shared_workspace_size");
     return 0;
   }
-  return workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_size, 0, true, num_groups)
-      .total;
+  if (num_groups == 0)  // the call is pa_decode's library choice
+    return pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_size,
+                                    max_blocks_per_seq, block_size, 0);
+  return workspace_layout(num_seqs, num_q_heads, head_size, 0, true, num_groups).total;
 }
 
 int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_blocks_per_seq,

@@ -36,9 +36,10 @@
 // permutation is applied to q, so the dot product is unchanged) and the
 // head_size index of V maps to output rows in a lane-contiguous order.
 //
-// This header holds the fixed-partition kernel (partitions of a given size,
-// grid (KV head groups, partitions, sequences)) and the per-block step, query
-// fragment load and fused token write that the stream-K kernel
+// This header holds the partition kernel (partitions of a given size, grid
+// (KV head groups, partitions, sequences), or a balanced split of one wave
+// planned in the kernel from the lengths) and the per-block step, query
+// fragment load and fused token write that the shared-prefix kernel
 // (pa_decode_split.cuh) shares with it, so both compute with the same bits.
 #pragma once
 
@@ -64,7 +65,12 @@ struct DecodeParams {
   int num_kv_heads;
   int kv_groups;                // CTAs per (sequence, partition): ceil(num_kv_heads / H)
   int group;                    // G = Hq / Hkv, 1..8
-  int partition_blocks;         // partition size in 16-token blocks (fixed kernel)
+  int partition_blocks;         // partition size in 16-token blocks; 0 = balanced (below)
+  // Balanced split: the partition size is chosen in the kernel from the actual
+  // context lengths, as the smallest one (>= min_partition_blocks) whose
+  // partitions over all sequences and KV heads fit in `slots` resident CTAs.
+  int min_partition_blocks;
+  int slots;
   int num_partitions;           // P = partitions of the longest possible sequence
   float scale_log2;             // scale * log2(e) (* kv_scale for E4M3)
   float out_scale;              // kv_scale for E4M3, else 1
@@ -89,7 +95,8 @@ struct DecodeParams {
   float* whole_m;               // [2][B][Hq] (shared-prefix mode only)
   float* whole_l;
   float* whole_o;               // [2][B][Hq][D]
-  int* plan;                    // the attention kernel's plan, for the merge kernel
+  int* plan;                    // the attention kernel's plan (balanced: its partition
+                                // size; stream-K: the plan record), for the merge kernel
 };
 
 
@@ -412,6 +419,34 @@ __device__ __forceinline__ void dump_state(const WarpState<D>& st, float* red_o,
   }
 }
 
+// Eight source elements (16 bytes of q's dtype) to eight E4M3 codes:
+// e4m3_rn_satfinite(x / kv_scale), x widened exactly to fp32, an IEEE division.
+template <int QT>
+__device__ __forceinline__ uint2 quantize8_e4m3(uint4 u, float kv_scale) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  float x[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (QT == kKvF16) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    } else {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+  uint32_t q8[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint16_t a = f32x2_to_e4m3x2(__fdiv_rn(x[4 * h], kv_scale), __fdiv_rn(x[4 * h + 1], kv_scale));
+    const uint16_t b =
+        f32x2_to_e4m3x2(__fdiv_rn(x[4 * h + 2], kv_scale), __fdiv_rn(x[4 * h + 3], kv_scale));
+    q8[h] = (uint32_t)a | ((uint32_t)b << 16);
+  }
+  return make_uint2(q8[0], q8[1]);
+}
+
 // append_kv for one sequence's new token, KV heads kv0 .. kv0+H-1, by the
 // calling warp: the same bytes pa_reshape_and_cache writes (a copy for a
 // 16-bit cache, e4m3_rn_satfinite(x / kv_scale) for E4M3), then a proxy fence
@@ -442,36 +477,68 @@ __device__ __forceinline__ void append_token(const DecodeParams& p, int seq, int
           const bool isv = lane >= kGrp;
           const int j = isv ? lane - kGrp : lane;
           const uint4 u = reinterpret_cast<const uint4*>((isv ? p.v_new : p.k_new) + src)[j];
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-          float x[8];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if constexpr (QT == kKvF16) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-              x[2 * i] = f.x;
-              x[2 * i + 1] = f.y;
-            } else {
-              x[2 * i] = __uint_as_float(w[i] << 16);
-              x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-            }
-          }
-          uint32_t q8[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint16_t a = f32x2_to_e4m3x2(__fdiv_rn(x[4 * h], p.kv_scale),
-                                               __fdiv_rn(x[4 * h + 1], p.kv_scale));
-            const uint16_t b = f32x2_to_e4m3x2(__fdiv_rn(x[4 * h + 2], p.kv_scale),
-                                               __fdiv_rn(x[4 * h + 3], p.kv_scale));
-            q8[h] = (uint32_t)a | ((uint32_t)b << 16);
-          }
           reinterpret_cast<uint2*>((isv ? p.v_cache : p.k_cache) + dst)[j] =
-              make_uint2(q8[0], q8[1]);
+              quantize8_e4m3<QT>(u, p.kv_scale);
         }
       }
       fence_proxy_async_global();
     }
   }
   __syncwarp();
+}
+
+// append_kv for the new tokens of `nrows` sequences (rows[]), KV heads kv0 ..
+// kv0+H-1, by `nthreads` threads (thread index `tid`): the same bytes as
+// append_token, each thread taking 16-byte source pieces in turn, four at a
+// time with all four loads issued before any store; then a proxy fence, so
+// TMA loads issued after a barrier that follows observe the writes.
+template <int D, int KV, int QT>
+__device__ __forceinline__ void append_rows(const DecodeParams& p, const int* rows, int nrows,
+                                            int kv0, int tid, int nthreads) {
+  using C = DecodeCfg<D, KV>;
+  constexpr int kUnits = D / 8;  // 16-byte source pieces per head row (8 elements)
+  constexpr int kPerRow = C::kHeads * 2 * kUnits;
+  constexpr int kBatch = 4;
+  constexpr int kDstPiece = (KV == kKvE4m3) ? 8 : 16;
+  const int total = nrows * kPerRow;
+  const int64_t pool_rows = (int64_t)p.num_blocks * 16;
+  for (int base = tid; base < total; base += kBatch * nthreads) {
+    uint4 x[kBatch];
+    uint8_t* dst[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int i = base + b * nthreads;
+      dst[b] = nullptr;
+      if (i < total) {
+        const int r = i / kPerRow;
+        const int rem = i - r * kPerRow;
+        const int hh = rem / (2 * kUnits);
+        const int isv = (rem - hh * 2 * kUnits) / kUnits;
+        const int j = rem - hh * 2 * kUnits - isv * kUnits;
+        const int seq = rows[r];
+        const int kvh = kv0 + hh;
+        const int L = min(max(p.context_lens[seq], 0), p.max_blocks_per_seq * 16);
+        const int64_t slot = L > 0 ? p.slot_mapping[seq] : -1;
+        if (kvh < p.num_kv_heads && slot >= 0 && slot < pool_rows) {
+          const size_t src = (size_t)seq * p.src_stride_bytes + (size_t)kvh * D * 2 + (size_t)j * 16;
+          x[b] = *reinterpret_cast<const uint4*>((isv ? p.v_new : p.k_new) + src);
+          dst[b] = (isv ? p.v_cache : p.k_cache) +
+                   (size_t)slot * (2ull * p.num_kv_heads * C::kRowBytes) +
+                   (size_t)kvh * C::kRowBytes + (size_t)j * kDstPiece;
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (dst[b] == nullptr) continue;
+      if constexpr (KV != kKvE4m3) {
+        *reinterpret_cast<uint4*>(dst[b]) = x[b];
+      } else {
+        *reinterpret_cast<uint2*>(dst[b]) = quantize8_e4m3<QT>(x[b], p.kv_scale);
+      }
+    }
+  }
+  fence_proxy_async_global();
 }
 
 // Issue the TMA loads of one 16-token block (K tile then V tile, H heads from
@@ -491,6 +558,208 @@ __device__ __forceinline__ void load_block(uint8_t* stage, const CUtensorMap* tm
     tma_load_3d(stage, tmap_k, full, 0, kv0, row, policy);
     tma_load_3d(stage + C::kTileBytes, tmap_v, full, 0, kv0, row, policy);
   }
+}
+
+// Balanced split (partition_blocks == 0).  The grid is one dimension of
+// `slots` CTAs (one wave on this GPU, or the number of (sequence, KV head
+// group) pairs if that is larger).  Every CTA computes the same plan from the
+// actual context lengths:
+//   pb = the smallest partition size in blocks, >= min_partition_blocks, with
+//        kv_groups * sum_i max(1, ceil(ceil(L_i / 16) / pb)) <= slots;
+// then takes work item blockIdx.x of the list ordered by (sequence, partition,
+// KV head group) -- each sequence has at least one item, so empty sequences
+// still get their zero output.  Items past the list's end exit at once.
+//
+// The plan is on every CTA's critical path, so it is a k-ary search: each
+// round tests evenly spaced sizes at once (the count is monotone in pb) and
+// keeps the interval where the test flips.  The interval starts narrow: with
+// T blocks over V sequences, count(pb) <= T / pb + V, so every
+// pb >= kv_groups * T / (slots - kv_groups * V) fits, while none below
+// kv_groups * T / slots does; for a few long sequences that is a window of a
+// few dozen sizes.  Up to 32 sequences, one warp does it all (a lane per
+// sequence and a lane per tested size, 32 sizes a round, no barrier inside);
+// beyond that the CTA's warps each test one size per round.
+constexpr int kMaxBalancedSeqs = 512;  // the host only picks the mode below this
+
+struct BalancedItem {
+  int pb, seq, part, kvg;
+  int len;  // the sequence's context length (-1: not known here)
+  bool valid;
+};
+
+struct BalancedScratch {
+  int nb[kMaxBalancedSeqs];  // blocks per sequence; -1: negative length (no item)
+  int fits[2][32];           // per round parity, per warp
+  int chunk[kMaxBalancedSeqs / 32];
+  int pick[5];
+};
+
+__device__ __forceinline__ int parts_of(int n, int pbv) {
+  return n < 0 ? 0 : max(1, (n + pbv - 1) / pbv);
+}
+
+// Up to 32 sequences: warp 0 computes the plan, every thread reads it.
+__device__ __forceinline__ BalancedItem balanced_plan_small(const DecodeParams& p,
+                                                           BalancedScratch& sc) {
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) {
+    const int B = p.num_seqs;
+    const int L = lane < B ? min(p.context_lens[lane], p.max_blocks_per_seq * 16) : -1;
+    const int n = L > 0 ? (L + 15) >> 4 : (L == 0 ? 0 : -1);  // -1: no item
+    int total = max(n, 0), maxnb = n, nvalid = n >= 0 ? 1 : 0;
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) {
+      total += __shfl_xor_sync(0xffffffffu, total, x);
+      maxnb = max(maxnb, __shfl_xor_sync(0xffffffffu, maxnb, x));
+      nvalid += __shfl_xor_sync(0xffffffffu, nvalid, x);
+    }
+    // The window's ends in float, widened so rounding cannot cut the answer
+    // off: below lo nothing fits, from hi on everything does.
+    const float tg = (float)total * (float)p.kv_groups;
+    const float want = tg / (float)p.slots * 0.999f;
+    int lo = max(p.min_partition_blocks, (int)fminf(want, 1.0e9f));
+    int ub = maxnb;
+    const int spare = p.slots - nvalid * p.kv_groups;
+    if (spare > 0) ub = min(ub, (int)fminf(tg / (float)spare * 1.001f + 2.f, 1.0e9f));
+    int hi = max(lo, ub);
+    while (lo < hi) {
+      const int span = hi - lo;
+      const int c = lo + (int)((long long)span * (lane + 1) / 32);  // lane 31 tests hi
+      int cnt = 0;
+      for (int i = 0; i < B; ++i) cnt += parts_of(__shfl_sync(0xffffffffu, n, i), c);
+      const unsigned fit =
+          __ballot_sync(0xffffffffu, (long long)cnt * p.kv_groups <= p.slots);
+      const int w = __ffs(fit) - 1;  // lane 31 (hi) always fits
+      const int cw = __shfl_sync(0xffffffffu, c, w);
+      const int cprev = __shfl_sync(0xffffffffu, c, w > 0 ? w - 1 : 0);
+      hi = cw;
+      lo = w > 0 ? cprev + 1 : lo;
+    }
+    const int pb = lo;
+    const int mine = parts_of(n, pb);
+    int incl = mine;
+#pragma unroll
+    for (int x = 1; x < 32; x <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, x);
+      if (lane >= x) incl += o;
+    }
+    const int all = __shfl_sync(0xffffffffu, incl, 31);
+    const int q = blockIdx.x / p.kv_groups;
+    const int excl = incl - mine;
+    const unsigned hit = __ballot_sync(0xffffffffu, q >= excl && q < excl + mine);
+    if (lane == 0) {
+      sc.pick[0] = hit ? __ffs(hit) - 1 : -1;
+      sc.pick[2] = pb;
+      sc.pick[3] = all;
+    }
+    if (hit && lane == __ffs(hit) - 1) {
+      sc.pick[1] = q - excl;
+      sc.pick[4] = L;
+    }
+  }
+  __syncthreads();
+  BalancedItem it;
+  it.pb = sc.pick[2];
+  const int q = blockIdx.x / p.kv_groups;
+  it.valid = q < sc.pick[3] && sc.pick[0] >= 0;
+  it.seq = it.valid ? sc.pick[0] : 0;
+  it.part = it.valid ? sc.pick[1] : 0;
+  it.kvg = blockIdx.x % p.kv_groups;
+  it.len = it.valid ? sc.pick[4] : -1;
+  return it;
+}
+
+template <int kThreads>
+__device__ __forceinline__ BalancedItem balanced_plan(const DecodeParams& p, BalancedScratch& sc) {
+  if (p.num_seqs <= 32) return balanced_plan_small(p, sc);
+  constexpr int kWarps = kThreads / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int B = p.num_seqs;
+  for (int i = threadIdx.x; i < B; i += kThreads) {
+    const int L = min(p.context_lens[i], p.max_blocks_per_seq * 16);
+    sc.nb[i] = L > 0 ? (L + 15) >> 4 : (L == 0 ? 0 : -1);
+  }
+  if (threadIdx.x == 0) sc.pick[0] = -1;
+  __syncthreads();
+  // Every warp reduces the totals itself: no barrier needed.
+  int total = 0, maxnb = 0, nvalid = 0;
+  for (int i = lane; i < B; i += 32) {
+    const int n = sc.nb[i];
+    total += max(n, 0);
+    maxnb = max(maxnb, n);
+    nvalid += n >= 0 ? 1 : 0;
+  }
+#pragma unroll
+  for (int x = 16; x > 0; x >>= 1) {
+    total += __shfl_xor_sync(0xffffffffu, total, x);
+    maxnb = max(maxnb, __shfl_xor_sync(0xffffffffu, maxnb, x));
+    nvalid += __shfl_xor_sync(0xffffffffu, nvalid, x);
+  }
+  const long long tg = (long long)total * p.kv_groups;
+  const long long want = (tg + p.slots - 1) / p.slots;
+  int lo = max(p.min_partition_blocks, (int)(want < (1ll << 30) ? want : (1ll << 30)));
+  // Every sequence in one partition (pb = maxnb) fits, as kv_groups * B <= slots.
+  long long ub = maxnb;
+  const long long spare = (long long)p.slots - (long long)nvalid * p.kv_groups;
+  if (spare > 0) ub = min(ub, (tg + spare - 1) / spare);
+  int hi = max(lo, (int)ub);
+  for (int round = 0; lo < hi; ++round) {
+    const long long span = hi - lo;
+    const int c = lo + (int)(span * (warp + 1) / kWarps);  // the last warp tests hi
+    int cnt = 0;
+    for (int i = lane; i < B; i += 32) cnt += parts_of(sc.nb[i], c);
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, x);
+    int* fits = sc.fits[round & 1];  // alternate so the next round's writes race no reads
+    if (lane == 0) fits[warp] = ((long long)cnt * p.kv_groups <= p.slots) ? 1 : 0;
+    __syncthreads();
+    int w = kWarps - 1;
+#pragma unroll
+    for (int k = kWarps - 2; k >= 0; --k) w = fits[k] ? k : w;
+    hi = lo + (int)(span * (w + 1) / kWarps);
+    lo = (w == 0) ? lo : lo + (int)(span * w / kWarps) + 1;
+  }
+  const int pb = lo;
+  // The item's (sequence, partition): prefix sums of partitions over
+  // sequences, by chunks of 32 sequences per warp.
+  const int nchunks = (B + 31) / 32;
+  for (int ch = warp; ch < nchunks; ch += kWarps) {
+    const int i = ch * 32 + lane;
+    int v = i < B ? parts_of(sc.nb[i], pb) : 0;
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) v += __shfl_xor_sync(0xffffffffu, v, x);
+    if (lane == 0) sc.chunk[ch] = v;
+  }
+  __syncthreads();
+  const int q = blockIdx.x / p.kv_groups;  // the item's (sequence, partition) index
+  int all = 0;
+  for (int ch = 0; ch < nchunks; ++ch) all += sc.chunk[ch];
+  for (int ch = warp; ch < nchunks; ch += kWarps) {
+    int before = 0;
+    for (int k = 0; k < ch; ++k) before += sc.chunk[k];
+    const int i = ch * 32 + lane;
+    const int mine = i < B ? parts_of(sc.nb[i], pb) : 0;
+    int incl = mine;
+#pragma unroll
+    for (int x = 1; x < 32; x <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, x);
+      if (lane >= x) incl += o;
+    }
+    const int excl = before + incl - mine;
+    if (q >= excl && q < excl + mine) {
+      sc.pick[0] = i;
+      sc.pick[1] = q - excl;
+    }
+  }
+  __syncthreads();
+  BalancedItem it;
+  it.pb = pb;
+  it.valid = q < all && sc.pick[0] >= 0;
+  it.seq = it.valid ? sc.pick[0] : 0;
+  it.part = it.valid ? sc.pick[1] : 0;
+  it.kvg = blockIdx.x % p.kv_groups;
+  it.len = -1;
+  return it;
 }
 
 template <int D, int KV, int QT, bool kAppend>
@@ -514,10 +783,22 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, DecodeCfg<D, KV>::
     tma_prefetch_desc(&tmap_v);
   }
   griddep_wait();
-  const int kvg = blockIdx.x, part = blockIdx.y, seq = blockIdx.z;
-  const int pb = p.partition_blocks;
+  int kvg = blockIdx.x, part = blockIdx.y, seq = blockIdx.z;
+  int pb = p.partition_blocks;
+  int L = -1;
+  if (pb == 0) {
+    __shared__ BalancedScratch plan_scratch;
+    const BalancedItem item = balanced_plan<C::kThreads>(p, plan_scratch);
+    if (threadIdx.x == 0 && blockIdx.x == 0) *p.plan = item.pb;
+    if (!item.valid) return;
+    pb = item.pb;
+    kvg = item.kvg;
+    part = item.part;
+    seq = item.seq;
+    L = item.len;
+  }
   // A length past the table's capacity is cut to it: no entry past the row is read.
-  const int L = min(p.context_lens[seq], p.max_blocks_per_seq * 16);
+  if (L < 0) L = min(p.context_lens[seq], p.max_blocks_per_seq * 16);
   const int part_tokens = pb * 16;
   const int tok0 = part * part_tokens;
   if (part > 0 && tok0 >= L) return;  // past the end of this sequence
@@ -749,10 +1030,12 @@ __global__ void __launch_bounds__(kMergeThreads)
   // The kernel before this one is always the same call's attention kernel,
   // which writes no lengths: they may be read before the wait.
   const int L = min(p.context_lens[seq], p.max_blocks_per_seq * 16);
-  const int part_tokens = p.partition_blocks * 16;
+  // A balanced split never cuts a sequence shorter than its minimum partition.
+  if (p.partition_blocks == 0 && L <= p.min_partition_blocks * 16) return;
+  griddep_wait();  // the partials (and a balanced split's size) come from the attention kernel
+  const int part_tokens = (p.partition_blocks ? p.partition_blocks : *p.plan) * 16;
   const int np = (L + part_tokens - 1) / part_tokens;
   if (np <= 1) return;  // written directly by the attention kernel
-  griddep_wait();  // the partials come from the attention kernel
   const size_t base = (size_t)idx * p.num_partitions;
   const int tid = threadIdx.x;
   const int r = tid / D;

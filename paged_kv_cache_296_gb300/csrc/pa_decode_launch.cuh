@@ -47,9 +47,29 @@ cudaError_t launch_fixed(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = smem_opt_in(paged_decode_kernel<D, KV, QT, kAppend>, C::kSmemBytes, attr_done, dev);
   if (e != cudaSuccess) return e;
+  // The balanced split's grid: resident CTAs of this kernel on the whole GPU
+  // (its partitions fit in one such wave), once per device.
+  if (p.partition_blocks == 0) {
+    static std::atomic<int> slots_cache[64];
+    int slots = slots_cache[dev & 63].load(std::memory_order_acquire);
+    if (slots == 0) {
+      int per_sm = 0, sms = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &per_sm, paged_decode_kernel<D, KV, QT, kAppend>, C::kThreads, C::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      slots = std::max(1, per_sm * sms);
+      slots_cache[dev & 63].store(slots, std::memory_order_release);
+    }
+    // one CTA per work item; at least one item per (sequence, KV head group)
+    const_cast<DecodeParams&>(p).slots = std::max(slots, a.num_seqs * p.kv_groups);
+  }
   cudaLaunchAttribute attr;
   cudaLaunchConfig_t cfg = pdl_config(
-      dim3((unsigned)p.kv_groups, (unsigned)a.num_partitions, (unsigned)a.num_seqs),
+      p.partition_blocks == 0
+          ? dim3((unsigned)p.slots)
+          : dim3((unsigned)p.kv_groups, (unsigned)a.num_partitions, (unsigned)a.num_seqs),
       dim3(C::kThreads), C::kSmemBytes, stream, &attr);
   e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, KV, QT, kAppend>, tk, tv, p);
   if (e != cudaSuccess || a.num_partitions <= 1) return e;
@@ -61,7 +81,7 @@ cudaError_t launch_fixed(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
 // CTAs of the stream-K kernel resident on the whole GPU for this shared-memory
 // size (one wave), capped at kMaxSplitCtas; cached per device for the last few
 // sizes asked.
-template <int D, int KV, int QT, bool kAppend, bool kShared>
+template <int D, int KV, int QT, bool kAppend>
 cudaError_t split_slots(int dev, size_t smem, int* slots) {
   using C = DecodeCfg<D, KV>;
   constexpr int kEntries = 8;
@@ -78,7 +98,7 @@ cudaError_t split_slots(int dev, size_t smem, int* slots) {
   }
   int per_sm = 0, sms = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, paged_decode_split_kernel<D, KV, QT, kAppend, kShared>, C::kThreads, smem);
+      &per_sm, paged_decode_split_kernel<D, KV, QT, kAppend>, SplitCfg<D, KV>::kThreads, smem);
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
@@ -89,25 +109,25 @@ cudaError_t split_slots(int dev, size_t smem, int* slots) {
   return cudaSuccess;
 }
 
-template <int D, int KV, int QT, bool kAppend, bool kShared>
+template <int D, int KV, int QT, bool kAppend>
 cudaError_t launch_split(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                          const DecodeArgs& a, cudaStream_t stream, int dev) {
   using C = DecodeCfg<D, KV>;
   using SC = SplitCfg<D, KV>;
   static std::atomic<unsigned long long> attr_done{0};
-  cudaError_t e = smem_opt_in(paged_decode_split_kernel<D, KV, QT, kAppend, kShared>,
+  cudaError_t e = smem_opt_in(paged_decode_split_kernel<D, KV, QT, kAppend>,
                               (int)SC::smem_bytes(kMaxPlanSeqs, kMaxPlanGroups), attr_done, dev);
   if (e != cudaSuccess) return e;
   const size_t smem = SC::smem_bytes(a.num_seqs, a.num_groups);
   int slots = 0;
-  e = split_slots<D, KV, QT, kAppend, kShared>(dev, smem, &slots);
+  e = split_slots<D, KV, QT, kAppend>(dev, smem, &slots);
   if (e != cudaSuccess) return e;
   // at least two CTAs per KV head group (one for each line); the host admits
   // at most kMaxSplitCtas / 2 groups
   const int grid = std::max(slots, 2 * p.kv_groups);
   cudaLaunchAttribute attr;
-  cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)grid), dim3(C::kThreads), smem, stream, &attr);
-  e = cudaLaunchKernelEx(&cfg, paged_decode_split_kernel<D, KV, QT, kAppend, kShared>, tk, tv, p);
+  cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)grid), dim3(SC::kThreads), smem, stream, &attr);
+  e = cudaLaunchKernelEx(&cfg, paged_decode_split_kernel<D, KV, QT, kAppend>, tk, tv, p);
   if (e != cudaSuccess) return e;
   const long long rows = (long long)a.num_seqs * a.num_q_heads;
   cudaLaunchConfig_t mcfg =
@@ -159,7 +179,9 @@ cudaError_t launch_decode_instance(const DecodeArgs& a, cudaStream_t stream, con
   p.src_stride_bytes = a.src_stride_bytes;
   p.k_cache = static_cast<uint8_t*>(const_cast<void*>(a.k_cache));
   p.v_cache = static_cast<uint8_t*>(const_cast<void*>(a.v_cache));
-  if (a.partition_tokens > 0) {
+  p.min_partition_blocks = a.min_partition_tokens / 16;
+  p.plan = a.plan;
+  if (a.num_groups == 0) {
     if (a.append) return launch_fixed<D, KV, QT, true>(tk, tv, p, a, stream, dev);
     return launch_fixed<D, KV, QT, false>(tk, tv, p, a, stream, dev);
   }
@@ -176,12 +198,8 @@ cudaError_t launch_decode_instance(const DecodeArgs& a, cudaStream_t stream, con
   p.whole_l = a.whole_l;
   p.whole_o = a.whole_o;
   p.plan = a.plan;
-  if (a.num_groups > 0) {
-    if (a.append) return launch_split<D, KV, QT, true, true>(tk, tv, p, a, stream, dev);
-    return launch_split<D, KV, QT, false, true>(tk, tv, p, a, stream, dev);
-  }
-  if (a.append) return launch_split<D, KV, QT, true, false>(tk, tv, p, a, stream, dev);
-  return launch_split<D, KV, QT, false, false>(tk, tv, p, a, stream, dev);
+  if (a.append) return launch_split<D, KV, QT, true>(tk, tv, p, a, stream, dev);
+  return launch_split<D, KV, QT, false>(tk, tv, p, a, stream, dev);
 }
 
 }  // namespace pa

@@ -1,4 +1,4 @@
-// Stream-K split of paged decode, with optional shared-prefix groups.
+// Paged decode of a batch with shared-prefix groups, as a stream-K split.
 //
 // The work is laid out as lines of units, one unit = one 16-token block, two
 // lines per KV head group (the same units for every group), and every CTA
@@ -27,7 +27,7 @@
 //
 // The plan is computed by every CTA from the context lengths (no host sync):
 // prefix sums of row lengths, the number of CTAs each line gets (in
-// proportion to its units, prefix units counted double) and the range width
+// proportion to its units, prefix units weighted by their cost) and the range width
 // W = ceil(units / CTAs) of each line (at least min_units).  CTA 0 stores it
 // for the merge kernel.
 //
@@ -37,7 +37,11 @@
 // segments), and at each segment end the four warps' states are merged through
 // a buffer outside the ring (the producer keeps filling the ring meanwhile).
 // On the prefix line every consumer warp reads every block for its own n-tile
-// of columns and writes its columns' partials itself.
+// of columns and writes its columns' partials itself.  With the fused write
+// (pa_decode_append_shared) the consumer warps write, at the CTA's start, the
+// new token of every row whose last block the CTA reads (they wait for data
+// then anyway), and the producer loads such a block only after their arrival
+// on a barrier, so the writes leave the producer's issue loop.
 #pragma once
 
 #include "pa_decode_kernel.cuh"
@@ -47,13 +51,13 @@ namespace pa {
 
 // Plan record in the workspace (ints): [0] CTAs on each group's prefix line,
 // [1] its range width, [2] the suffix line's width, [3] KV head groups; from
-// kPlanHeader, per sequence i four ints: U_i (suffix blocks before i), n_i
-// (its suffix blocks), g_i (its group or -1), j_i (its index among the
-// group's members); then per group g two ints: Up_g, n_g.  CTA c of line
-// position k serves KV head group c % kvgc with k = c / kvgc (prefix line
-// first).
-__host__ __device__ constexpr size_t split_plan_ints(int num_seqs, int num_groups) {
-  return (size_t)kPlanHeader + 4 * (size_t)num_seqs + 2 * (size_t)num_groups;
+// kPlanHeader, per sequence i kPlanSeqInts ints: U_i (suffix blocks before i),
+// n_i (its suffix blocks), g_i (its group or -1), j_i (its index among the
+// group's members), and for a member its group's Up_g (prefix blocks before
+// the group) and n_g (the group's prefix blocks).  CTA c of line position k
+// serves KV head group c % kvgc with k = c / kvgc (prefix line first).
+__host__ __device__ constexpr size_t split_plan_ints(int num_seqs) {
+  return (size_t)kPlanHeader + kPlanSeqInts * (size_t)num_seqs;
 }
 
 // Shared-memory plan arrays (ints): sU[B+1], sP[B], sG[B], sJ[B], sUp[NG+1].
@@ -64,14 +68,31 @@ __host__ __device__ constexpr size_t split_smem_plan_bytes(int num_seqs, int num
 template <int D, int KV>
 struct SplitCfg {
   using C = DecodeCfg<D, KV>;
+  // Eight consumer warps whatever the cache: 8 per head for a 16-bit cache
+  // (one KV head per CTA), 4 per head for E4M3 (two).  On the prefix line a
+  // head's warps form 4 n-tiles x kPrefixPhases block phases.
+  static constexpr int kConsumerWarps = 8;
+  static constexpr int kWarpsPerHead = kConsumerWarps / C::kHeads;
+  static constexpr int kPrefixPhases = kWarpsPerHead / 4;
+  static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+  static_assert(C::kStages % kWarpsPerHead == 0,
+                "each stage must belong to exactly one consumer warp per head");
+  static constexpr int kRedBytes =
+      kConsumerWarps * 8 * C::kRedStride * 4 + 2 * kConsumerWarps * 8 * 4;
   // Two CTAs per SM (shared memory allows no more).  The register cap this implies
-  // is per SM sub-partition: 2 x 9 warps of the E4M3 CTA put 5 warps on one of
-  // the four 16K-register files, so at most 96 registers a thread.
+  // is per SM sub-partition: 2 x 9 warps put 5 warps on one of the four
+  // 16K-register files, so at most 96 registers a thread.
   static constexpr int kMinCtasPerSm = 2;
-  // ring (1024-aligned) | merge buffer | full and empty barriers | plan arrays
+  // Suffix segments' query rows (H heads x up to 8 query heads x D, q's
+  // dtype) and context length, prefetched by the producer: two slots.
+  static constexpr int kQSlots = 2;
+  static constexpr int kQSlotBytes = C::kHeads * 8 * D * 2;
+  // ring (1024-aligned) | merge buffer | query slots | barriers (ring full and
+  // empty, slot full and empty) | plan arrays
   static constexpr int kRedOffset = C::kRingBytes;
-  static constexpr int kBarOffset = kRedOffset + C::kRedBytes;
-  static constexpr int kPlanOffset = kBarOffset + 2 * C::kStages * 8;
+  static constexpr int kQOffset = kRedOffset + kRedBytes;
+  static constexpr int kBarOffset = kQOffset + kQSlots * kQSlotBytes;
+  static constexpr int kPlanOffset = kBarOffset + (2 * C::kStages + 2 * kQSlots) * 8;
   __host__ __device__ static constexpr size_t smem_bytes(int num_seqs, int num_groups) {
     return 1024 + (size_t)kPlanOffset + split_smem_plan_bytes(num_seqs, num_groups);
   }
@@ -136,29 +157,35 @@ __device__ __forceinline__ void consumer_bar(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-// kShared: the call has shared-prefix groups (else the prefix line, its plan
-// and its consumer path are compiled out).
-template <int D, int KV, int QT, bool kAppend, bool kShared>
-__global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::kMinCtasPerSm)
+template <int D, int KV, int QT, bool kAppend>
+__global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kMinCtasPerSm)
     paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                               const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
   using C = DecodeCfg<D, KV>;
   using SC = SplitCfg<D, KV>;
-  constexpr int kT = C::kThreads;
-  constexpr int kConsumerThreads = C::kConsumerWarps * 32;
+  constexpr int kT = SC::kThreads;
+  constexpr int kConsumerWarps = SC::kConsumerWarps;
+  constexpr int kWarpsPerHead = SC::kWarpsPerHead;
+  constexpr int kConsumerThreads = kConsumerWarps * 32;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   float* red_o = reinterpret_cast<float*>(smem + SC::kRedOffset);    // [warps][8][D+4]
-  float* red_m = red_o + C::kConsumerWarps * 8 * C::kRedStride;       // [warps][8]
-  float* red_l = red_m + C::kConsumerWarps * 8;                       // [warps][8]
+  float* red_m = red_o + kConsumerWarps * 8 * C::kRedStride;          // [warps][8]
+  float* red_l = red_m + kConsumerWarps * 8;                          // [warps][8]
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + SC::kBarOffset);
   uint64_t* empty_bar = full_bar + C::kStages;
+  uint64_t* qfull_bar = empty_bar + C::kStages;
+  uint64_t* qempty_bar = qfull_bar + SC::kQSlots;
+  uint8_t* qslots = smem + SC::kQOffset;
+  __shared__ int qslot_len[SC::kQSlots];
+  // rows whose fused writes of new tokens are finished (see below)
+  __shared__ unsigned appended;
   __shared__ int abort_flag;
 
   const int B = p.num_seqs;
-  const int NG = kShared ? p.num_groups : 0;
+  const int NG = p.num_groups;
   const int kvgc = p.kv_groups;
   const int cap = p.max_blocks_per_seq * 16;
   int* sU = reinterpret_cast<int*>(smem + SC::kPlanOffset);  // [B+1]
@@ -167,7 +194,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
   int* sJ = sG + B;                                          // [B]
   int* sUp = sJ + B;                                         // [NG+1]
 
-  if (threadIdx.x == C::kConsumerWarps * 32) {
+  if (threadIdx.x == kConsumerWarps * 32) {
     tma_prefetch_desc(&tmap_k);
     tma_prefetch_desc(&tmap_v);
   }
@@ -181,14 +208,17 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
     sG[i] = -1;
     sJ[i] = 0;
   }
-  if (tid == 0) abort_flag = 0;
+  if (tid == 0) {
+    abort_flag = 0;
+    appended = 0;
+  }
   __syncthreads();
   // Groups: each member's suffix starts after the group's shared blocks.  A
   // group's prefix row has n_g = min(shared blocks, the longest member's
   // blocks) units.  Members past the columns a prefix CTA has (32 / G per KV
   // head) are left out of the group: their whole context is suffix.
   const int max_members = kPrefixCols / p.group;
-  const int n_members = (kShared && NG > 0) ? max(0, p.grp_off[NG]) : 0;
+  const int n_members = NG > 0 ? max(0, p.grp_off[NG]) : 0;
   for (int g = tid; g < NG; g += kT) {
     const int o0 = min(max(p.grp_off[g], 0), n_members);
     const int o1 = min(max(p.grp_off[g + 1], o0), min(n_members, o0 + max_members));
@@ -218,8 +248,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
   // Each KV head group has its own two lines (the units are the same for every
   // group); CTA c serves group c % kvgc, so the kvgc CTAs that read the same
   // blocks' adjacent head slices run side by side (DRAM pages are opened once
-  // for all of them).  Prefix units count double in the split of a group's
-  // CTAs between its lines: a prefix CTA's warps each run every block.
+  // for all of them).  In the split of a group's CTAs between its lines a
+  // prefix unit is weighted by its cost: a prefix CTA's n-tile warps each run
+  // every block of their phase.
   const int Tp = sUp[NG];
   const int Ts = sU[B];
   const int Skv = (int)gridDim.x / kvgc;  // >= 2 (the launcher's rule)
@@ -229,7 +260,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
   } else if (Ts == 0) {
     n_pre = Skv;
   } else {
-    const long long wp = 2LL * Tp;
+    // a prefix unit costs its CTA 4 / (4 x phases) warp passes per block more
+    // than a suffix unit: count it double with one phase, once with two
+    const long long wp = (long long)(2 / SC::kPrefixPhases) * Tp;
     n_pre = (int)(((long long)Skv * wp + (wp + Ts) / 2) / (wp + Ts));
     n_pre = min(max(n_pre, 1), Skv - 1);
   }
@@ -243,22 +276,17 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
       p.plan[3] = kvgc;
     }
     for (int i = tid; i < B; i += kT) {
-      int* r = p.plan + kPlanHeader + 4 * i;
-      r[0] = sU[i];
-      r[1] = sU[i + 1] - sU[i];
-      r[2] = sG[i];
-      r[3] = sJ[i];
-    }
-    for (int g = tid; g < NG; g += kT) {
-      int* r = p.plan + kPlanHeader + 4 * B + 2 * g;
-      r[0] = sUp[g];
-      r[1] = sUp[g + 1] - sUp[g];
+      int* r = p.plan + kPlanHeader + kPlanSeqInts * i;
+      const int g = sG[i];
+      *reinterpret_cast<int4*>(r) = make_int4(sU[i], sU[i + 1] - sU[i], g, sJ[i]);
+      *reinterpret_cast<int4*>(r + 4) =
+          g >= 0 ? make_int4(sUp[g], sUp[g + 1] - sUp[g], 0, 0) : make_int4(0, 0, 0, 0);
     }
   }
   const int my_kvg = (int)blockIdx.x % kvgc;
   const int ci = (int)blockIdx.x / kvgc;
   if (ci >= Skv) return;  // past the last whole set of kvgc CTAs
-  const bool pre = kShared && ci < n_pre;
+  const bool pre = ci < n_pre;
   const int cidx = pre ? ci : ci - n_pre;
   const int W = pre ? Wp : Ws;
   const int T = pre ? Tp : Ts;
@@ -274,17 +302,24 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      // suffix line: one consumer warp per head reads a stage; prefix line: all
-      mbar_init(&empty_bar[s], pre ? C::kConsumerWarps : C::kHeads);
+      // suffix line: one consumer warp per head reads a stage; prefix line:
+      // the four n-tile warps of its block phase, per head
+      mbar_init(&empty_bar[s], pre ? 4 * C::kHeads : C::kHeads);
+    }
+    for (int q = 0; q < SC::kQSlots; ++q) {
+      mbar_init(&qfull_bar[q], 1);
+      mbar_init(&qempty_bar[q], kConsumerWarps);
     }
     mbar_fence_init();
   }
   __syncthreads();
 
-  if (warp == C::kConsumerWarps) {
+  if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     const uint64_t kv_policy = l2_evict_first_policy();  // the KV stream is read once
     bool ok = true;
+    int row_ends = 0;
+    int nseg = 0;  // suffix segments so far: segment k uses query slot k % kQSlots
     int issued = 0;
     int it = 0;
     for (int u = u_begin; u < u_end && ok;) {
@@ -300,14 +335,34 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
           const int s = p.grp_seq[k];
           if (s >= 0 && s < B) seq = s;
         }
-      } else if constexpr (kAppend) {
-        // append_kv for this sequence's new token: written by the CTA that
-        // reads the row's last block, before it loads it.
-        if (sg.row_end) {
-          const int L = min(max(p.context_lens[seq], 0), cap);
-          const int64_t slot = L > 0 ? p.slot_mapping[seq] : -1;
-          append_token<D, KV, QT>(p, seq, sg.kvg * C::kHeads, slot);
+      }
+      // append_kv for a sequence's new token: the consumer warps write the
+      // tokens of the CTA's row-ending segments at its start, in order (they
+      // lie in the rows' last blocks, which this CTA reads); the r-th such
+      // row's last block is loaded only once more than r rows are written.
+      const bool gate = kAppend && !pre && sg.row_end;
+      if (!pre) {
+        // the segment's query rows and context length, into the next slot
+        const int qs = nseg % SC::kQSlots;
+        if (lane == 0 && ok) {
+          if (!mbar_wait_bounded(&qempty_bar[qs], ((uint32_t)(nseg / SC::kQSlots) & 1u) ^ 1u,
+                                 p.status)) {
+            ok = false;
+            abort_flag = 1;
+          } else {
+            const int kv0 = sg.kvg * C::kHeads;
+            const uint32_t bytes =
+                (uint32_t)(min(C::kHeads, p.num_kv_heads - kv0) * p.group * D * 2);
+            qslot_len[qs] = min(max(p.context_lens[seq], 0), cap);
+            mbar_arrive_expect_tx(&qfull_bar[qs], bytes);
+            bulk_load(qslots + qs * SC::kQSlotBytes,
+                      reinterpret_cast<const uint16_t*>(p.q) +
+                          ((size_t)seq * p.num_q_heads + (size_t)kv0 * p.group) * D,
+                      bytes, &qfull_bar[qs]);
+          }
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        ++nseg;
       }
       const int32_t* tbl = p.block_tables + (size_t)max(seq, 0) * p.max_blocks_per_seq + sg.b0;
       const int kv0 = sg.kvg * C::kHeads;
@@ -316,6 +371,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
         const int cnt = min(32, sg.nblk - base);
         for (int j = 0; j < cnt; ++j) {
           const int blk = __shfl_sync(0xffffffffu, mine, j);
+          if (gate && base + j == sg.nblk - 1) {
+            if (lane == 0 && ok && !smem_count_wait_bounded(&appended, (unsigned)row_ends, p.status)) {
+              ok = false;
+              abort_flag = 1;
+            }
+            ++row_ends;
+          }
           if (lane == 0 && ok) {
             const int s = it % C::kStages;
             const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
@@ -346,8 +408,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
   }
 
   // -------------------------------------------------------------- consumers
-  const int hsel = warp / C::kWarpsPerHead;
-  const int wq = warp % C::kWarpsPerHead;  // block phase (suffix) or n-tile (prefix)
+  const int hsel = warp / kWarpsPerHead;
+  const int wq = warp % kWarpsPerHead;  // suffix: block phase; prefix: n-tile + 4 x phase
   const int g = lane >> 2;
   const int t = lane & 3;
   float* my_o = red_o + warp * 8 * C::kRedStride;
@@ -356,6 +418,43 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
   WarpState<D> st;
   uint32_t qb[C::kMTiles][2];
   int it0 = 0;
+
+  if constexpr (kAppend) {
+    // The new token of every row whose last block this CTA reads, written by
+    // all consumer threads together, kAppendBatch rows at a time in segment
+    // order (append_rows: the loads of a thread's pieces are issued together,
+    // then the stores and a proxy fence); after each batch a barrier and a
+    // release addition to `appended` let the producer load those rows' last
+    // blocks.
+    constexpr int kAppendBatch = 64;
+    __shared__ int arow[kAppendBatch];
+    __shared__ int acount;
+    __shared__ int anext;
+    if (!pre) {
+      int u_scan = u_begin;
+      for (;;) {
+        if (tid == 0) {
+          int n = 0;
+          int u = u_scan;
+          while (u < u_end && n < kAppendBatch) {
+            const Segment sg = segment_at(u, u_begin, u_end, line_base, line_rows, line_first);
+            if (sg.row_end) arow[n++] = sg.row;
+            u += sg.nblk;
+          }
+          acount = n;
+          anext = u;
+        }
+        consumer_bar(kConsumerThreads);
+        const int n = acount;
+        u_scan = anext;
+        if (n > 0) append_rows<D, KV, QT>(p, arow, n, my_kvg * C::kHeads, tid, kConsumerThreads);
+        consumer_bar(kConsumerThreads);  // the writes, and the reads of arow, are done
+        if (n > 0 && tid == 0) smem_count_release(&appended, (unsigned)n);
+        if (n == 0 || u_scan >= u_end) break;
+      }
+    }
+  }
+  int nseg = 0;  // suffix segments so far (query slot nseg % kQSlots)
 
   for (int u = u_begin; u < u_end;) {
     Segment sg = segment_at(u, u_begin, u_end, line_base, line_rows, line_first);
@@ -366,17 +465,28 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
       // ------------------------------------------------ suffix line
       const int seq = sg.row;
       const bool live = kvh < p.num_kv_heads && g < p.group;
-      load_q_frag<D, KV, QT>(qb, p.q,
-                             ((size_t)seq * p.num_q_heads + kvh * p.group + (live ? g : 0)) * D,
-                             live);
+      // the segment's query rows and length, prefetched by the producer
+      const int qs = nseg % SC::kQSlots;
+      bool aborted = *reinterpret_cast<volatile int*>(&abort_flag) != 0;
+      if (!aborted &&
+          !mbar_wait_bounded(&qfull_bar[qs], (uint32_t)(nseg / SC::kQSlots) & 1u, p.status)) {
+        abort_flag = 1;
+        aborted = true;
+      }
+      ++nseg;
+      load_q_frag<D, KV, QT>(qb, qslots + qs * SC::kQSlotBytes,
+                             (size_t)(hsel * p.group + (live ? g : 0)) * D, live && !aborted);
       // tokens from the segment's first block to the context's end (the last
       // block of a row may be partial)
-      const int seg_ntok = min(max(p.context_lens[seq], 0), cap) - 16 * sg.b0;
+      const int seg_ntok = qslot_len[qs] - 16 * sg.b0;
+      // release the slot (generic reads before the next bulk copy's writes)
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qempty_bar[qs]);
       // block k of the segment sits at ring position it0 + k; this warp takes
       // the positions that are wq mod 4, as in the fixed kernel
-      const bool aborted = *reinterpret_cast<volatile int*>(&abort_flag) != 0;
-      for (int k = (wq - it0) & (C::kWarpsPerHead - 1); k < sg.nblk && !aborted;
-           k += C::kWarpsPerHead) {
+      for (int k = (wq - it0) & (kWarpsPerHead - 1); k < sg.nblk && !aborted;
+           k += kWarpsPerHead) {
         const int it = it0 + k;
         const int s = it % C::kStages;
         if (!mbar_wait_bounded(&full_bar[s], (uint32_t)(it / C::kStages) & 1u, p.status)) {
@@ -404,14 +514,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
         const int d = (rem - h * kQuads) * 4;
         const int kvh2 = sg.kvg * C::kHeads + hs;
         if (kvh2 >= p.num_kv_heads) break;
-        const int w0 = hs * C::kWarpsPerHead;
+        const int w0 = hs * kWarpsPerHead;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = w0; w < w0 + C::kWarpsPerHead; ++w) M = fmaxf(M, red_m[w * 8 + h]);
+        for (int w = w0; w < w0 + kWarpsPerHead; ++w) M = fmaxf(M, red_m[w * 8 + h]);
         float num[4] = {0.f, 0.f, 0.f, 0.f}, den = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
-          for (int w = w0; w < w0 + C::kWarpsPerHead; ++w) {
+          for (int w = w0; w < w0 + kWarpsPerHead; ++w) {
             const float wt = ex2_approx(__fsub_rn(red_m[w * 8 + h], M));
             const float4 ov =
                 *reinterpret_cast<const float4*>(&red_o[(w * 8 + h) * C::kRedStride + d]);
@@ -462,8 +572,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
       const int o1 = min(max(p.grp_off[sg.row + 1], o0), min(n_members, o0 + max_members));
       const int mcnt = o1 - o0;
       const bool kv_live = kvh < p.num_kv_heads;
-      // B operand: this lane's column 8 wq + g -> member, query head of the group
-      const int cb = 8 * wq + g;
+      const int nt = wq % 4;                     // this warp's n-tile of 8 columns
+      const int phase = wq / 4;                  // and its block phase
+      // B operand: this lane's column 8 nt + g -> member, query head of the group
+      const int cb = 8 * nt + g;
       const int jb = cb / p.group;
       const int sb = (jb < mcnt) ? p.grp_seq[o0 + jb] : -1;
       const bool bl = kv_live && sb >= 0 && sb < B;
@@ -473,7 +585,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
       int lim[2];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        const int j = (8 * wq + 2 * t + c) / p.group;
+        const int j = (8 * nt + 2 * t + c) / p.group;
         const int s = (j < mcnt) ? p.grp_seq[o0 + j] : -1;
         lim[c] = (s >= 0 && s < B && kv_live) ? min(max(p.context_lens[s], 0), cap) : -1;
       }
@@ -487,7 +599,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
       const int l1c = lim[1] < 0 ? (1 << 30) : lim[1];
       const bool need_mask = __any_sync(0xffffffffu, l0c < seg_tok_end || l1c < seg_tok_end);
       const bool aborted = *reinterpret_cast<volatile int*>(&abort_flag) != 0;
-      for (int k = 0; k < sg.nblk && !aborted; ++k) {
+      for (int k = (phase - it0) & (SC::kPrefixPhases - 1); k < sg.nblk && !aborted;
+           k += SC::kPrefixPhases) {
         const int it = it0 + k;
         const int s = it % C::kStages;
         if (!mbar_wait_bounded(&full_bar[s], (uint32_t)(it / C::kStages) & 1u, p.status)) {
@@ -509,35 +622,58 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
         if (lane == 0) mbar_arrive(&empty_bar[s]);
       }
       finish_row_sums(st);
-      // this warp's 8 columns -> their members' partials
+      // The block phases' states of each n-tile merge into its 8 columns'
+      // partials (one phase: a copy): every warp dumps its state, then the
+      // consumers write (column, 4 head_size elements) items.
       dump_state<D, KV>(st, my_o, my_m, my_l);
-      __syncwarp();
-      for (int c = 0; c < 8; ++c) {
-        const int col = 8 * wq + c;
+      consumer_bar(kConsumerThreads);
+      constexpr int kQuads = D / 4;
+      for (int idx = tid; idx < C::kHeads * kPrefixCols * kQuads; idx += kConsumerThreads) {
+        const int hs = idx / (kPrefixCols * kQuads);
+        const int rem = idx - hs * (kPrefixCols * kQuads);
+        const int col = rem / kQuads;             // 0..31: n-tile col / 8, column col % 8
+        const int d = (rem - col * kQuads) * 4;
         const int j = col / p.group;
-        if (j >= mcnt || !kv_live) break;  // later columns are past the members too
-        const int s = p.grp_seq[o0 + j];
-        if (s < 0 || s >= B) continue;
-        const int qh = kvh * p.group + col % p.group;
+        const int kvh2 = sg.kvg * C::kHeads + hs;
+        if (j >= mcnt || kvh2 >= p.num_kv_heads) continue;
+        const int sq = p.grp_seq[o0 + j];
+        if (sq < 0 || sq >= B) continue;
+        const int c = col % 8;
+        const int w0 = hs * kWarpsPerHead + col / 8;  // phase 0's warp of this n-tile
+        float M = -INFINITY;
+#pragma unroll
+        for (int ph = 0; ph < SC::kPrefixPhases; ++ph) M = fmaxf(M, red_m[(w0 + 4 * ph) * 8 + c]);
+        float num[4] = {0.f, 0.f, 0.f, 0.f}, den = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int ph = 0; ph < SC::kPrefixPhases; ++ph) {
+            const int w = w0 + 4 * ph;
+            const float wt = ex2_approx(__fsub_rn(red_m[w * 8 + c], M));
+            const float4 ov = *reinterpret_cast<const float4*>(&red_o[(w * 8 + c) * C::kRedStride + d]);
+            num[0] = __fmaf_rn(wt, ov.x, num[0]);
+            num[1] = __fmaf_rn(wt, ov.y, num[1]);
+            num[2] = __fmaf_rn(wt, ov.z, num[2]);
+            num[3] = __fmaf_rn(wt, ov.w, num[3]);
+            den = __fmaf_rn(wt, red_l[w * 8 + c], den);
+          }
+        }
+        const int qh = kvh2 * p.group + col % p.group;
         size_t pi;
         float *pm, *pl, *po;
         if (sg.whole) {
-          pi = (size_t)s * p.num_q_heads + qh;
+          pi = (size_t)sq * p.num_q_heads + qh;
           pm = p.whole_m; pl = p.whole_l; po = p.whole_o;
         } else {
-          pi = ((size_t)blockIdx.x * 2 + (sg.first ? 0 : 1)) * p.cut_cols + hsel * kPrefixCols + col;
+          pi = ((size_t)blockIdx.x * 2 + (sg.first ? 0 : 1)) * p.cut_cols + hs * kPrefixCols + col;
           pm = p.cut_m; pl = p.cut_l; po = p.cut_o;
         }
-        if (lane < D / 4) {
-          const float4 ov = *reinterpret_cast<const float4*>(&my_o[c * C::kRedStride + 4 * lane]);
-          *reinterpret_cast<float4*>(po + pi * D + 4 * lane) = ov;
-        }
-        if (lane == 0) {
-          pm[pi] = my_m[c];
-          pl[pi] = my_l[c];
+        *reinterpret_cast<float4*>(po + pi * D + d) = make_float4(num[0], num[1], num[2], num[3]);
+        if (d == 0) {
+          pm[pi] = M;
+          pl[pi] = den;
         }
       }
-      __syncwarp();
+      consumer_bar(kConsumerThreads);  // the buffer is free for the next segment
     }
     it0 += sg.nblk;
     u += sg.nblk;
@@ -557,7 +693,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, KV>::kThreads, SplitCfg<D, KV>::k
 constexpr int kSplitMergeWarps = 8;
 
 template <int D, int QT, int H>
-__global__ void __launch_bounds__(kSplitMergeWarps * 32)
+__global__ void __launch_bounds__(kSplitMergeWarps * 32, 4)
     paged_decode_split_merge_kernel(const DecodeParams p) {
   constexpr int kPer = D / 32;  // head_size elements per lane
   const int lane = threadIdx.x & 31;
@@ -570,8 +706,10 @@ __global__ void __launch_bounds__(kSplitMergeWarps * 32)
   const int n_pre = plan[0];
   const int Wp = plan[1], Ws = plan[2];
   const int kvgc = plan[3];
-  const int* rec = plan + kPlanHeader + 4 * seq;
-  const int U = rec[0], nsuf = rec[1], grp = rec[2], mem = rec[3];
+  const int4 r0 = *reinterpret_cast<const int4*>(plan + kPlanHeader + kPlanSeqInts * seq);
+  const int4 r1 = *reinterpret_cast<const int4*>(plan + kPlanHeader + kPlanSeqInts * seq + 4);
+  const int U = r0.x, nsuf = r0.y, grp = r0.z, mem = r0.w;
+  const int pre_start = r1.x, pre_len = r1.y;
   const int G = p.group;
   const int kvh = h / G;
   const int kvg = kvh / H;
@@ -597,10 +735,9 @@ __global__ void __launch_bounds__(kSplitMergeWarps * 32)
   int np = 0, p_start = 0, p_c0 = 0;
   bool p_whole = false;
   if (grp >= 0) {
-    const int* grec = plan + kPlanHeader + 4 * p.num_seqs + 2 * grp;
-    const int npre = grec[1];
+    const int npre = pre_len;
     if (npre > 0) {
-      p_start = grec[0];
+      p_start = pre_start;
       p_c0 = p_start / Wp;
       const int c1 = (p_start + npre - 1) / Wp;
       if (p_c0 == c1) {
@@ -662,13 +799,13 @@ __global__ void __launch_bounds__(kSplitMergeWarps * 32)
 #pragma unroll
     for (int x = 16; x > 0; x >>= 1) dl = __fadd_rn(dl, __shfl_xor_sync(0xffffffffu, dl, x));
     den = __fadd_rn(den, dl);
-    // O rows 8 at a time: all eight loads are issued before any is used
+    // O rows 4 at a time: all four loads are issued before any is used
     const int cnt = min(32, K - base);
-    for (int j0 = 0; j0 < cnt; j0 += 8) {
-      float w8[8];
-      float row8[8][kPer];
+    for (int j0 = 0; j0 < cnt; j0 += 4) {
+      float w8[4];
+      float row8[4][kPer];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 4; ++j) {
         const int jj = min(j0 + j, cnt - 1);
         w8[j] = (j0 + j < cnt) ? __shfl_sync(0xffffffffu, wk, jj) : 0.f;
         const float* row = reinterpret_cast<const float*>(
@@ -682,7 +819,7 @@ __global__ void __launch_bounds__(kSplitMergeWarps * 32)
         }
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 4; ++j) {
         if (j0 + j < cnt) {
 #pragma unroll
           for (int e = 0; e < kPer; ++e) acc[e] = __fmaf_rn(w8[j], row8[j][e], acc[e]);

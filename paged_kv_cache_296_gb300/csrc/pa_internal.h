@@ -8,12 +8,14 @@
 
 namespace pa {
 
-// Stream-K split (pa_decode_split.cuh): limits the host checks before choosing it.
+// The shared-prefix (stream-K) kernel (pa_decode_split.cuh): limits the host
+// checks before using it.
 constexpr int kMaxSplitCtas = 1024;   // grid cap; cut partials are sized for it
 constexpr int kMaxPlanSeqs = 1024;    // sequences in one stream-K call
 constexpr int kMaxPlanGroups = 1024;  // shared-prefix groups in one call
 constexpr int kPrefixCols = 32;       // MMA columns per KV head on the prefix line
 constexpr int kPlanHeader = 8;        // ints before the per-sequence plan records
+constexpr int kPlanSeqInts = 8;       // ints of one sequence's plan record
 constexpr int kMaxSplitHeads = 2;     // KV heads per CTA of any instantiation (E4M3)
 
 // Everything one pa_decode launch needs, already validated by the caller.
@@ -34,10 +36,10 @@ struct DecodeArgs {
   int kv_dtype;  // 0 f16, 1 bf16, 2 e4m3
   float scale;
   float kv_scale;
-  int partition_tokens;      // > 0: fixed partitions; 0: stream-K split chosen in the kernel
-  int min_partition_tokens;  // stream-K: the smallest range a CTA takes
-  int num_partitions;        // fixed partitions: grid partitions per sequence
-  float* part_m;             // fixed partitions: partials [B, Hq, P]
+  int partition_tokens;      // > 0: given partitions; 0: balanced split chosen in the kernel
+  int min_partition_tokens;  // balanced split / shared prefixes: the smallest partition or range
+  int num_partitions;        // grid partitions per sequence (balanced: an upper bound)
+  float* part_m;             // partitions: partials [B, Hq, P]
   float* part_l;
   float* part_o;
   unsigned* status;
@@ -47,7 +49,8 @@ struct DecodeArgs {
   const void* v_new;
   const int64_t* slot_mapping;
   int64_t src_stride_bytes;
-  // stream-K: shared-prefix groups (num_groups == 0: none) and the partials
+  // shared prefixes: the groups (num_groups == 0: none, the partition kernel
+  // runs) and the stream-K kernel's partials
   const int32_t* grp_off;
   const int32_t* grp_seq;
   const int32_t* grp_blocks;

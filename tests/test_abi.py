@@ -94,39 +94,40 @@ def test_decode_zero_sequences_is_a_no_op(lib):
 
 def test_workspace_size(lib):
     al = lambda x: (x + 255) // 256 * 256
-    plan_fixed = 256                        # the fixed layout keeps a 256-byte tail
+    plan = 256                              # where a balanced split records its size
     # 64 x 32 (sequence, KV head) pairs: enough CTAs, no split below 8192 tokens, no workspace
     assert lib.pa_decode_workspace_size(64, 32, 32, 128, 128, 16, 0) == 0
     assert pa.pa_decode_partition_size(64, 32, 128) == 2048
-    # 8 x 8 pairs: the stream-K split (0), planned on the device.  Its workspace:
-    # cut partials for up to 1024 CTAs x 2 slots x (2 KV heads x 8 query heads)
-    # columns (m, l, O), then the plan (8 ints + 4 per sequence)
+    # 8 x 8 pairs: a balanced split (0), chosen on the device; the workspace
+    # covers its smallest partition, 512 tokens: 32768 / 512 = 64 partitions
     assert pa.pa_decode_partition_size(8, 8, 2048) == 0
-    cut = 1024 * 2 * (2 * 8)
+    rows = 8 * 64 * 64
     assert lib.pa_decode_workspace_size(8, 64, 8, 128, 2048, 16, 0) == \
-        2 * al(cut * 4) + al(cut * 128 * 4) + al((8 + 4 * 8) * 4)
+        2 * al(rows * 4) + al(rows * 128 * 4) + plan
     # explicit sizes: 128 blocks = 2048 tokens = 4 partitions of 512
     rows = 64 * 32 * 4
     assert lib.pa_decode_workspace_size(64, 32, 32, 128, 128, 16, 512) == \
-        2 * al(rows * 4) + al(rows * 128 * 4) + plan_fixed
+        2 * al(rows * 4) + al(rows * 128 * 4) + plan
     assert lib.pa_decode_workspace_size(64, 32, 32, 128, 128, 16, 256) == \
-        2 * al(rows * 2 * 4) + al(rows * 2 * 128 * 4) + plan_fixed
+        2 * al(rows * 2 * 4) + al(rows * 2 * 128 * 4) + plan
     assert lib.pa_decode_workspace_size(64, 32, 32, 128, 128, 15, 0) == 0   # invalid block size
-    # shared prefixes: cut columns 2 x 32 per slot, whole partials (prefix and
-    # suffix) per (sequence, query head), the plan with 2 ints per group
+    # shared prefixes: cut partials of up to 1024 CTAs x 2 slots x (2 KV heads x
+    # 32 columns), whole partials (prefix and suffix) per (sequence, query head),
+    # the plan (8 ints + 8 per sequence)
     cut = 1024 * 2 * 64
     whole = 2 * 128 * 32
     assert lib.pa_decode_shared_workspace_size(128, 32, 8, 128, 81, 16, 16) == \
         2 * al(cut * 4) + al(cut * 128 * 4) + 2 * al(whole * 4) + al(whole * 128 * 4) \
-        + al((8 + 4 * 128 + 2 * 16) * 4)
+        + al((8 + 8 * 128) * 4)
+    # no groups: pa_decode's own choice and workspace
+    assert lib.pa_decode_shared_workspace_size(8, 64, 8, 128, 2048, 16, 0) == \
+        lib.pa_decode_workspace_size(8, 64, 8, 128, 2048, 16, 0)
     assert lib.pa_decode_shared_workspace_size(1025, 32, 8, 128, 81, 16, 1) == 0  # too many seqs
     assert lib.pa_decode_shared_workspace_size(8, 32, 8, 128, 81, 16, 1025) == 0  # too many groups
     # the library's choice
     assert pa.pa_decode_partition_size(4, 4, 2) == 32            # short: one partition
-    assert pa.pa_decode_partition_size(1, 1, 100000) == 0        # few pairs: stream-K split
+    assert pa.pa_decode_partition_size(1, 1, 100000) == 0        # few pairs: balanced split
     assert pa.pa_decode_partition_size(1024, 8, 4096) == 8192    # many pairs, 65536 tokens: capped
-    # few pairs, but more blocks over sequences and heads than the plan counts: capped partitions
-    assert pa.pa_decode_partition_size(300, 1, 1 << 23) == 8192
     assert pa.pa_decode_partition_size(64, 8, 128, partition_size=48) == 48
     assert pa.pa_decode_partition_size(64, 8, 128, partition_size=40) == -1
 

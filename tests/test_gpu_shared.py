@@ -250,9 +250,9 @@ def test_shared_run_to_run_bitwise_and_workspace_garbage():
         assert torch.equal(_bits(o), _bits(outs[0]))
 
 
-def test_no_groups_equals_the_stream_k_decode_bitwise():
-    """With no groups the shared call is the plain stream-K split: same plan,
-    same arithmetic, same bits as pa_decode's library choice."""
+def test_no_groups_is_pa_decode_bitwise():
+    """With no groups the shared call is pa_decode with the library's choice of
+    split: the same kernels and plan, the same bits."""
     W = wl.make_workload(wl.SPECS[5], 5, device="cuda")
     assert pa.pa_decode_partition_size(8, 8, W.max_blocks_per_seq) == 0
     pool = H.gpu_pool(W)
