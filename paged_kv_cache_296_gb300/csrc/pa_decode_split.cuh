@@ -79,6 +79,8 @@ struct SplitCfg {
                 "each stage must belong to exactly one consumer warp per head");
   static constexpr int kRedBytes =
       kConsumerWarps * 8 * C::kRedStride * 4 + 2 * kConsumerWarps * 8 * 4;
+  static_assert(kRedBytes >= (3 * kMaxPlanGroups + 1) * 4,
+                "the plan keeps the group arrays in the merge buffer");
   // Two CTAs per SM (shared memory allows no more).  The register cap this implies
   // is per SM sub-partition: 2 x 9 warps put 5 warps on one of the four
   // 16K-register files, so at most 96 registers a thread.
@@ -202,11 +204,26 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
   griddep_wait();
 
   // ------------------------------------------------------------------ plan
+  // Two rounds of global loads (every load of a round issued by its own
+  // thread): lengths and group arrays, then the members' sequence ids.  The
+  // merge buffer is free here and holds the group arrays meanwhile.
   const int tid = threadIdx.x;
+  int* gOff = reinterpret_cast<int*>(red_o);  // [NG+1] group offsets as given
+  int* gBlk = gOff + NG + 1;                  // [NG] shared blocks, clamped
+  int* gMax = gBlk + NG;                      // [NG] longest member, in blocks
   for (int i = tid; i < B; i += kT) {
+    const int L = min(max(p.context_lens[i], 0), cap);
+    sU[i + 1] = (L + 15) >> 4;  // the sequence's blocks, for now
     sP[i] = 0;
     sG[i] = -1;
     sJ[i] = 0;
+  }
+  for (int g = tid; g <= NG; g += kT) {
+    gOff[g] = p.grp_off[g];
+    if (g < NG) {
+      gBlk[g] = min(max(p.grp_blocks[g], 0), p.max_blocks_per_seq);
+      gMax[g] = 0;
+    }
   }
   if (tid == 0) {
     abort_flag = 0;
@@ -216,30 +233,26 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
   // Groups: each member's suffix starts after the group's shared blocks.  A
   // group's prefix row has n_g = min(shared blocks, the longest member's
   // blocks) units.  Members past the columns a prefix CTA has (32 / G per KV
-  // head) are left out of the group: their whole context is suffix.
+  // head) are left out of the group: their whole context is suffix.  One
+  // (group, member slot) pair per item.
   const int max_members = kPrefixCols / p.group;
-  const int n_members = NG > 0 ? max(0, p.grp_off[NG]) : 0;
-  for (int g = tid; g < NG; g += kT) {
-    const int o0 = min(max(p.grp_off[g], 0), n_members);
-    const int o1 = min(max(p.grp_off[g + 1], o0), min(n_members, o0 + max_members));
-    const int pg = min(max(p.grp_blocks[g], 0), p.max_blocks_per_seq);
-    int maxnb = 0;
-    for (int k = o0; k < o1; ++k) {
-      const int s = p.grp_seq[k];
-      if (s < 0 || s >= B) continue;
-      const int L = min(max(p.context_lens[s], 0), cap);
-      maxnb = max(maxnb, (L + 15) >> 4);
-      sP[s] = pg;
-      sG[s] = g;
-      sJ[s] = k - o0;
-    }
-    sUp[g + 1] = min(pg, maxnb);
+  const int n_members = NG > 0 ? max(0, gOff[NG]) : 0;
+  for (int item = tid; item < NG * max_members; item += kT) {
+    const int g = item / max_members;
+    const int j = item - g * max_members;
+    const int o0 = min(max(gOff[g], 0), n_members);
+    const int o1 = min(max(gOff[g + 1], o0), min(n_members, o0 + max_members));
+    if (o0 + j >= o1) continue;
+    const int s = p.grp_seq[o0 + j];
+    if (s < 0 || s >= B) continue;
+    atomicMax(&gMax[g], sU[s + 1]);
+    sP[s] = gBlk[g];
+    sG[s] = g;
+    sJ[s] = j;
   }
   __syncthreads();
-  for (int i = tid; i < B; i += kT) {
-    const int L = min(max(p.context_lens[i], 0), cap);
-    sU[i + 1] = max(0, ((L + 15) >> 4) - sP[i]);
-  }
+  for (int g = tid; g < NG; g += kT) sUp[g + 1] = min(gBlk[g], gMax[g]);
+  for (int i = tid; i < B; i += kT) sU[i + 1] = max(0, sU[i + 1] - sP[i]);
   __syncthreads();
   if (tid < 32) warp_scan_counts(sU, B);
   else if (tid < 64) warp_scan_counts(sUp, NG);
