@@ -202,17 +202,21 @@ __device__ __forceinline__ void load_q_frag(uint32_t (&qb)[D / 16][2], const voi
   }
 }
 
-// One 16-token block of one head, for the calling warp's 8 columns: S^T = K Q^T,
-// online softmax, O^T += V^T P^T.  kbase / vbase: the stage's K and V tiles
-// (H heads, token-major); hsel: this warp's head within the tile; valid: the
-// block's tokens that exist (V rows past it are zeroed, their logits -inf).
-// kColMask: token r of the block counts for column 2t only if r < lim0 and for
-// column 2t + 1 only if r < lim1 (columns of different sequences), and a column
-// with no token so far keeps a zero state.
-template <int D, int KV, bool kColMask>
-__device__ __forceinline__ void decode_block(WarpState<D>& st, const uint32_t (&qb)[D / 16][2],
-                                             uint32_t kbase, uint32_t vbase, int hsel, int valid,
-                                             float scale_log2, int lim0, int lim1) {
+// NB 16-token blocks of one head (NB = 1 or 2), for the calling warp's 8
+// columns: S^T = K Q^T, online softmax, O^T += V^T P^T.  kbase[b] / vbase[b]:
+// block b's K and V tiles in its stage (H heads, token-major); hsel: this
+// warp's head within the tile; valid[b]: the block's tokens that exist (V rows
+// past it are zeroed, their logits -inf).  kColMask: token r of block b counts
+// for column 2t only if r < lim0[b] and for column 2t + 1 only if r < lim1[b]
+// (columns of different sequences), and a column with no token so far keeps a
+// zero state.  With NB = 2 the blocks' MMA chains interleave and they share
+// one softmax step (one running-maximum update over their 32 tokens).
+template <int D, int KV, bool kColMask, int NB>
+__device__ __forceinline__ void decode_blocks(WarpState<D>& st, const uint32_t (&qb)[D / 16][2],
+                                              const uint32_t (&kbase)[NB],
+                                              const uint32_t (&vbase)[NB], int hsel,
+                                              const int (&valid)[NB], float scale_log2,
+                                              const int (&lim0)[NB], const int (&lim1)[NB]) {
   using C = DecodeCfg<D, KV>;
   constexpr bool kFp8 = (KV == kKvE4m3);
   // The P^T / V operands of the PV product are f16 unless the cache is bf16.
@@ -224,57 +228,74 @@ __device__ __forceinline__ void decode_block(WarpState<D>& st, const uint32_t (&
   auto row_of = [&](int tok) { return (uint32_t)((tok * C::kHeads + hsel) * C::kRowBytes); };
 
   // ---- S^T = K . Q^T  (rows: tokens, columns: query heads)
-  float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+  float sacc[NB][4];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) sacc[b][0] = sacc[b][1] = sacc[b][2] = sacc[b][3] = 0.f;
   if constexpr (!kFp8) {
     const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
     for (int ks = 0; ks < C::kMTiles; ++ks) {
-      uint32_t a[4];
-      ldsm_x4(a, kbase + swz<C::kSwizzle>(row_of(tok) + (ks * 2 + (lane >> 4)) * 16));
-      if constexpr (kBf16Mma) {
-        mma_bf16(sacc, a, qb[ks][0], qb[ks][1]);
-      } else {
-        mma_f16(sacc, a, qb[ks][0], qb[ks][1]);
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        uint32_t a[4];
+        ldsm_x4(a, kbase[b] + swz<C::kSwizzle>(row_of(tok) + (ks * 2 + (lane >> 4)) * 16));
+        if constexpr (kBf16Mma) {
+          mma_bf16(sacc[b], a, qb[ks][0], qb[ks][1]);
+        } else {
+          mma_f16(sacc[b], a, qb[ks][0], qb[ks][1]);
+        }
       }
     }
   } else {
     constexpr int kCpl = D / 64;  // 16-byte chunks per lane per row
-    uint32_t wa[C::kMTiles], wb[C::kMTiles];
 #pragma unroll
-    for (int i = 0; i < kCpl; ++i) {
-      const uint4 xa = lds128(kbase + swz<C::kSwizzle>(row_of(g) + (kCpl * t + i) * 16));
-      const uint4 xb = lds128(kbase + swz<C::kSwizzle>(row_of(g + 8) + (kCpl * t + i) * 16));
-      wa[4 * i + 0] = xa.x; wa[4 * i + 1] = xa.y; wa[4 * i + 2] = xa.z; wa[4 * i + 3] = xa.w;
-      wb[4 * i + 0] = xb.x; wb[4 * i + 1] = xb.y; wb[4 * i + 2] = xb.z; wb[4 * i + 3] = xb.w;
-    }
+    for (int b = 0; b < NB; ++b) {
+      uint32_t wa[C::kMTiles], wb[C::kMTiles];
 #pragma unroll
-    for (int ks = 0; ks < C::kMTiles; ++ks) {
-      uint32_t a[4];
-      a[0] = e4m3x2_to_f16x2((uint16_t)(wa[ks] & 0xFFFFu));
-      a[1] = e4m3x2_to_f16x2((uint16_t)(wb[ks] & 0xFFFFu));
-      a[2] = e4m3x2_to_f16x2((uint16_t)(wa[ks] >> 16));
-      a[3] = e4m3x2_to_f16x2((uint16_t)(wb[ks] >> 16));
-      mma_f16(sacc, a, qb[ks][0], qb[ks][1]);
+      for (int i = 0; i < kCpl; ++i) {
+        const uint4 xa = lds128(kbase[b] + swz<C::kSwizzle>(row_of(g) + (kCpl * t + i) * 16));
+        const uint4 xb = lds128(kbase[b] + swz<C::kSwizzle>(row_of(g + 8) + (kCpl * t + i) * 16));
+        wa[4 * i + 0] = xa.x; wa[4 * i + 1] = xa.y; wa[4 * i + 2] = xa.z; wa[4 * i + 3] = xa.w;
+        wb[4 * i + 0] = xb.x; wb[4 * i + 1] = xb.y; wb[4 * i + 2] = xb.z; wb[4 * i + 3] = xb.w;
+      }
+#pragma unroll
+      for (int ks = 0; ks < C::kMTiles; ++ks) {
+        uint32_t a[4];
+        a[0] = e4m3x2_to_f16x2((uint16_t)(wa[ks] & 0xFFFFu));
+        a[1] = e4m3x2_to_f16x2((uint16_t)(wb[ks] & 0xFFFFu));
+        a[2] = e4m3x2_to_f16x2((uint16_t)(wa[ks] >> 16));
+        a[3] = e4m3x2_to_f16x2((uint16_t)(wb[ks] >> 16));
+        mma_f16(sacc[b], a, qb[ks][0], qb[ks][1]);
+      }
     }
   }
 
-  // ---- online softmax on the fragment: c0/c1 token g, c2/c3 token g+8
+  // ---- online softmax on the fragments: c0/c1 token g, c2/c3 token g+8
   // Every rounding step below is spelled out (_rn intrinsics), so no
   // instantiation of this kernel contracts them into FMAs differently:
   // all variants produce the same bits.
-  float s0 = __fmul_rn(sacc[0], scale_log2), s1 = __fmul_rn(sacc[1], scale_log2);
-  float s2 = __fmul_rn(sacc[2], scale_log2), s3 = __fmul_rn(sacc[3], scale_log2);
-  if (valid < 16) {
-    if (g >= valid) s0 = s1 = -INFINITY;
-    if (g + 8 >= valid) s2 = s3 = -INFINITY;
+  float sc[NB][4];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc[b][i] = __fmul_rn(sacc[b][i], scale_log2);
+    if (valid[b] < 16) {
+      if (g >= valid[b]) sc[b][0] = sc[b][1] = -INFINITY;
+      if (g + 8 >= valid[b]) sc[b][2] = sc[b][3] = -INFINITY;
+    }
+    if constexpr (kColMask) {
+      if (g >= lim0[b]) sc[b][0] = -INFINITY;
+      if (g >= lim1[b]) sc[b][1] = -INFINITY;
+      if (g + 8 >= lim0[b]) sc[b][2] = -INFINITY;
+      if (g + 8 >= lim1[b]) sc[b][3] = -INFINITY;
+    }
   }
-  if constexpr (kColMask) {
-    if (g >= lim0) s0 = -INFINITY;
-    if (g >= lim1) s1 = -INFINITY;
-    if (g + 8 >= lim0) s2 = -INFINITY;
-    if (g + 8 >= lim1) s3 = -INFINITY;
+  float bm0 = fmaxf(sc[0][0], sc[0][2]), bm1 = fmaxf(sc[0][1], sc[0][3]);
+#pragma unroll
+  for (int b = 1; b < NB; ++b) {
+    bm0 = fmaxf(bm0, fmaxf(sc[b][0], sc[b][2]));
+    bm1 = fmaxf(bm1, fmaxf(sc[b][1], sc[b][3]));
   }
-  float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
 #pragma unroll
   for (int x = 4; x < 32; x <<= 1) {
     bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
@@ -288,24 +309,35 @@ __device__ __forceinline__ void decode_block(WarpState<D>& st, const uint32_t (&
   const float al0 = ex2_approx(__fsub_rn(st.m0, mr0)), al1 = ex2_approx(__fsub_rn(st.m1, mr1));
   st.m0 = mn0;
   st.m1 = mn1;
-  const float p0 = ex2_approx(__fsub_rn(s0, mr0)), p1 = ex2_approx(__fsub_rn(s1, mr1));
-  const float p2 = ex2_approx(__fsub_rn(s2, mr0)), p3 = ex2_approx(__fsub_rn(s3, mr1));
-  uint32_t P01, P23;
-  float r0, r1, r2, r3;  // the rounded probabilities the MMA will use
-  if constexpr (kBf16Mma) {
-    P01 = pack_bf16x2(p0, p1);
-    P23 = pack_bf16x2(p2, p3);
-    r0 = __uint_as_float(P01 << 16); r1 = __uint_as_float(P01 & 0xFFFF0000u);
-    r2 = __uint_as_float(P23 << 16); r3 = __uint_as_float(P23 & 0xFFFF0000u);
-  } else {
-    P01 = pack_f16x2(p0, p1);
-    P23 = pack_f16x2(p2, p3);
-    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&P01));
-    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&P23));
-    r0 = f01.x; r1 = f01.y; r2 = f23.x; r3 = f23.y;
+  uint32_t P01[NB], P23[NB];
+  float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const float p0 = ex2_approx(__fsub_rn(sc[b][0], mr0)), p1 = ex2_approx(__fsub_rn(sc[b][1], mr1));
+    const float p2 = ex2_approx(__fsub_rn(sc[b][2], mr0)), p3 = ex2_approx(__fsub_rn(sc[b][3], mr1));
+    float r0, r1, r2, r3;  // the rounded probabilities the MMA will use
+    if constexpr (kBf16Mma) {
+      P01[b] = pack_bf16x2(p0, p1);
+      P23[b] = pack_bf16x2(p2, p3);
+      r0 = __uint_as_float(P01[b] << 16); r1 = __uint_as_float(P01[b] & 0xFFFF0000u);
+      r2 = __uint_as_float(P23[b] << 16); r3 = __uint_as_float(P23[b] & 0xFFFF0000u);
+    } else {
+      P01[b] = pack_f16x2(p0, p1);
+      P23[b] = pack_f16x2(p2, p3);
+      const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&P01[b]));
+      const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&P23[b]));
+      r0 = f01.x; r1 = f01.y; r2 = f23.x; r3 = f23.y;
+    }
+    if (b == 0) {
+      sum0 = __fadd_rn(r0, r2);
+      sum1 = __fadd_rn(r1, r3);
+    } else {
+      sum0 = __fadd_rn(sum0, __fadd_rn(r0, r2));
+      sum1 = __fadd_rn(sum1, __fadd_rn(r1, r3));
+    }
   }
-  st.l0 = __fmaf_rn(st.l0, al0, __fadd_rn(r0, r2));
-  st.l1 = __fmaf_rn(st.l1, al1, __fadd_rn(r1, r3));
+  st.l0 = __fmaf_rn(st.l0, al0, sum0);
+  st.l1 = __fmaf_rn(st.l1, al1, sum1);
   if (__any_sync(0xffffffffu, (al0 != 1.f) || (al1 != 1.f))) {
 #pragma unroll
     for (int i = 0; i < C::kMTiles; ++i) {
@@ -314,9 +346,14 @@ __device__ __forceinline__ void decode_block(WarpState<D>& st, const uint32_t (&
     }
   }
   // P^T as the B operand: k = tokens (2t, 2t+1 | 2t+8, 2t+9), n = head g.
-  const uint32_t pb0 = movmatrix_trans(P01);
-  const uint32_t pb1 = movmatrix_trans(P23);
-  const uint32_t mlo = token_mask(2 * t, valid), mhi = token_mask(2 * t + 8, valid);
+  uint32_t pb0[NB], pb1[NB], mlo[NB], mhi[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    pb0[b] = movmatrix_trans(P01[b]);
+    pb1[b] = movmatrix_trans(P23[b]);
+    mlo[b] = token_mask(2 * t, valid[b]);
+    mhi[b] = token_mask(2 * t + 8, valid[b]);
+  }
 
   // ---- O^T += V^T . P^T
   if constexpr (!kFp8) {
@@ -324,57 +361,73 @@ __device__ __forceinline__ void decode_block(WarpState<D>& st, const uint32_t (&
     const int tok = (lane & 7) + 8 * (mi >> 1);
 #pragma unroll
     for (int mt = 0; mt < C::kMTiles; ++mt) {
-      uint32_t a[4];
-      ldsm_x4_trans(a, vbase + swz<C::kSwizzle>(row_of(tok) + (mt * 2 + (mi & 1)) * 16));
-      if (valid < 16) {
-        a[0] &= mlo; a[1] &= mlo; a[2] &= mhi; a[3] &= mhi;
-      }
-      if constexpr (kBf16Mma) {
-        mma_bf16(st.o[mt], a, pb0, pb1);
-      } else {
-        mma_f16(st.o[mt], a, pb0, pb1);
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        uint32_t a[4];
+        ldsm_x4_trans(a, vbase[b] + swz<C::kSwizzle>(row_of(tok) + (mt * 2 + (mi & 1)) * 16));
+        if (valid[b] < 16) {
+          a[0] &= mlo[b]; a[1] &= mlo[b]; a[2] &= mhi[b]; a[3] &= mhi[b];
+        }
+        if constexpr (kBf16Mma) {
+          mma_bf16(st.o[mt], a, pb0[b], pb1[b]);
+        } else {
+          mma_f16(st.o[mt], a, pb0[b], pb1[b]);
+        }
       }
     }
   } else {
-    // Lane (g, t) owns head_size indices [D/8 * g, D/8 * (g+1)) of tokens
-    // 2t, 2t+1, 2t+8, 2t+9; m-tile mt row g is index D/8*g + 2mt, row g+8
-    // is the next one.
-    uint32_t va[D / 32], vb[D / 32], vc[D / 32], vd[D / 32];
-    if constexpr (D == 128) {
-      const uint32_t col = g * 16;
-      const uint4 x0 = lds128(vbase + swz<C::kSwizzle>(row_of(2 * t) + col));
-      const uint4 x1 = lds128(vbase + swz<C::kSwizzle>(row_of(2 * t + 1) + col));
-      const uint4 x2 = lds128(vbase + swz<C::kSwizzle>(row_of(2 * t + 8) + col));
-      const uint4 x3 = lds128(vbase + swz<C::kSwizzle>(row_of(2 * t + 9) + col));
-      va[0] = x0.x; va[1] = x0.y; va[2] = x0.z; va[3] = x0.w;
-      vb[0] = x1.x; vb[1] = x1.y; vb[2] = x1.z; vb[3] = x1.w;
-      vc[0] = x2.x; vc[1] = x2.y; vc[2] = x2.z; vc[3] = x2.w;
-      vd[0] = x3.x; vd[1] = x3.y; vd[2] = x3.z; vd[3] = x3.w;
-    } else {
-      const uint32_t col = g * 8;
-      const uint2 x0 = lds64(vbase + swz<C::kSwizzle>(row_of(2 * t) + col));
-      const uint2 x1 = lds64(vbase + swz<C::kSwizzle>(row_of(2 * t + 1) + col));
-      const uint2 x2 = lds64(vbase + swz<C::kSwizzle>(row_of(2 * t + 8) + col));
-      const uint2 x3 = lds64(vbase + swz<C::kSwizzle>(row_of(2 * t + 9) + col));
-      va[0] = x0.x; va[1] = x0.y; vb[0] = x1.x; vb[1] = x1.y;
-      vc[0] = x2.x; vc[1] = x2.y; vd[0] = x3.x; vd[1] = x3.y;
-    }
 #pragma unroll
-    for (int mt = 0; mt < C::kMTiles; ++mt) {
-      const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-      const uint32_t lo = __byte_perm(va[mt >> 1], vb[mt >> 1], sel);  // tokens 2t, 2t+1
-      const uint32_t hi = __byte_perm(vc[mt >> 1], vd[mt >> 1], sel);  // tokens 2t+8, 2t+9
-      uint32_t a[4];
-      a[0] = e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu));
-      a[1] = e4m3x2_to_f16x2((uint16_t)(lo >> 16));
-      a[2] = e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu));
-      a[3] = e4m3x2_to_f16x2((uint16_t)(hi >> 16));
-      if (valid < 16) {
-        a[0] &= mlo; a[1] &= mlo; a[2] &= mhi; a[3] &= mhi;
+    for (int b = 0; b < NB; ++b) {
+      // Lane (g, t) owns head_size indices [D/8 * g, D/8 * (g+1)) of tokens
+      // 2t, 2t+1, 2t+8, 2t+9; m-tile mt row g is index D/8*g + 2mt, row g+8
+      // is the next one.
+      uint32_t va[D / 32], vb[D / 32], vc[D / 32], vd[D / 32];
+      if constexpr (D == 128) {
+        const uint32_t col = g * 16;
+        const uint4 x0 = lds128(vbase[b] + swz<C::kSwizzle>(row_of(2 * t) + col));
+        const uint4 x1 = lds128(vbase[b] + swz<C::kSwizzle>(row_of(2 * t + 1) + col));
+        const uint4 x2 = lds128(vbase[b] + swz<C::kSwizzle>(row_of(2 * t + 8) + col));
+        const uint4 x3 = lds128(vbase[b] + swz<C::kSwizzle>(row_of(2 * t + 9) + col));
+        va[0] = x0.x; va[1] = x0.y; va[2] = x0.z; va[3] = x0.w;
+        vb[0] = x1.x; vb[1] = x1.y; vb[2] = x1.z; vb[3] = x1.w;
+        vc[0] = x2.x; vc[1] = x2.y; vc[2] = x2.z; vc[3] = x2.w;
+        vd[0] = x3.x; vd[1] = x3.y; vd[2] = x3.z; vd[3] = x3.w;
+      } else {
+        const uint32_t col = g * 8;
+        const uint2 x0 = lds64(vbase[b] + swz<C::kSwizzle>(row_of(2 * t) + col));
+        const uint2 x1 = lds64(vbase[b] + swz<C::kSwizzle>(row_of(2 * t + 1) + col));
+        const uint2 x2 = lds64(vbase[b] + swz<C::kSwizzle>(row_of(2 * t + 8) + col));
+        const uint2 x3 = lds64(vbase[b] + swz<C::kSwizzle>(row_of(2 * t + 9) + col));
+        va[0] = x0.x; va[1] = x0.y; vb[0] = x1.x; vb[1] = x1.y;
+        vc[0] = x2.x; vc[1] = x2.y; vd[0] = x3.x; vd[1] = x3.y;
       }
-      mma_f16(st.o[mt], a, pb0, pb1);
+#pragma unroll
+      for (int mt = 0; mt < C::kMTiles; ++mt) {
+        const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+        const uint32_t lo = __byte_perm(va[mt >> 1], vb[mt >> 1], sel);  // tokens 2t, 2t+1
+        const uint32_t hi = __byte_perm(vc[mt >> 1], vd[mt >> 1], sel);  // tokens 2t+8, 2t+9
+        uint32_t a[4];
+        a[0] = e4m3x2_to_f16x2((uint16_t)(lo & 0xFFFFu));
+        a[1] = e4m3x2_to_f16x2((uint16_t)(lo >> 16));
+        a[2] = e4m3x2_to_f16x2((uint16_t)(hi & 0xFFFFu));
+        a[3] = e4m3x2_to_f16x2((uint16_t)(hi >> 16));
+        if (valid[b] < 16) {
+          a[0] &= mlo[b]; a[1] &= mlo[b]; a[2] &= mhi[b]; a[3] &= mhi[b];
+        }
+        mma_f16(st.o[mt], a, pb0[b], pb1[b]);
+      }
     }
   }
+}
+
+// One block: decode_blocks with NB = 1.
+template <int D, int KV, bool kColMask>
+__device__ __forceinline__ void decode_block(WarpState<D>& st, const uint32_t (&qb)[D / 16][2],
+                                             uint32_t kbase, uint32_t vbase, int hsel, int valid,
+                                             float scale_log2, int lim0, int lim1) {
+  const uint32_t kb[1] = {kbase}, vb[1] = {vbase};
+  const int va[1] = {valid}, l0[1] = {lim0}, l1[1] = {lim1};
+  decode_blocks<D, KV, kColMask, 1>(st, qb, kb, vb, hsel, va, scale_log2, l0, l1);
 }
 
 // Sum l over the 8 lanes that share t (tokens g and g+8 of every block).
@@ -388,14 +441,16 @@ __device__ __forceinline__ void finish_row_sums(WarpState<D>& st) {
 }
 
 // Store a warp's state to its slice of the merge buffer: O rows of columns
-// 0..7 (stride kRedStride floats, head_size in natural order), m and l.
+// 0..ncols-1 (ncols 4 or 8; stride kRedStride floats, head_size in natural
+// order), m and l.
 template <int D, int KV>
 __device__ __forceinline__ void dump_state(const WarpState<D>& st, float* red_o, float* red_m,
-                                           float* red_l) {
+                                           float* red_l, int ncols = 8) {
   using C = DecodeCfg<D, KV>;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
   const int t = lane & 3;
+  if (2 * t >= ncols) return;
 #pragma unroll
   for (int mt = 0; mt < C::kMTiles; ++mt) {
     int d_lo, d_hi;

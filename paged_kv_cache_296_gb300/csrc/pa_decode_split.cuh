@@ -32,16 +32,18 @@
 // for the merge kernel.
 //
 // Inside a CTA the ring, the producer and the per-block step are the fixed
-// kernel's.  On the suffix line warp 4j + w of head j consumes blocks
-// w, w+4, ... of the CTA's range (stage ownership never changes across
-// segments), and at each segment end the four warps' states are merged through
-// a buffer outside the ring (the producer keeps filling the ring meanwhile).
-// On the prefix line every consumer warp reads every block for its own n-tile
-// of columns and writes its columns' partials itself.  With the fused write
-// (pa_decode_append_shared) the consumer warps write, at the CTA's start, the
-// new token of every row whose last block the CTA reads (they wait for data
-// then anyway), and the producer loads such a block only after their arrival
-// on a barrier, so the writes leave the producer's issue loop.
+// kernel's.  On the suffix line the consumer warps of a head take the blocks
+// of the CTA's range in rotation (stage ownership never changes across
+// segments); at a segment end each warp leaves its state in one of two slots
+// of a merge buffer and goes on with the next segment, and a combiner warp
+// merges the slot and writes the segment's result, so no consumer waits for
+// another.  On the prefix line the n-tile warps of a block phase read each of
+// its blocks, and at a segment end the phases' states are merged behind a
+// barrier (a prefix CTA has one or two segments).  With the fused write
+// (pa_decode_append_shared) the warp that takes a row's last block loads the
+// row's new token when the segment starts, writes it into the stage once the
+// block is in (the block as it is after the write) and into the pool, so no
+// load waits for the write.
 #pragma once
 
 #include "pa_decode_kernel.cuh"
@@ -74,15 +76,28 @@ struct SplitCfg {
   static constexpr int kConsumerWarps = 8;
   static constexpr int kWarpsPerHead = kConsumerWarps / C::kHeads;
   static constexpr int kPrefixPhases = kWarpsPerHead / 4;
-  static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+  // consumers, then the producer warp, then the combiner warp
+  static constexpr int kProducerWarp = kConsumerWarps;
+  static constexpr int kCombinerWarp = kConsumerWarps + 1;
+  static constexpr int kThreads = (kConsumerWarps + 2) * 32;
   static_assert(C::kStages % kWarpsPerHead == 0,
                 "each stage must belong to exactly one consumer warp per head");
   static constexpr int kRedBytes =
       kConsumerWarps * 8 * C::kRedStride * 4 + 2 * kConsumerWarps * 8 * 4;
   static_assert(kRedBytes >= (3 * kMaxPlanGroups + 1) * 4,
                 "the plan keeps the group arrays in the merge buffer");
+  // Suffix segments' states: two slots of 4 columns per warp when G <= 4,
+  // else one slot of 8 (the same bytes as the prefix phases' [warp][8] view).
+  __host__ __device__ static constexpr int red_slot_cols(int group) { return group <= 4 ? 4 : 8; }
+  __host__ __device__ static constexpr int red_slots(int group) { return group <= 4 ? 2 : 1; }
+  __host__ __device__ static constexpr int red_slot_floats(int group) {
+    return kConsumerWarps * red_slot_cols(group) * (C::kRedStride + 2);
+  }
+  static_assert(2 * kConsumerWarps * 4 * (C::kRedStride + 2) * 4 <= kRedBytes &&
+                    kConsumerWarps * 8 * (C::kRedStride + 2) * 4 <= kRedBytes,
+                "suffix merge slots must fit in the merge buffer");
   // Two CTAs per SM (shared memory allows no more).  The register cap this implies
-  // is per SM sub-partition: 2 x 9 warps put 5 warps on one of the four
+  // is per SM sub-partition: 2 x 10 warps put 5 warps on each of the four
   // 16K-register files, so at most 96 registers a thread.
   static constexpr int kMinCtasPerSm = 2;
   // Suffix segments' query rows (H heads x up to 8 query heads x D, q's
@@ -90,11 +105,11 @@ struct SplitCfg {
   static constexpr int kQSlots = 2;
   static constexpr int kQSlotBytes = C::kHeads * 8 * D * 2;
   // ring (1024-aligned) | merge buffer | query slots | barriers (ring full and
-  // empty, slot full and empty) | plan arrays
+  // empty, query slot full and empty, merge slot full and empty) | plan arrays
   static constexpr int kRedOffset = C::kRingBytes;
   static constexpr int kQOffset = kRedOffset + kRedBytes;
   static constexpr int kBarOffset = kQOffset + kQSlots * kQSlotBytes;
-  static constexpr int kPlanOffset = kBarOffset + (2 * C::kStages + 2 * kQSlots) * 8;
+  static constexpr int kPlanOffset = kBarOffset + (2 * C::kStages + 2 * kQSlots + 4) * 8;
   __host__ __device__ static constexpr size_t smem_bytes(int num_seqs, int num_groups) {
     return 1024 + (size_t)kPlanOffset + split_smem_plan_bytes(num_seqs, num_groups);
   }
@@ -159,6 +174,74 @@ __device__ __forceinline__ void consumer_bar(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
+// A sequence's new token for KV head kvh (append_kv), held by one warp: lane
+// i < 2 x D/8 has 16 source bytes (the K row's pieces, then the V row's), with
+// the slot it goes to and the block the row's last table entry names.
+struct NewToken {
+  uint4 x;
+  long long slot;  // < 0: nothing is written
+  int blk;
+};
+
+// The loads are independent of one another, so they are in flight together.
+template <int D>
+__device__ __forceinline__ NewToken load_new_token(const DecodeParams& p, int seq, int kvh, int L,
+                                                   int last_entry) {
+  constexpr int kPieces = D / 8;
+  const int lane = threadIdx.x & 31;
+  NewToken tk;
+  tk.x = make_uint4(0u, 0u, 0u, 0u);
+  tk.slot = -1;
+  tk.blk = -1;
+  if (L <= 0 || kvh >= p.num_kv_heads) return tk;
+  tk.slot = p.slot_mapping[seq];
+  tk.blk = p.block_tables[(size_t)seq * p.max_blocks_per_seq + last_entry];
+  if (lane < 2 * kPieces) {
+    const int isv = lane / kPieces;
+    const int j = lane - isv * kPieces;
+    tk.x = *reinterpret_cast<const uint4*>((isv ? p.v_new : p.k_new) +
+                                           (size_t)seq * p.src_stride_bytes +
+                                           (size_t)kvh * D * 2 + (size_t)j * 16);
+  }
+  return tk;
+}
+
+// Write the token into the pool (the bytes append_rows writes) and, when its
+// slot lies in the block just loaded into `stage` (the row's last), into the
+// stage's row slot % 16 of head hsel: the block then reads as it does after
+// the write.  A slot outside the pool writes nothing.
+template <int D, int KV, int QT>
+__device__ __forceinline__ void write_new_token(const DecodeParams& p, const NewToken& tk, int kvh,
+                                                int hsel, uint8_t* stage) {
+  using C = DecodeCfg<D, KV>;
+  constexpr int kPieces = D / 8;
+  constexpr int kDstPiece = (KV == kKvE4m3) ? 8 : 16;
+  const int lane = threadIdx.x & 31;
+  const long long pool_rows = (long long)p.num_blocks * 16;
+  if (tk.slot >= 0 && tk.slot < pool_rows && lane < 2 * kPieces) {
+    const int isv = lane / kPieces;
+    const int j = lane - isv * kPieces;
+    uint8_t* dst = (isv ? p.v_cache : p.k_cache) +
+                   (size_t)tk.slot * (2ull * p.num_kv_heads * C::kRowBytes) +
+                   (size_t)kvh * C::kRowBytes + (size_t)j * kDstPiece;
+    uint8_t* sdst = nullptr;
+    if (tk.slot / 16 == tk.blk) {
+      const int row = (int)(tk.slot & 15);
+      sdst = stage + (isv ? C::kTileBytes : 0) +
+             swz<C::kSwizzle>((uint32_t)((row * C::kHeads + hsel) * C::kRowBytes + j * kDstPiece));
+    }
+    if constexpr (KV != kKvE4m3) {
+      *reinterpret_cast<uint4*>(dst) = tk.x;
+      if (sdst) *reinterpret_cast<uint4*>(sdst) = tk.x;
+    } else {
+      const uint2 c = quantize8_e4m3<QT>(tk.x, p.kv_scale);
+      *reinterpret_cast<uint2*>(dst) = c;
+      if (sdst) *reinterpret_cast<uint2*>(sdst) = c;
+    }
+  }
+  __syncwarp();  // the stage row is written before any lane reads the block
+}
+
 template <int D, int KV, int QT, bool kAppend>
 __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kMinCtasPerSm)
     paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -180,10 +263,10 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
   uint64_t* empty_bar = full_bar + C::kStages;
   uint64_t* qfull_bar = empty_bar + C::kStages;
   uint64_t* qempty_bar = qfull_bar + SC::kQSlots;
+  uint64_t* rfull_bar = qempty_bar + SC::kQSlots;   // [2] merge slot written by the consumers
+  uint64_t* rempty_bar = rfull_bar + 2;             // [2] merge slot read by the combiner
   uint8_t* qslots = smem + SC::kQOffset;
   __shared__ int qslot_len[SC::kQSlots];
-  // rows whose fused writes of new tokens are finished (see below)
-  __shared__ unsigned appended;
   __shared__ int abort_flag;
 
   const int B = p.num_seqs;
@@ -196,7 +279,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
   int* sJ = sG + B;                                          // [B]
   int* sUp = sJ + B;                                         // [NG+1]
 
-  if (threadIdx.x == kConsumerWarps * 32) {
+  if (threadIdx.x == SC::kProducerWarp * 32) {
     tma_prefetch_desc(&tmap_k);
     tma_prefetch_desc(&tmap_v);
   }
@@ -225,10 +308,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
       gMax[g] = 0;
     }
   }
-  if (tid == 0) {
-    abort_flag = 0;
-    appended = 0;
-  }
+  if (tid == 0) abort_flag = 0;
   __syncthreads();
   // Groups: each member's suffix starts after the group's shared blocks.  A
   // group's prefix row has n_g = min(shared blocks, the longest member's
@@ -273,11 +353,11 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
   } else if (Ts == 0) {
     n_pre = Skv;
   } else {
-    // a prefix unit costs its CTA 4 / (4 x phases) warp passes per block more
-    // than a suffix unit: count it double with one phase, once with two.  On
-    // the shared-prefix sampling batch (16-bit) weights of 3/4, 7/8, 9/8 and
-    // 11/8 gave 61.0, 57.7, 59.0 and 61.1 us per step against 56.8 for 1.
-    const long long wp = (long long)(2 / SC::kPrefixPhases) * Tp;
+    // A prefix unit costs its CTA more than a suffix unit: four n-tile warp
+    // passes per block, shared by 4 x phases warps.  With one phase (E4M3) it
+    // counts double; with two (16-bit) 5/4, the best of 1, 5/4 and 3/2 on the
+    // shared-prefix sampling batch on GB300 (55.9, 52.1 and 54.0 us per step).
+    const long long wp = SC::kPrefixPhases == 2 ? (5LL * Tp) / 4 : 2LL * Tp;
     n_pre = (int)(((long long)Skv * wp + (wp + Ts) / 2) / (wp + Ts));
     n_pre = min(max(n_pre, 1), Skv - 1);
   }
@@ -325,15 +405,18 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
       mbar_init(&qfull_bar[q], 1);
       mbar_init(&qempty_bar[q], kConsumerWarps);
     }
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(&rfull_bar[r], kConsumerWarps);
+      mbar_init(&rempty_bar[r], 1);
+    }
     mbar_fence_init();
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
+  if (warp == SC::kProducerWarp) {
     // ------------------------------------------------------------ producer
     const uint64_t kv_policy = l2_evict_first_policy();  // the KV stream is read once
     bool ok = true;
-    int row_ends = 0;
     int nseg = 0;  // suffix segments so far: segment k uses query slot k % kQSlots
     int issued = 0;
     int it = 0;
@@ -351,11 +434,6 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
           if (s >= 0 && s < B) seq = s;
         }
       }
-      // append_kv for a sequence's new token: the consumer warps write the
-      // tokens of the CTA's row-ending segments at its start, in order (they
-      // lie in the rows' last blocks, which this CTA reads); the r-th such
-      // row's last block is loaded only once more than r rows are written.
-      const bool gate = kAppend && !pre && sg.row_end;
       if (!pre) {
         // the segment's query rows and context length, into the next slot
         const int qs = nseg % SC::kQSlots;
@@ -386,13 +464,6 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
         const int cnt = min(32, sg.nblk - base);
         for (int j = 0; j < cnt; ++j) {
           const int blk = __shfl_sync(0xffffffffu, mine, j);
-          if (gate && base + j == sg.nblk - 1) {
-            if (lane == 0 && ok && !smem_count_wait_bounded(&appended, (unsigned)row_ends, p.status)) {
-              ok = false;
-              abort_flag = 1;
-            }
-            ++row_ends;
-          }
           if (lane == 0 && ok) {
             const int s = it % C::kStages;
             const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
@@ -422,9 +493,101 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
     return;
   }
 
+  // -------------------------------------------------------------- combiner
+  if (warp == SC::kCombinerWarp) {
+    if (!pre) {
+      // Each suffix segment's result: the head's warp states from the merge
+      // slot, combined by log-sum-exp, written as the output (a sequence with
+      // no shared prefix whose whole suffix is the segment) or as a partial.
+      const int cw = SC::red_slot_cols(p.group);
+      const int R = SC::red_slots(p.group);
+      constexpr int kQuads = D / 4;
+      const int per_head = p.group * kQuads;
+      int k = 0;
+      for (int u = u_begin; u < u_end; ++k) {
+        const Segment sg = segment_at(u, u_begin, u_end, line_base, line_rows, line_first);
+        u += sg.nblk;
+        const int r = k % R;
+        if (*reinterpret_cast<volatile int*>(&abort_flag) != 0 ||
+            !mbar_wait_bounded(&rfull_bar[r], (uint32_t)(k / R) & 1u, p.status)) {
+          abort_flag = 1;
+          break;
+        }
+        const float* so = red_o + r * SC::red_slot_floats(p.group);  // [warp][cw][stride]
+        const float* sm = so + kConsumerWarps * cw * C::kRedStride;   // [warp][cw]
+        const float* sl = sm + kConsumerWarps * cw;                   // [warp][cw]
+        const int seq = sg.row;
+        const bool direct = sg.whole && sG[seq] < 0;
+        for (int idx = lane; idx < C::kHeads * per_head; idx += 32) {
+          const int hs = idx / per_head;
+          const int rem = idx - hs * per_head;
+          const int h = rem / kQuads;
+          const int d = (rem - h * kQuads) * 4;
+          const int kvh2 = my_kvg * C::kHeads + hs;
+          if (kvh2 >= p.num_kv_heads) break;
+          const int w0 = hs * kWarpsPerHead;
+          float M = -INFINITY;
+#pragma unroll
+          for (int w = w0; w < w0 + kWarpsPerHead; ++w) M = fmaxf(M, sm[w * cw + h]);
+          float num[4] = {0.f, 0.f, 0.f, 0.f}, den = 0.f;
+          if (M != -INFINITY) {
+#pragma unroll
+            for (int w = w0; w < w0 + kWarpsPerHead; ++w) {
+              const float wt = ex2_approx(__fsub_rn(sm[w * cw + h], M));
+              const float4 ov =
+                  *reinterpret_cast<const float4*>(&so[(w * cw + h) * C::kRedStride + d]);
+              num[0] = __fmaf_rn(wt, ov.x, num[0]);
+              num[1] = __fmaf_rn(wt, ov.y, num[1]);
+              num[2] = __fmaf_rn(wt, ov.z, num[2]);
+              num[3] = __fmaf_rn(wt, ov.w, num[3]);
+              den = __fmaf_rn(wt, sl[w * cw + h], den);
+            }
+          }
+          const int qh = kvh2 * p.group + h;
+          if (direct) {
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              v[e] = (den > 0.f) ? __fmul_rn(__fdiv_rn(num[e], den), p.out_scale) : 0.f;
+            uint2 pk;
+            if constexpr (QT == kKvF16) {
+              pk.x = pack_f16x2(v[0], v[1]);
+              pk.y = pack_f16x2(v[2], v[3]);
+            } else {
+              pk.x = pack_bf16x2(v[0], v[1]);
+              pk.y = pack_bf16x2(v[2], v[3]);
+            }
+            *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) +
+                                      ((size_t)seq * p.num_q_heads + qh) * D + d) = pk;
+          } else {
+            size_t pi;
+            float *pm, *pl, *po;
+            if (sg.whole) {  // a member's whole suffix
+              pi = (size_t)B * p.num_q_heads + (size_t)seq * p.num_q_heads + qh;
+              pm = p.whole_m; pl = p.whole_l; po = p.whole_o;
+            } else {
+              pi = ((size_t)blockIdx.x * 2 + (sg.first ? 0 : 1)) * p.cut_cols + hs * p.group + h;
+              pm = p.cut_m; pl = p.cut_l; po = p.cut_o;
+            }
+            *reinterpret_cast<float4*>(po + pi * D + d) =
+                make_float4(num[0], num[1], num[2], num[3]);
+            if (d == 0) {
+              pm[pi] = M;
+              pl[pi] = den;
+            }
+          }
+        }
+        __syncwarp();  // every lane has read the slot
+        if (lane == 0) mbar_arrive(&rempty_bar[r]);
+      }
+    }
+    griddep_launch_dependents();
+    return;
+  }
+
   // -------------------------------------------------------------- consumers
   const int hsel = warp / kWarpsPerHead;
-  const int wq = warp % kWarpsPerHead;  // suffix: block phase; prefix: n-tile + 4 x phase
+  const int wq = warp % kWarpsPerHead;  // suffix: block rotation; prefix: n-tile + 4 x phase
   const int g = lane >> 2;
   const int t = lane & 3;
   float* my_o = red_o + warp * 8 * C::kRedStride;
@@ -433,43 +596,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
   WarpState<D> st;
   uint32_t qb[C::kMTiles][2];
   int it0 = 0;
-
-  if constexpr (kAppend) {
-    // The new token of every row whose last block this CTA reads, written by
-    // all consumer threads together, kAppendBatch rows at a time in segment
-    // order (append_rows: the loads of a thread's pieces are issued together,
-    // then the stores and a proxy fence); after each batch a barrier and a
-    // release addition to `appended` let the producer load those rows' last
-    // blocks.
-    constexpr int kAppendBatch = 64;
-    __shared__ int arow[kAppendBatch];
-    __shared__ int acount;
-    __shared__ int anext;
-    if (!pre) {
-      int u_scan = u_begin;
-      for (;;) {
-        if (tid == 0) {
-          int n = 0;
-          int u = u_scan;
-          while (u < u_end && n < kAppendBatch) {
-            const Segment sg = segment_at(u, u_begin, u_end, line_base, line_rows, line_first);
-            if (sg.row_end) arow[n++] = sg.row;
-            u += sg.nblk;
-          }
-          acount = n;
-          anext = u;
-        }
-        consumer_bar(kConsumerThreads);
-        const int n = acount;
-        u_scan = anext;
-        if (n > 0) append_rows<D, KV, QT>(p, arow, n, my_kvg * C::kHeads, tid, kConsumerThreads);
-        consumer_bar(kConsumerThreads);  // the writes, and the reads of arow, are done
-        if (n > 0 && tid == 0) smem_count_release(&appended, (unsigned)n);
-        if (n == 0 || u_scan >= u_end) break;
-      }
-    }
-  }
-  int nseg = 0;  // suffix segments so far (query slot nseg % kQSlots)
+  int nseg = 0;  // suffix segments so far: query slot nseg % kQSlots, merge slot nseg % R
 
   for (int u = u_begin; u < u_end;) {
     Segment sg = segment_at(u, u_begin, u_end, line_base, line_rows, line_first);
@@ -479,35 +606,46 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
     if (!pre) {
       // ------------------------------------------------ suffix line
       const int seq = sg.row;
+      const int sidx = nseg++;
       const bool live = kvh < p.num_kv_heads && g < p.group;
       // the segment's query rows and length, prefetched by the producer
-      const int qs = nseg % SC::kQSlots;
+      const int qs = sidx % SC::kQSlots;
       bool aborted = *reinterpret_cast<volatile int*>(&abort_flag) != 0;
       if (!aborted &&
-          !mbar_wait_bounded(&qfull_bar[qs], (uint32_t)(nseg / SC::kQSlots) & 1u, p.status)) {
+          !mbar_wait_bounded(&qfull_bar[qs], (uint32_t)(sidx / SC::kQSlots) & 1u, p.status)) {
         abort_flag = 1;
         aborted = true;
       }
-      ++nseg;
       load_q_frag<D, KV, QT>(qb, qslots + qs * SC::kQSlotBytes,
                              (size_t)(hsel * p.group + (live ? g : 0)) * D, live && !aborted);
+      const int L = qslot_len[qs];
       // tokens from the segment's first block to the context's end (the last
       // block of a row may be partial)
-      const int seg_ntok = qslot_len[qs] - 16 * sg.b0;
-      // release the slot (generic reads before the next bulk copy's writes)
+      const int seg_ntok = L - 16 * sg.b0;
+      // block k of the segment sits at ring position it0 + k; this warp takes
+      // the positions that are wq mod kWarpsPerHead, as in the fixed kernel
+      const int k_first = (wq - it0) & (kWarpsPerHead - 1);
+      const int k_last = sg.nblk - 1;
+      // the fused write of the row's new token, by the warp of its last block
+      const bool tok_mine = kAppend && sg.row_end && !aborted &&
+                            ((k_last - k_first) & (kWarpsPerHead - 1)) == 0;
+      NewToken tk;
+      tk.slot = -1;
+      if (tok_mine) tk = load_new_token<D>(p, seq, kvh, L, sg.b0 + k_last);
+      // release the query slot (generic reads before the next bulk copy's writes)
       fence_proxy_async_shared();
       __syncwarp();
       if (lane == 0) mbar_arrive(&qempty_bar[qs]);
-      // block k of the segment sits at ring position it0 + k; this warp takes
-      // the positions that are wq mod 4, as in the fixed kernel
-      for (int k = (wq - it0) & (kWarpsPerHead - 1); k < sg.nblk && !aborted;
-           k += kWarpsPerHead) {
+      for (int k = k_first; k < sg.nblk && !aborted; k += kWarpsPerHead) {
         const int it = it0 + k;
         const int s = it % C::kStages;
         if (!mbar_wait_bounded(&full_bar[s], (uint32_t)(it / C::kStages) & 1u, p.status)) {
           abort_flag = 1;
+          aborted = true;
           break;
         }
+        if (tok_mine && k == k_last)
+          write_new_token<D, KV, QT>(p, tk, kvh, hsel, smem + s * C::kStageBytes);
         const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
         decode_block<D, KV, false>(st, qb, kbase, kbase + C::kTileBytes, hsel,
                                    min(16, seg_ntok - 16 * k), p.scale_log2, 16, 16);
@@ -516,71 +654,23 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
         if (lane == 0) mbar_arrive(&empty_bar[s]);
       }
       finish_row_sums(st);
-      dump_state<D, KV>(st, my_o, my_m, my_l);
-      consumer_bar(kConsumerThreads);
-      // Merge each head's four warp states and write the segment's result.
-      const bool direct = sg.whole && sG[seq] < 0;
-      constexpr int kQuads = D / 4;
-      const int per_head = p.group * kQuads;
-      for (int idx = tid; idx < C::kHeads * per_head; idx += kConsumerThreads) {
-        const int hs = idx / per_head;
-        const int rem = idx - hs * per_head;
-        const int h = rem / kQuads;
-        const int d = (rem - h * kQuads) * 4;
-        const int kvh2 = sg.kvg * C::kHeads + hs;
-        if (kvh2 >= p.num_kv_heads) break;
-        const int w0 = hs * kWarpsPerHead;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = w0; w < w0 + kWarpsPerHead; ++w) M = fmaxf(M, red_m[w * 8 + h]);
-        float num[4] = {0.f, 0.f, 0.f, 0.f}, den = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int w = w0; w < w0 + kWarpsPerHead; ++w) {
-            const float wt = ex2_approx(__fsub_rn(red_m[w * 8 + h], M));
-            const float4 ov =
-                *reinterpret_cast<const float4*>(&red_o[(w * 8 + h) * C::kRedStride + d]);
-            num[0] = __fmaf_rn(wt, ov.x, num[0]);
-            num[1] = __fmaf_rn(wt, ov.y, num[1]);
-            num[2] = __fmaf_rn(wt, ov.z, num[2]);
-            num[3] = __fmaf_rn(wt, ov.w, num[3]);
-            den = __fmaf_rn(wt, red_l[w * 8 + h], den);
-          }
-        }
-        const int qh = kvh2 * p.group + h;
-        if (direct) {
-          float v[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            v[k] = (den > 0.f) ? __fmul_rn(__fdiv_rn(num[k], den), p.out_scale) : 0.f;
-          uint2 pk;
-          if constexpr (QT == kKvF16) {
-            pk.x = pack_f16x2(v[0], v[1]);
-            pk.y = pack_f16x2(v[2], v[3]);
-          } else {
-            pk.x = pack_bf16x2(v[0], v[1]);
-            pk.y = pack_bf16x2(v[2], v[3]);
-          }
-          *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) +
-                                    ((size_t)seq * p.num_q_heads + qh) * D + d) = pk;
-        } else {
-          size_t pi;
-          float *pm, *pl, *po;
-          if (sg.whole) {  // a member's whole suffix
-            pi = (size_t)B * p.num_q_heads + (size_t)seq * p.num_q_heads + qh;
-            pm = p.whole_m; pl = p.whole_l; po = p.whole_o;
-          } else {
-            pi = ((size_t)blockIdx.x * 2 + (sg.first ? 0 : 1)) * p.cut_cols + hs * p.group + h;
-            pm = p.cut_m; pl = p.cut_l; po = p.cut_o;
-          }
-          *reinterpret_cast<float4*>(po + pi * D + d) = make_float4(num[0], num[1], num[2], num[3]);
-          if (d == 0) {
-            pm[pi] = M;
-            pl[pi] = den;
-          }
-        }
+      // Leave the state in the segment's merge slot for the combiner warp and
+      // go on (the slot is free once the combiner has read its last use).
+      const int R = SC::red_slots(p.group);
+      const int cw = SC::red_slot_cols(p.group);
+      const int r = sidx % R;
+      if (!aborted &&
+          !mbar_wait_bounded(&rempty_bar[r], ((uint32_t)(sidx / R) & 1u) ^ 1u, p.status)) {
+        abort_flag = 1;
+        aborted = true;
       }
-      consumer_bar(kConsumerThreads);  // the buffer is free for the next segment
+      if (aborted) break;  // no barrier follows on this line
+      float* so = red_o + r * SC::red_slot_floats(p.group);
+      float* sm = so + kConsumerWarps * cw * C::kRedStride;
+      dump_state<D, KV>(st, so + warp * cw * C::kRedStride, sm + warp * cw,
+                        sm + kConsumerWarps * cw + warp * cw, cw);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rfull_bar[r]);
     } else {
       // ------------------------------------------------ prefix line
       const int o0 = min(max(p.grp_off[sg.row], 0), n_members);
@@ -614,27 +704,57 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
       const int l1c = lim[1] < 0 ? (1 << 30) : lim[1];
       const bool need_mask = __any_sync(0xffffffffu, l0c < seg_tok_end || l1c < seg_tok_end);
       const bool aborted = *reinterpret_cast<volatile int*>(&abort_flag) != 0;
-      for (int k = (phase - it0) & (SC::kPrefixPhases - 1); k < sg.nblk && !aborted;
-           k += SC::kPrefixPhases) {
-        const int it = it0 + k;
-        const int s = it % C::kStages;
-        if (!mbar_wait_bounded(&full_bar[s], (uint32_t)(it / C::kStages) & 1u, p.status)) {
+      // Blocks of this warp's phase two at a time over a 16-bit cache (their
+      // MMA chains interleave and they share one softmax step), an odd last
+      // one alone; one at a time over E4M3 (whose widening needs the registers).
+      constexpr int kStep = SC::kPrefixPhases;
+      constexpr bool kPairs = (KV != kKvE4m3);
+      int k = (phase - it0) & (kStep - 1);
+      while (k < sg.nblk && !aborted) {
+        const bool two = kPairs && k + kStep < sg.nblk;
+        const int itA = it0 + k;
+        const int itB = itA + kStep;
+        const int sA = itA % C::kStages;
+        const int sB = itB % C::kStages;
+        if (!mbar_wait_bounded(&full_bar[sA], (uint32_t)(itA / C::kStages) & 1u, p.status) ||
+            (two &&
+             !mbar_wait_bounded(&full_bar[sB], (uint32_t)(itB / C::kStages) & 1u, p.status))) {
           abort_flag = 1;
           break;
         }
-        const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
-        const int tok0 = 16 * (sg.b0 + k);
-        const int valid = min(16, vmax - tok0);
-        if (need_mask) {
-          decode_block<D, KV, true>(st, qb, kbase, kbase + C::kTileBytes, hsel, valid,
-                                    p.scale_log2, l0c - tok0, l1c - tok0);
+        const uint32_t kA = smem_u32(smem + sA * C::kStageBytes);
+        const uint32_t kB = smem_u32(smem + sB * C::kStageBytes);
+        const int tokA = 16 * (sg.b0 + k);
+        const int tokB = tokA + 16 * kStep;
+        if (two) {
+          const uint32_t kb[2] = {kA, kB};
+          const uint32_t vb[2] = {kA + C::kTileBytes, kB + C::kTileBytes};
+          const int va[2] = {min(16, vmax - tokA), min(16, vmax - tokB)};
+          if (need_mask) {
+            const int m0[2] = {l0c - tokA, l0c - tokB};
+            const int m1[2] = {l1c - tokA, l1c - tokB};
+            decode_blocks<D, KV, true, 2>(st, qb, kb, vb, hsel, va, p.scale_log2, m0, m1);
+          } else {
+            const int full[2] = {16, 16};
+            decode_blocks<D, KV, false, 2>(st, qb, kb, vb, hsel, va, p.scale_log2, full, full);
+          }
         } else {
-          decode_block<D, KV, false>(st, qb, kbase, kbase + C::kTileBytes, hsel, valid,
-                                     p.scale_log2, 16, 16);
+          const int valid = min(16, vmax - tokA);
+          if (need_mask) {
+            decode_block<D, KV, true>(st, qb, kA, kA + C::kTileBytes, hsel, valid, p.scale_log2,
+                                      l0c - tokA, l1c - tokA);
+          } else {
+            decode_block<D, KV, false>(st, qb, kA, kA + C::kTileBytes, hsel, valid,
+                                       p.scale_log2, 16, 16);
+          }
         }
         fence_proxy_async_shared();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        if (lane == 0) {
+          mbar_arrive(&empty_bar[sA]);
+          if (two) mbar_arrive(&empty_bar[sB]);
+        }
+        k += two ? 2 * kStep : kStep;
       }
       finish_row_sums(st);
       // The block phases' states of each n-tile merge into its 8 columns'
