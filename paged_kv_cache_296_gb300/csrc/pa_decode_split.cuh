@@ -62,9 +62,11 @@ __host__ __device__ constexpr size_t split_plan_ints(int num_seqs) {
   return (size_t)kPlanHeader + kPlanSeqInts * (size_t)num_seqs;
 }
 
-// Shared-memory plan arrays (ints): sU[B+1], sP[B], sG[B], sJ[B], sUp[NG+1].
+// Shared-memory plan arrays (ints): sU[B+1], sP[B], sG[B], sJ[B], sUp[NG+1],
+// and the inputs the CTAs read again: sL[B] (context lengths), sGo[2 NG]
+// (each group's member range) and sMem[B] (member sequences, -1 if invalid).
 __host__ __device__ constexpr size_t split_smem_plan_bytes(int num_seqs, int num_groups) {
-  return (4 * (size_t)num_seqs + (size_t)num_groups + 2) * 4;
+  return (6 * (size_t)num_seqs + 3 * (size_t)num_groups + 2) * 4;
 }
 
 template <int D, int KV>
@@ -278,6 +280,9 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
   int* sG = sP + B;                                          // [B]
   int* sJ = sG + B;                                          // [B]
   int* sUp = sJ + B;                                         // [NG+1]
+  int* sL = sUp + NG + 1;                                    // [B]
+  int* sGo = sL + B;                                         // [2 NG]
+  int* sMem = sGo + 2 * NG;                                  // [B]
 
   if (threadIdx.x == SC::kProducerWarp * 32) {
     tma_prefetch_desc(&tmap_k);
@@ -296,6 +301,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
   int* gMax = gBlk + NG;                      // [NG] longest member, in blocks
   for (int i = tid; i < B; i += kT) {
     const int L = min(max(p.context_lens[i], 0), cap);
+    sL[i] = L;
     sU[i + 1] = (L + 15) >> 4;  // the sequence's blocks, for now
     sP[i] = 0;
     sG[i] = -1;
@@ -315,8 +321,14 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
   // blocks) units.  Members past the columns a prefix CTA has (32 / G per KV
   // head) are left out of the group: their whole context is suffix.  One
   // (group, member slot) pair per item.
+  // (A valid input lists each sequence at most once, so at most B members.)
   const int max_members = kPrefixCols / p.group;
-  const int n_members = NG > 0 ? max(0, gOff[NG]) : 0;
+  const int n_members = NG > 0 ? min(max(0, gOff[NG]), B) : 0;
+  for (int g = tid; g < NG; g += kT) {
+    const int o0 = min(max(gOff[g], 0), n_members);
+    sGo[2 * g] = o0;
+    sGo[2 * g + 1] = min(max(gOff[g + 1], o0), min(n_members, o0 + max_members));
+  }
   for (int item = tid; item < NG * max_members; item += kT) {
     const int g = item / max_members;
     const int j = item - g * max_members;
@@ -324,6 +336,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
     const int o1 = min(max(gOff[g + 1], o0), min(n_members, o0 + max_members));
     if (o0 + j >= o1) continue;
     const int s = p.grp_seq[o0 + j];
+    sMem[o0 + j] = (s >= 0 && s < B) ? s : -1;
     if (s < 0 || s >= B) continue;
     atomicMax(&gMax[g], sU[s + 1]);
     sP[s] = gBlk[g];
@@ -426,13 +439,10 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
       int seq = sg.row;
       if (pre) {
         // the table of the group's first listed sequence (all members share these blocks)
-        const int o0 = min(max(p.grp_off[sg.row], 0), n_members);
-        const int o1 = min(max(p.grp_off[sg.row + 1], o0), min(n_members, o0 + max_members));
+        const int o0 = sGo[2 * sg.row];
+        const int o1 = sGo[2 * sg.row + 1];
         seq = -1;
-        for (int k = o0; k < o1 && seq < 0; ++k) {
-          const int s = p.grp_seq[k];
-          if (s >= 0 && s < B) seq = s;
-        }
+        for (int k = o0; k < o1 && seq < 0; ++k) seq = sMem[k];
       }
       if (!pre) {
         // the segment's query rows and context length, into the next slot
@@ -446,7 +456,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
             const int kv0 = sg.kvg * C::kHeads;
             const uint32_t bytes =
                 (uint32_t)(min(C::kHeads, p.num_kv_heads - kv0) * p.group * D * 2);
-            qslot_len[qs] = min(max(p.context_lens[seq], 0), cap);
+            qslot_len[qs] = sL[seq];
             mbar_arrive_expect_tx(&qfull_bar[qs], bytes);
             bulk_load(qslots + qs * SC::kQSlotBytes,
                       reinterpret_cast<const uint16_t*>(p.q) +
@@ -673,8 +683,8 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
       if (lane == 0) mbar_arrive(&rfull_bar[r]);
     } else {
       // ------------------------------------------------ prefix line
-      const int o0 = min(max(p.grp_off[sg.row], 0), n_members);
-      const int o1 = min(max(p.grp_off[sg.row + 1], o0), min(n_members, o0 + max_members));
+      const int o0 = sGo[2 * sg.row];
+      const int o1 = sGo[2 * sg.row + 1];
       const int mcnt = o1 - o0;
       const bool kv_live = kvh < p.num_kv_heads;
       const int nt = wq % 4;                     // this warp's n-tile of 8 columns
@@ -682,7 +692,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
       // B operand: this lane's column 8 nt + g -> member, query head of the group
       const int cb = 8 * nt + g;
       const int jb = cb / p.group;
-      const int sb = (jb < mcnt) ? p.grp_seq[o0 + jb] : -1;
+      const int sb = (jb < mcnt) ? sMem[o0 + jb] : -1;
       const bool bl = kv_live && sb >= 0 && sb < B;
       load_q_frag<D, KV, QT>(
           qb, p.q, ((size_t)(bl ? sb : 0) * p.num_q_heads + kvh * p.group + cb % p.group) * D, bl);
@@ -691,8 +701,8 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int j = (8 * nt + 2 * t + c) / p.group;
-        const int s = (j < mcnt) ? p.grp_seq[o0 + j] : -1;
-        lim[c] = (s >= 0 && s < B && kv_live) ? min(max(p.context_lens[s], 0), cap) : -1;
+        const int s = (j < mcnt) ? sMem[o0 + j] : -1;
+        lim[c] = (s >= 0 && kv_live) ? sL[s] : -1;
       }
       // tokens past every live column's length are masked for the whole warp
       int vmax = max(lim[0], lim[1]);
@@ -771,7 +781,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
         const int j = col / p.group;
         const int kvh2 = sg.kvg * C::kHeads + hs;
         if (j >= mcnt || kvh2 >= p.num_kv_heads) continue;
-        const int sq = p.grp_seq[o0 + j];
+        const int sq = sMem[o0 + j];
         if (sq < 0 || sq >= B) continue;
         const int c = col % 8;
         const int w0 = hs * kWarpsPerHead + col / 8;  // phase 0's warp of this n-tile
