@@ -69,8 +69,8 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 PREFILL_METRIC = "paged-prefill TFLOP/s (causal attention FLOPs); µs per prefill step"
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-KERNEL_SOURCES = ["pa_decode_kernel.cuh", "pa_ptx.cuh", "pa_decode_launch.cuh", "pa_cache.cu",
-                  "pa_decode_f16.cu", "pa_decode_bf16.cu", "pa_decode_e4m3.cu"]
+KERNEL_SOURCES = ["pa_decode_kernel.cuh", "pa_decode_split.cuh", "pa_ptx.cuh", "pa_decode_launch.cuh",
+                  "pa_cache.cu", "pa_decode_f16.cu", "pa_decode_bf16.cu", "pa_decode_e4m3.cu"]
 
 
 # ---------------------------------------------------------------- helpers
