@@ -128,8 +128,8 @@ def tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback bf16"
 
 
-PREFILL_SOURCES = ["pa_prefill_tc.cuh", "pa_prefill_params.cuh", "pa_prefill_launch.cuh", "pa_prefill.cu",
-                   "pa_prefill_fp8.cu", "pa_ptx.cuh", "pa_cache.cu"]
+PREFILL_SOURCES = ["pa_prefill_tc.cuh", "pa_tcgen05.cuh", "pa_prefill_params.cuh", "pa_prefill_launch.cuh",
+                   "pa_prefill.cu", "pa_prefill_fp8.cu", "pa_ptx.cuh", "pa_cache.cu"]
 
 
 def kernel_source_hash(sources=None):

@@ -111,21 +111,9 @@ cudaError_t split_slots(int dev, size_t smem, int* slots) {
 
 template <int D, int KV, int QT, bool kAppend>
 cudaError_t launch_split(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
-                         const DecodeArgs& a, cudaStream_t stream, int dev, const char** why) {
+                         const DecodeArgs& a, cudaStream_t stream, int dev) {
   using C = DecodeCfg<D, KV>;
   using SC = SplitCfg<D, KV>;
-  // The tensor-core prefix line (16-bit caches) loads blocks through the
-  // pool's piece-major view: a box is one 128-byte piece of 16 token rows.
-  alignas(64) CUtensorMap tkp = tk;
-  alignas(64) CUtensorMap tvp = tv;
-  if constexpr (KV != kKvE4m3) {
-    if (!encode_kv_tensor_map_planes(&tkp, a.k_cache, a.num_blocks, a.num_kv_heads, D, 2, 1,
-                                     why) ||
-        !encode_kv_tensor_map_planes(&tvp, a.v_cache, a.num_blocks, a.num_kv_heads, D, 2, 1,
-                                     why)) {
-      return cudaErrorInvalidValue;
-    }
-  }
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = smem_opt_in(paged_decode_split_kernel<D, KV, QT, kAppend>,
                               (int)SC::smem_bytes(kMaxPlanSeqs, kMaxPlanGroups), attr_done, dev);
@@ -139,7 +127,7 @@ cudaError_t launch_split(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
   const int grid = std::max(slots, 2 * p.kv_groups);
   cudaLaunchAttribute attr;
   cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)grid), dim3(SC::kThreads), smem, stream, &attr);
-  e = cudaLaunchKernelEx(&cfg, paged_decode_split_kernel<D, KV, QT, kAppend>, tk, tv, tkp, tvp, p);
+  e = cudaLaunchKernelEx(&cfg, paged_decode_split_kernel<D, KV, QT, kAppend>, tk, tv, p);
   if (e != cudaSuccess) return e;
   const long long rows = (long long)a.num_seqs * a.num_q_heads;
   cudaLaunchConfig_t mcfg =
@@ -210,8 +198,8 @@ cudaError_t launch_decode_instance(const DecodeArgs& a, cudaStream_t stream, con
   p.whole_l = a.whole_l;
   p.whole_o = a.whole_o;
   p.plan = a.plan;
-  if (a.append) return launch_split<D, KV, QT, true>(tk, tv, p, a, stream, dev, why);
-  return launch_split<D, KV, QT, false>(tk, tv, p, a, stream, dev, why);
+  if (a.append) return launch_split<D, KV, QT, true>(tk, tv, p, a, stream, dev);
+  return launch_split<D, KV, QT, false>(tk, tv, p, a, stream, dev);
 }
 
 }  // namespace pa

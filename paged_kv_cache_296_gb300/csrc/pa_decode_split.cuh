@@ -47,8 +47,6 @@
 #pragma once
 
 #include "pa_decode_kernel.cuh"
-#include "pa_decode_prefix_tc.cuh"
-#include "pa_decode_segment.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -119,10 +117,6 @@ struct SplitCfg {
   }
 };
 
-// The cost of a prefix unit on the tensor-core prefix line relative to a
-// suffix unit, in eighths (splits a head group's CTAs between the lines).
-constexpr int kTcPrefixWeight = 8;
-
 // Exclusive scan in place: on entry a[1..n] hold counts, on exit a[i] is the
 // sum of the first i counts (a[0] = 0).  One warp.
 __device__ __forceinline__ void warp_scan_counts(int* a, int n) {
@@ -140,6 +134,42 @@ __device__ __forceinline__ void warp_scan_counts(int* a, int n) {
     carry += __shfl_sync(0xffffffffu, v, 31);
   }
   if (lane == 0) a[0] = 0;
+}
+
+// The segment of a line that starts at unit u (u inside the line, u < end).
+struct Segment {
+  int row;            // sequence (suffix line) or group (prefix line)
+  int kvg;            // KV head group
+  int b0;             // first block, counted from the row's first (shared) block
+  int nblk;           // blocks in the segment
+  bool whole;         // the segment is its row's whole range
+  bool first;         // the segment starts the CTA's range (cut slot 0, else 1)
+  bool row_end;       // the segment reaches its row's last block
+};
+
+// The segment of a KV head group's line that starts at unit u (u < u_end).
+// Unit counts fit in 32 bits: the host admits a call only if (sequences +
+// groups) x max_blocks_per_seq x num_kv_heads < 2^31.
+__device__ __forceinline__ Segment segment_at(int u, int u_begin, int u_end, const int* base,
+                                              int nrows, const int* first_blk) {
+  // the row r with base[r] <= u < base[r + 1] (rows of no units skipped)
+  int lo = 0, hi = nrows - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (base[mid + 1] > u) hi = mid; else lo = mid + 1;
+  }
+  Segment s;
+  s.row = lo;
+  s.kvg = 0;  // set by the caller: a CTA's line belongs to one KV head group
+  const int row_start = base[lo];
+  const int row_stop = base[lo + 1];
+  const int seg_end = min(row_stop, u_end);
+  s.b0 = (first_blk ? first_blk[lo] : 0) + (u - row_start);
+  s.nblk = seg_end - u;
+  s.whole = (u == row_start) && (seg_end == row_stop);
+  s.first = (u == u_begin);
+  s.row_end = (seg_end == row_stop);
+  return s;
 }
 
 __device__ __forceinline__ void consumer_bar(int nthreads) {
@@ -217,20 +247,9 @@ __device__ __forceinline__ void write_new_token(const DecodeParams& p, const New
 template <int D, int KV, int QT, bool kAppend>
 __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kMinCtasPerSm)
     paged_decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                              const __grid_constant__ CUtensorMap tmap_v,
-                              const __grid_constant__ CUtensorMap tmap_kp,
-                              const __grid_constant__ CUtensorMap tmap_vp, const DecodeParams p) {
+                              const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
   using C = DecodeCfg<D, KV>;
   using SC = SplitCfg<D, KV>;
-  // Over a 16-bit cache the prefix line runs on the 5th-generation tensor
-  // cores (pa_decode_prefix_tc.cuh; tmap_kp / tmap_vp: the pool's piece-major
-  // view); over E4M3 it runs the mma.sync steps below.
-  constexpr bool kTcPrefix = (KV != kKvE4m3);
-  static_assert(!kTcPrefix || (PrefixTcCfg<D>::kNumBars <= 2 * C::kStages + 2 * SplitCfg<D, KV>::kQSlots + 4 &&
-                               PrefixTcCfg<D>::kQBytes <= SplitCfg<D, KV>::kRedBytes &&
-                               SplitCfg<D, KV>::kRedOffset % 1024 == 0 &&
-                               C::kRingBytes >= 2 * PrefixTcCfg<D>::kSlotBytes),
-                "the tensor-core prefix line reuses the ring, the merge buffer and the barriers");
   constexpr int kT = SC::kThreads;
   constexpr int kConsumerWarps = SC::kConsumerWarps;
   constexpr int kWarpsPerHead = SC::kWarpsPerHead;
@@ -251,7 +270,6 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
   uint8_t* qslots = smem + SC::kQOffset;
   __shared__ int qslot_len[SC::kQSlots];
   __shared__ int abort_flag;
-  __shared__ uint32_t tmem_slot;
 
   const int B = p.num_seqs;
   const int NG = p.num_groups;
@@ -348,10 +366,11 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
   } else if (Ts == 0) {
     n_pre = Skv;
   } else {
-    // A prefix unit's cost relative to a suffix unit's.  Tensor-core prefix
-    // line (16-bit): kTcPrefixWeight / 8.  mma.sync prefix line (E4M3): four
-    // n-tile warp passes per block by four warps, counted double.
-    const long long wp = kTcPrefix ? ((long long)kTcPrefixWeight * Tp) / 8 : 2LL * Tp;
+    // A prefix unit costs its CTA more than a suffix unit: four n-tile warp
+    // passes per block, shared by 4 x phases warps.  With one phase (E4M3) it
+    // counts double; with two (16-bit) 5/4, the best of 1, 5/4 and 3/2 on the
+    // shared-prefix sampling batch on GB300 (55.9, 52.1 and 54.0 us per step).
+    const long long wp = SC::kPrefixPhases == 2 ? (5LL * Tp) / 4 : 2LL * Tp;
     n_pre = (int)(((long long)Skv * wp + (wp + Ts) / 2) / (wp + Ts));
     n_pre = min(max(n_pre, 1), Skv - 1);
   }
@@ -388,15 +407,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
 
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const bool tcpre = kTcPrefix && pre;
-  // the tensor-core prefix line's chunk slots in the ring and its barriers
-  const PrefixTcBars tcbars{full_bar,
-                           min(PrefixTcCfg<D>::kMaxSlots, C::kRingBytes / PrefixTcCfg<D>::kSlotBytes)};
-  if (tid == 0 && tcpre) {
-    prefix_tc_init_bars<D>(tcbars, kConsumerThreads);
-    mbar_fence_init();
-  }
-  if (tid == 0 && !tcpre) {
+  if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       // suffix line: one consumer warp per head reads a stage; prefix line:
@@ -413,60 +424,7 @@ __global__ void __launch_bounds__(SplitCfg<D, KV>::kThreads, SplitCfg<D, KV>::kM
     }
     mbar_fence_init();
   }
-  if (tcpre && warp == SC::kCombinerWarp) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&tmem_slot)),
-                 "r"(PrefixTcCfg<D>::kTmemCols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-  }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-
-  if constexpr (kTcPrefix) {
-    if (pre) {
-      // ---------------------------------------------- tensor-core prefix line
-      const uint32_t tmem = tmem_slot;
-      uint8_t* qtile = smem + SC::kRedOffset;  // 1024-aligned, kQBytes <= kRedBytes
-      const int kvh = my_kvg;                  // one KV head per CTA
-      if (warp == SC::kProducerWarp) {
-        int chunks = 0;
-        if (!prefix_tc_produce<D>(p, &tmap_kp, &tmap_vp, smem, tcbars, sUp, NG, sGo, sMem,
-                                  u_begin, u_end, kvh, &abort_flag, &chunks) &&
-            lane == 0)
-          atomicExch(&abort_flag, 1);
-        griddep_launch_dependents();
-        // never leave the CTA with copies in flight
-        if (lane == 0) {
-          for (int k = max(0, chunks - tcbars.slots); k < chunks; ++k)
-            mbar_wait_bounded(tcbars.full(k % tcbars.slots), (uint32_t)(k / tcbars.slots) & 1u,
-                              p.status);
-        }
-        return;
-      }
-      if (warp == SC::kCombinerWarp) {
-        if (lane == 0) {
-          if (!prefix_tc_mma<D, KV>(p, smem, qtile, tmem, tcbars, sUp, NG, u_begin, u_end,
-                                    &abort_flag))
-            atomicExch(&abort_flag, 1);
-          // every MMA issued has completed before TMEM is freed
-          umma_commit(tcbars.drained());
-          mbar_wait_bounded(tcbars.drained(), 0, p.status);
-        }
-        __syncwarp();
-        mbar_wait_bounded(tcbars.tfree(), 0, p.status);  // warp 0's last TMEM read
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(PrefixTcCfg<D>::kTmemCols));
-        griddep_launch_dependents();
-        return;
-      }
-      prefix_tc_consume<D, KV, QT>(p, smem, qtile, tmem, tcbars, sUp, NG, sGo, sMem, sL, u_begin,
-                                   u_end, kvh, kConsumerThreads, &abort_flag);
-      griddep_launch_dependents();
-      return;
-    }
-  }
 
   if (warp == SC::kProducerWarp) {
     // ------------------------------------------------------------ producer
