@@ -430,6 +430,131 @@ def oracle_rows_fn(W):
     return rows
 
 
+# The oracle on every host core: worker processes (spawn start, one BLAS
+# thread each) attach to the pool rows in shared memory and decode whole
+# sequences; the parent hands out sequences in turn and divides the attended
+# bytes of the finished ones by the wall time.
+_ORACLE_WORKER = {}
+
+
+def _oracle_worker_init(shm_name, shape, dtype, q_bits, tables, q_dtype, kv_dtype, scale, kv_scale):
+    from multiprocessing import shared_memory
+    shm = shared_memory.SharedMemory(name=shm_name)
+    _ORACLE_WORKER.update(shm=shm, pool=np.ndarray(shape, dtype=np.dtype(dtype), buffer=shm.buf),
+                          q=q_bits, tables=tables, q_dtype=q_dtype, kv_dtype=kv_dtype,
+                          scale=scale, kv_scale=kv_scale)
+
+
+def _oracle_worker_decode(task):
+    """One sequence (index, attended tokens): gather its rows, run the oracle."""
+    from oracle import paged_attention as ref  # test infrastructure: the CPU baseline legs only
+    i, L = task
+    o = _ORACLE_WORKER
+    nb = -(-L // 16)
+    rows = o["pool"][o["tables"][i, :nb].astype(np.int64)]
+    ref.paged_decode(o["q"][i:i + 1], o["q_dtype"], rows, np.arange(max(nb, 1))[None, :],
+                     np.array([L]), o["scale"], o["kv_dtype"], o["kv_scale"])
+    return L
+
+
+class ParallelOracleSampler:
+    """The float64 oracle over a decode workload on ``workers`` host processes.
+
+    Over a 16-bit cache only (an E4M3 pool would have to be quantised by the
+    oracle in every worker): the pool's rows as drawn go to shared memory once.
+    ``sample(seconds)`` hands out whole sequences, in turn, until ``seconds`` of
+    wall time have passed, waits for those in flight and returns (attended
+    bytes, wall seconds, sequences).
+    """
+
+    def __init__(self, W, workers):
+        import multiprocessing as mp
+        from multiprocessing import shared_memory
+        spec = W.spec
+        self.spec = spec
+        self.workers = workers
+        self.tok_bytes = spec.num_kv_heads * spec.head_size * 2 * 2
+        pool = W.pool.cpu().view(torch.int16).numpy().view(np.uint16)
+        self.shm = shared_memory.SharedMemory(create=True, size=max(pool.nbytes, 1))
+        np.ndarray(pool.shape, dtype=pool.dtype, buffer=self.shm.buf)[...] = pool
+        self.lens = W.context_lens.cpu().numpy()
+        q_bits = W.q.cpu().view(torch.int16).numpy().view(np.uint16)
+        tables = W.block_tables.cpu().numpy()
+        self.pool = mp.get_context("spawn").Pool(
+            processes=workers, initializer=_oracle_worker_init,
+            initargs=(self.shm.name, pool.shape, pool.dtype.str, q_bits, tables, spec.q_dtype,
+                      spec.kv_dtype, W.scale, W.kv_scale))
+        self.cursor = 0
+        # every worker started and warm (imports done) before any timing
+        self.pool.map(_oracle_worker_decode, [(self._next(), 16)] * workers, chunksize=1)
+
+    def _next(self):
+        i = self.cursor % self.spec.num_seqs
+        self.cursor += 1
+        return i
+
+    def sample(self, seconds):
+        pending = []
+        done_tok, n = 0, 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds or not (pending or n):
+            while len(pending) < 2 * self.workers:
+                i = self._next()
+                pending.append(self.pool.apply_async(_oracle_worker_decode,
+                                                     ((i, int(self.lens[i])),)))
+            head = pending.pop(0)
+            done_tok += head.get()
+            n += 1
+        for r in pending:
+            done_tok += r.get()
+            n += 1
+        return done_tok * self.tok_bytes, time.perf_counter() - t0, n
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+        self.shm.close()
+        self.shm.unlink()
+
+
+def shm_fits(nbytes):
+    """Whether POSIX shared memory has room for ``nbytes`` (with a margin)."""
+    try:
+        st = os.statvfs("/dev/shm")
+    except OSError:
+        return False
+    return st.f_bavail * st.f_frsize > 1.2 * nbytes
+
+
+def parallel_oracle_ok(W, cores):
+    """The parallel oracle runs over 16-bit caches, on several cores, when the
+    pool fits in shared memory; else the one-core sampler runs."""
+    return (W.spec.kv_dtype != "e4m3" and cores > 1
+            and shm_fits(W.pool.numel() * W.pool.element_size()))
+
+
+def oracle_baseline(W, seconds):
+    """The cpu_baseline block: the oracle on every host core over ``seconds`` of
+    wall time (16-bit caches), else on one core over ``seconds`` of its time."""
+    cores = os.cpu_count() or 1
+    if parallel_oracle_ok(W, cores):
+        sampler = ParallelOracleSampler(W, cores)
+        try:
+            b, secs, nseq = sampler.sample(seconds)
+        finally:
+            sampler.close()
+        where = f"{cores} worker processes (spawn), 1 BLAS thread each, wall time"
+    else:
+        b, secs, nseq = OracleSampler(W, oracle_rows_fn(W)).sample(seconds)
+        cores = 1
+        where = "1 BLAS thread, oracle time"
+    return {"value": round(b / secs / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "host_cpus": os.cpu_count(), "kind": "oracle",
+            "sample": f"float64 NumPy oracle, {nseq} sequences of this batch (all heads; a "
+                      f"sequence cut to fewer tokens only on one core, if the time budget ends "
+                      f"inside it), {secs:.1f} s, {where}"}
+
+
 # ---------------------------------------------------------------- main legs
 
 def parallelism(world, shard):
@@ -706,12 +831,7 @@ def decode_leg(args, config_id, world, rank, device, headline):
     # ---- CPU oracle baseline (rank 0, N=1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        b, secs, nseq = OracleSampler(W, oracle_rows_fn(W)).sample(args.cpu_seconds)
-        cpu = {"value": round(b / secs / 1e9, 4), "unit": "GB/s", "cores": 1,
-               "host_cpus": os.cpu_count(), "kind": "oracle",
-               "sample": f"float64 NumPy oracle, {nseq} sequences of this batch (all heads; a "
-                         f"sequence cut to fewer tokens only if the time budget ends inside it), "
-                         f"{secs:.1f} s, 1 BLAS thread"}
+        cpu = oracle_baseline(W, args.cpu_seconds)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -1261,21 +1381,38 @@ def run_reference(args, world, rank, local):
     W = wl.make_workload(spec, args.config, device="cpu")
     # the whole run holds about --ref-seconds of oracle time, whatever --steps
     per_step = args.ref_seconds / max(1, args.steps + args.warmup)
-    sampler = OracleSampler(W, oracle_rows_fn(W))
-    for _ in range(args.warmup):
-        sampler.sample(per_step)
-    tot_b, tot_s, nseq = 0, 0.0, 0
-    for _ in range(args.steps):
-        b, s, k = sampler.sample(per_step)
-        tot_b += b
-        tot_s += s
-        nseq += k
+    cores = os.cpu_count() or 1
+    parallel = parallel_oracle_ok(W, cores)
+    # every host core (16-bit caches: the pool in shared memory), else one
+    sampler = ParallelOracleSampler(W, cores) if parallel else OracleSampler(W, oracle_rows_fn(W))
+    try:
+        tot_b, tot_s, nseq = 0, 0.0, 0
+        if parallel:
+            # the workers stay busy across steps: the warm-up and the timed steps
+            # are two stretches of wall time (a per-step drain of the pool would
+            # cost more than a step's budget)
+            sampler.sample(per_step * args.warmup)
+            tot_b, tot_s, nseq = sampler.sample(per_step * args.steps)
+        else:
+            for _ in range(args.warmup):
+                sampler.sample(per_step)
+            for _ in range(args.steps):
+                b, s, k = sampler.sample(per_step)
+                tot_b += b
+                tot_s += s
+                nseq += k
+    finally:
+        if parallel:
+            sampler.close()
     value = tot_b / tot_s / 1e9
-    cpu = {"value": round(value, 4), "unit": "GB/s", "cores": 1, "host_cpus": os.cpu_count(),
-           "kind": "oracle",
-           "sample": f"float64 NumPy oracle, {nseq} sequence samples (all heads, contexts cut to "
-                     f"the per-step time budget) over {args.steps} steps "
-                     f"({tot_s:.1f} s), 1 BLAS thread"}
+    cpu = {"value": round(value, 4), "unit": "GB/s", "cores": cores if parallel else 1,
+           "host_cpus": os.cpu_count(), "kind": "oracle",
+           "sample": (f"float64 NumPy oracle, {nseq} whole sequences over {args.steps} steps "
+                      f"({tot_s:.1f} s of wall time), {cores} worker processes (spawn), "
+                      f"1 BLAS thread each" if parallel else
+                      f"float64 NumPy oracle, {nseq} sequence samples (all heads, contexts cut "
+                      f"to the per-step time budget) over {args.steps} steps "
+                      f"({tot_s:.1f} s), 1 BLAS thread")}
     # the same config as the GPU arm's line for this workload and seed
     l2 = l2_text(decode_distinct_bytes(W), device_l2_bytes())
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
@@ -1285,7 +1422,8 @@ def run_reference(args, world, rank, local):
             "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) K/V/q; no model weights)",
             "config": workload_config(spec, W, l2, world, args.shard),
-            "run": {"where": "host cores, one thread (rank 0 alone)"},
+            "run": {"where": (f"host cores, {cores} processes (rank 0 alone)" if parallel
+                              else "host cores, one thread (rank 0 alone)")},
             "cpu_baseline": cpu,
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
