@@ -12,8 +12,9 @@
 //     ("vLLM GitHub 项目…", section 二 item 4: block-level sharing, so shared
 //     storage is not repeated); a prefix CTA streams each such block once and
 //     computes the logits of all members' query heads against it, the
-//     members x G heads forming up to 32 MMA columns (four n-tiles, one per
-//     consumer warp of each head).
+//     members x G heads forming up to 32 MMA columns (four n-tiles of 8; a
+//     head's warps are 4 n-tiles x 2 block phases over a 16-bit cache, 4 x 1
+//     over E4M3).
 // CTA c serves KV head group c % kvgc, so the CTAs reading the adjacent head
 // slices of the same blocks run side by side.  A CTA's range may end inside
 // a row or span several rows; each stretch of a row it covers is a segment.

@@ -76,38 +76,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
-// ---------------------------------------------------------------- shared-memory counters
-
-// Add n to a shared-memory counter with release semantics (CTA scope): this
-// thread's earlier memory operations, and those of threads it synchronised
-// with (e.g. a named barrier), happen before the addition.
-__device__ __forceinline__ void smem_count_release(unsigned* counter, unsigned n = 1) {
-  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(counter)), "r"(n)
-               : "memory");
-}
-
-__device__ __forceinline__ unsigned smem_load_acquire(const unsigned* counter) {
-  unsigned v;
-  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(counter)) : "memory");
-  return v;
-}
-
-// Bounded wait until *counter > n.  Gives up after `limit_ns` of wall time,
-// raises kErrWaitTimeout in `*status` and returns false.
-__device__ __forceinline__ bool smem_count_wait_bounded(const unsigned* counter, unsigned n,
-                                                        unsigned* status,
-                                                        uint64_t limit_ns = 1000000000ull) {
-  if (smem_load_acquire(counter) > n) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (smem_load_acquire(counter) <= n) {
-    if (globaltimer_ns() - t0 > limit_ns) {
-      atomicOr(status, kErrWaitTimeout);
-      return false;
-    }
-  }
-  return true;
-}
-
 // ---------------------------------------------------------------- programmatic dependent launch
 
 // Block until every grid this one depends on (the preceding kernel on the
