@@ -205,6 +205,39 @@ def test_fp8_shared_odd_kv_head_counts(hkv, group):
     check_against_oracle(W, pool, out, "fp8 shared odd heads")
 
 
+@pytest.mark.parametrize("kv,q", [("f16", "f16"), ("e4m3", "bf16")])
+def test_plan_at_its_size_limit(kv, q):
+    """The largest batch the stream-K plan holds: 1024 sequences in 512 groups of
+    two (short contexts keep the oracle quick).  Every output against the oracle."""
+    rng = np.random.default_rng(91)
+    B = 1024
+    lens = [int(x) for x in rng.integers(20, 200, B)]
+    spec = wl.Spec("plan size limit", B, 4, 2, 64, q, kv, ("fixed", lens), ("factor", 1.3))
+    W = wl.make_workload(spec, 91, poison=True, table_garbage=True)
+    order = [int(x) for x in rng.permutation(B)]
+    pairs = [sorted(order[i:i + 2], key=lambda s: -lens[s]) for i in range(0, B, 2)]
+    groups = alias_groups(W, pairs, rng)
+    assert groups.num_groups >= 400
+    pool = H.gpu_pool(W)
+    out = run_shared(W, groups, pool, "append")
+    check_against_oracle(W, pool, out, f"plan size limit, {kv}")
+
+
+def test_plan_past_its_size_limit_is_refused():
+    """One sequence more than the plan holds: refused before any launch."""
+    B = 1025
+    spec = wl.Spec("past the plan", B, 4, 2, 64, "f16", "f16", ("fixed", [40] * B))
+    W = wl.make_workload(spec, 92, device="cuda")
+    groups = pa.SharedGroups(torch.tensor([0, 2], dtype=torch.int32, device="cuda"),
+                             torch.tensor([0, 1], dtype=torch.int32, device="cuda"),
+                             torch.tensor([1], dtype=torch.int32, device="cuda"))
+    kc, vc = pa.kv_views(H.gpu_pool(W))
+    out = torch.empty_like(W.q)
+    with pytest.raises(pa.PagedAttentionError, match="at most 1024 sequences"):
+        pa.pa_decode_shared(out, W.q, kc, vc, W.block_tables, W.context_lens, W.scale, groups)
+    assert pa.pa_device_status(clear=True) == 0
+
+
 # ---------------------------------------------------------------- bitwise properties
 
 def _bits(t):
