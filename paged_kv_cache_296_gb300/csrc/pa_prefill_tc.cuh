@@ -387,6 +387,16 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
     const uint8_t* ring = smem + (isv ? C::kVOff : C::kKOff);
     uint8_t* st = smem + (isv ? C::kVStOff : C::kKStOff);
     constexpr int kRuns = D / 16;  // 16-byte runs of an fp8 row
+    constexpr int kStride = 32 * C::kConvWarps;  // runs between one lane's consecutive runs
+    static_assert(kStride % kRuns == 0, "a lane keeps one run index in every row");
+    constexpr int kRStep = kStride / kRuns;  // rows between one lane's consecutive runs
+    // run u = r * kRuns + j of a chunk: this lane takes j = cl % kRuns in rows
+    // cl / kRuns, + kRStep, ...; its f16 elements 16 j .. 16 j + 15 go to piece
+    // j / 4, 16-byte chunks 2 (j % 4) and + 1 of the staged row
+    const int j = cl % kRuns;
+    const int r_first = cl / kRuns;
+    const int cc = 2 * (j % 4);
+    uint8_t* dst = st + (j / 4) * C::kPlaneBytes;
     for (int c = 0; c < nchunks; ++c) {
       const int slot = c % kR;
       const bool w = mbar_wait_bounded(&full[slot], (uint32_t)(c / kR) & 1u, p.status) &&
@@ -396,41 +406,34 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
         break;
       }
       const int nrows = 16 * min(kBpc, nkb - kBpc * c);
-      constexpr int kStride = 32 * C::kConvWarps;  // runs between one lane's consecutive runs
-      constexpr int kBatch = 4;                    // runs loaded before any is converted
-      for (int u0 = cl; u0 < nrows * kRuns; u0 += kBatch * kStride) {
+      // V rows of keys at or past L are written as zeros
+      const int live_rows = isv ? min(nrows, L - kBpc * 16 * c) : nrows;
+      const uint8_t* src = ring + slot * C::kChunkBytes8;
+      constexpr int kBatch = 4;  // runs loaded before any is converted
+#pragma unroll 1
+      for (int r0 = r_first; r0 < nrows; r0 += kBatch * kRStep) {
         uint4 x[kBatch];
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
-          const int u = u0 + b * kStride;
-          const int r = u / kRuns, j = u % kRuns;
-          // the TMA's swizzle of the [16 rows][D bytes] tile of block r / 16
-          const uint32_t o = (uint32_t)((r & 15) * D + j * 16);
-          const uint32_t sw =
-              D == 128 ? (o ^ (((o >> 7) & 7u) << 4)) : (o ^ (((o >> 7) & 3u) << 4));
-          if (u < nrows * kRuns)
-            x[b] = *reinterpret_cast<const uint4*>(ring + slot * C::kChunkBytes8 +
-                                                   (r >> 4) * (16 * D) + sw);
+          const int r = r0 + b * kRStep;
+          // the TMA's swizzle of the [16 rows][D bytes] tile: 16-byte chunk j of
+          // row r sits at chunk j ^ (r & 7) (128-byte rows) or j ^ ((r >> 1) & 3)
+          const int sw = D == 128 ? (r & 7) : ((r >> 1) & 3);
+          if (r < nrows) x[b] = *reinterpret_cast<const uint4*>(src + r * D + ((j ^ sw) << 4));
         }
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
-          const int u = u0 + b * kStride;
-          if (u >= nrows * kRuns) break;
-          const int r = u / kRuns, j = u % kRuns;
+          const int r = r0 + b * kRStep;
+          if (r >= nrows) break;
           uint4 y0 = make_uint4(0u, 0u, 0u, 0u), y1 = y0;
-          if (!isv || kBpc * 16 * c + r < L) {
-            y0 = make_uint4(e4m3x2_to_f16x2((uint16_t)(x[b].x & 0xFFFFu)),
-                            e4m3x2_to_f16x2((uint16_t)(x[b].x >> 16)),
-                            e4m3x2_to_f16x2((uint16_t)(x[b].y & 0xFFFFu)),
-                            e4m3x2_to_f16x2((uint16_t)(x[b].y >> 16)));
-            y1 = make_uint4(e4m3x2_to_f16x2((uint16_t)(x[b].z & 0xFFFFu)),
-                            e4m3x2_to_f16x2((uint16_t)(x[b].z >> 16)),
-                            e4m3x2_to_f16x2((uint16_t)(x[b].w & 0xFFFFu)),
-                            e4m3x2_to_f16x2((uint16_t)(x[b].w >> 16)));
+          if (r < live_rows) {
+            e4m3x4_to_f16x4(x[b].x, y0.x, y0.y);
+            e4m3x4_to_f16x4(x[b].y, y0.z, y0.w);
+            e4m3x4_to_f16x4(x[b].z, y1.x, y1.y);
+            e4m3x4_to_f16x4(x[b].w, y1.z, y1.w);
           }
-          // elements 16 j .. 16 j + 15: piece j / 4, 16-byte chunks 2 (j % 4) and + 1
-          const int cc = 2 * (j % 4);
-          uint8_t* row = st + (j / 4) * C::kPlaneBytes + r * 128;
+          // the 16-bit row's 16-byte chunks cc and cc + 1, 128B-swizzled
+          uint8_t* row = dst + r * 128;
           *reinterpret_cast<uint4*>(row + ((cc ^ (r & 7)) << 4)) = y0;
           *reinterpret_cast<uint4*>(row + (((cc + 1) ^ (r & 7)) << 4)) = y1;
         }
