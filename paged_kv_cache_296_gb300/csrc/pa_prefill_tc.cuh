@@ -41,11 +41,12 @@
 namespace pa {
 
 // KV8: the cache holds E4M3 codes.  The TMA then loads fp8 rows into rings of
-// their own and six converter warps (three for K, three for V) widen each chunk
+// their own and eight converter warps (four for K, four for V) widen each chunk
 // into 16-bit staging planes laid out like the 16-bit rings (one chunk of K, one
 // of V), which the MMAs read; the MMAs run in f16 (every E4M3 value is exact in
 // f16).  The widening (cvt.f16x2.e4m3x2) is throughput-bound, so it is spread
-// over as many warps as the 128-register budget of 16 warps allows.
+// over many warps: 18 in all, 112 registers each (2 or 3 converter warps per
+// operand measured slower).
 template <int D, bool KV8>
 struct PrefillTcCfg {
   static constexpr int kRows = 128;                        // rows of one tile (TMEM lanes)
@@ -76,7 +77,7 @@ struct PrefillTcCfg {
   static constexpr int kProducerWarp = kSoftmaxThreads / 32;
   static constexpr int kMmaWarp = kProducerWarp + 1;
   static constexpr int kConvWarp = kMmaWarp + 1;           // KV8: K converters, then V converters
-  static constexpr int kConvWarps = 3;                     // KV8: warps per operand
+  static constexpr int kConvWarps = 4;                     // KV8: warps per operand
   static constexpr int kThreads = kSoftmaxThreads + 64 + (KV8 ? 64 * kConvWarps : 0);
   // TMEM columns of tile t (base 256 t): O [0, D); S(c) in fp32 at [128, 256),
   // then P(c) (16-bit pairs) over it once the softmax has read it: keys 0..63
