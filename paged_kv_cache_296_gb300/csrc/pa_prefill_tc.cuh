@@ -42,8 +42,9 @@ namespace pa {
 
 // KV8: the cache holds E4M3 codes.  The TMA then loads fp8 rows into rings of
 // their own and eight converter warps (four for K, four for V) widen each chunk
-// into 16-bit staging planes laid out like the 16-bit rings (one chunk of K, one
-// of V), which the MMAs read; the MMAs run in f16 (every E4M3 value is exact in
+// into 16-bit staging planes laid out like the 16-bit rings (one chunk of K; two
+// of V, so that V(c + 1) is widened while the P V MMAs of chunk c read V(c)),
+// which the MMAs read; the MMAs run in f16 (every E4M3 value is exact in
 // f16).  The widening (cvt.f16x2.e4m3x2) is throughput-bound, so it is spread
 // over many warps: 18 in all, 112 registers each (2 or 3 converter warps per
 // operand measured slower).
@@ -66,12 +67,15 @@ struct PrefillTcCfg {
   static constexpr int kRingPart = KV8 ? kRing * kChunkBytes8 : kPieces * kPlaneBytes;
   static constexpr int kKOff = kQBytes;                    // K ring
   static constexpr int kVOff = kKOff + kRingPart;          // V ring
+  static constexpr int kStBytes = kPieces * kPlaneBytes;  // KV8: one staged 16-bit chunk
+  static constexpr int kVStages = 2;                       // KV8: staged V chunks
   static constexpr int kKStOff = kVOff + kRingPart;        // KV8: 16-bit K of one chunk
-  static constexpr int kVStOff = kKStOff + (KV8 ? kPieces * kPlaneBytes : 0);
-  static constexpr int kBarOff = kVStOff + (KV8 ? kPieces * kPlaneBytes : 0);
+  static constexpr int kVStOff = kKStOff + (KV8 ? kStBytes : 0);  // KV8: 16-bit V, two chunks
+  static constexpr int kBarOff = kVStOff + (KV8 ? kVStages * kStBytes : 0);
   // barriers: K full / empty, V full / empty per ring slot; s_full, p_full per
-  // tile; q_ready, tail, o_done; KV8: staged K full / empty, staged V full / empty
-  static constexpr int kNumBars = 4 * kRing + 2 * kTiles + 3 + (KV8 ? 4 : 0);
+  // tile; q_ready, tail, o_done; KV8: staged K full / empty, staged V full and
+  // empty per staged chunk
+  static constexpr int kNumBars = 4 * kRing + 2 * kTiles + 3 + (KV8 ? 2 + 2 * kVStages : 0);
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr int kSoftmaxThreads = 128 * kTiles;
   static constexpr int kProducerWarp = kSoftmaxThreads / 32;
@@ -116,10 +120,10 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
   uint64_t* q_ready = p_full + kT;
   uint64_t* tail_bar = q_ready + 1;
   uint64_t* o_done = q_ready + 2;
-  uint64_t* kst_full = o_done + 1;  // KV8: the staged 16-bit K / V chunk
+  uint64_t* kst_full = o_done + 1;  // KV8: the staged 16-bit K chunk
   uint64_t* kst_empty = o_done + 2;
-  uint64_t* vst_full = o_done + 3;
-  uint64_t* vst_empty = o_done + 4;
+  uint64_t* vst_full = o_done + 3;  // KV8: [kVStages] each, the staged 16-bit V chunks
+  uint64_t* vst_empty = vst_full + C::kVStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -188,8 +192,10 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
     if constexpr (KV8) {
       mbar_init(kst_full, 32 * C::kConvWarps);
       mbar_init(kst_empty, 1);
-      mbar_init(vst_full, 32 * C::kConvWarps);
-      mbar_init(vst_empty, 1);
+      for (int i = 0; i < C::kVStages; ++i) {
+        mbar_init(&vst_full[i], 32 * C::kConvWarps);
+        mbar_init(&vst_empty[i], 1);
+      }
     }
     for (int t = 0; t < kT; ++t) {
       mbar_init(&s_full[t], 1);
@@ -302,8 +308,12 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
       const uint32_t q_lo = umma_desc_lo(sbase, 16);
       const uint32_t k_lo = umma_desc_lo(sbase + (KV8 ? C::kKStOff : C::kKOff), 16);
       const uint32_t v_lo = umma_desc_lo(sbase + (KV8 ? C::kVStOff : C::kVOff), C::kPlaneBytes);
-      // KV8: one staged chunk of each (released once its MMAs are done), else ring slots
+      // KV8: one staged K chunk and two staged V chunks (each released once its MMAs
+      // are done), else ring slots
       auto slot_lo = [&](int c) { return KV8 ? 0u : (uint32_t)((c % kR) * C::kChunkBytes >> 4); };
+      auto vslot_lo = [&](int c) {
+        return KV8 ? (uint32_t)((c % C::kVStages) * C::kStBytes >> 4) : slot_lo(c);
+      };
       auto wait_k = [&](int c) {
         return KV8 ? mbar_wait_bounded(kst_full, (uint32_t)c & 1u, p.status)
                    : mbar_wait_bounded(&full_k[c % kR], (uint32_t)(c / kR) & 1u, p.status);
@@ -332,7 +342,8 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
         const int nblk = min(kBpc, nkb - kBpc * c);
         const bool more = c + 1 < nchunks;
         if constexpr (KV8) {
-          ok = mbar_wait_bounded(vst_full, (uint32_t)c & 1u, p.status);
+          ok = mbar_wait_bounded(&vst_full[c % C::kVStages], (uint32_t)(c / C::kVStages) & 1u,
+                                 p.status);
         } else {
           ok = mbar_wait_bounded(&full_v[slot], (uint32_t)(c / kR) & 1u, p.status);
           if (ok && has_tail && !more) ok = mbar_wait_bounded(tail_bar, 0, p.status);
@@ -343,7 +354,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t pcol = tmem + t * C::kTileCols + C::kS0;
-          const uint32_t va = v_lo + slot_lo(c);
+          const uint32_t va = v_lo + vslot_lo(c);
           auto pv = [&](int j) {
             umma_ts(tmem + t * C::kTileCols, pcol + 64 * (j / 4) + 8 * (j % 4),
                     umma_desc_join(va + (uint32_t)(j * (C::kBlockBytes >> 4))), id_pv,
@@ -355,7 +366,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
           } else {
             for (int j = 0; j < nblk; ++j) pv(j);
           }
-          if (t == kT - 1) umma_commit(KV8 ? vst_empty : &empty_v[slot]);
+          if (t == kT - 1) umma_commit(KV8 ? &vst_empty[c % C::kVStages] : &empty_v[slot]);
           if (more) {
             if (t == 0) {
               ok = wait_k(c + 1);
@@ -385,6 +396,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
     uint64_t* empty = isv ? empty_v : empty_k;
     uint64_t* st_full = isv ? vst_full : kst_full;
     uint64_t* st_empty = isv ? vst_empty : kst_empty;
+    const int nst = isv ? C::kVStages : 1;  // staged chunks of this operand
     const uint8_t* ring = smem + (isv ? C::kVOff : C::kKOff);
     uint8_t* st = smem + (isv ? C::kVStOff : C::kKStOff);
     constexpr int kRuns = D / 16;  // 16-byte runs of an fp8 row
@@ -397,11 +409,14 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
     const int j = cl % kRuns;
     const int r_first = cl / kRuns;
     const int cc = 2 * (j % 4);
-    uint8_t* dst = st + (j / 4) * C::kPlaneBytes;
+    uint8_t* const dst0 = st + (j / 4) * C::kPlaneBytes;
     for (int c = 0; c < nchunks; ++c) {
       const int slot = c % kR;
-      const bool w = mbar_wait_bounded(&full[slot], (uint32_t)(c / kR) & 1u, p.status) &&
-                     mbar_wait_bounded(st_empty, ((uint32_t)c & 1u) ^ 1u, p.status);
+      const int si = c % nst;  // the staged chunk this chunk goes to
+      uint8_t* const dst = dst0 + si * C::kStBytes;
+      const bool w =
+          mbar_wait_bounded(&full[slot], (uint32_t)(c / kR) & 1u, p.status) &&
+          mbar_wait_bounded(&st_empty[si], ((uint32_t)(c / nst) & 1u) ^ 1u, p.status);
       if (!__all_sync(kAll, w)) {
         if (lane == 0) fail();
         break;
@@ -440,7 +455,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
         }
       }
       fence_proxy_async_shared();  // the MMAs read the staging through the async proxy
-      mbar_arrive(st_full);
+      mbar_arrive(&st_full[si]);
       mbar_arrive(&empty[slot]);
     }
   } else {
