@@ -40,13 +40,21 @@
 
 namespace pa {
 
+// Four E4M3 bytes (byte i -> element i) to four f16: elements 0, 1 in lo, 2, 3 in hi.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
+}
+
 // KV8: the cache holds E4M3 codes.  The TMA then loads fp8 rows into rings of
 // their own and eight converter warps (four for K, four for V) widen each chunk
 // into 16-bit staging planes laid out like the 16-bit rings (one chunk of K; two
 // of V, so that V(c + 1) is widened while the P V MMAs of chunk c read V(c)),
 // which the MMAs read; the MMAs run in f16 (every E4M3 value is exact in
 // f16).  The widening (cvt.f16x2.e4m3x2) is throughput-bound, so it is spread
-// over many warps: 18 in all, 112 registers each (2 or 3 converter warps per
+// over many warps: 18 in all, 96 registers each (2 or 3 converter warps per
 // operand measured slower).
 template <int D, bool KV8>
 struct PrefillTcCfg {

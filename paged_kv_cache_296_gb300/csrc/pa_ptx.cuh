@@ -226,14 +226,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
   return y;
 }
 
-// Four E4M3 bytes (byte i -> element i) to four f16: elements 0, 1 in lo, 2, 3 in hi.
-__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
-  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(x));
-}
-
 // Two floats to two E4M3 bytes (lo -> low byte), round to nearest even,
 // saturating to +-448; cvt packs its first source into the upper byte.
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
