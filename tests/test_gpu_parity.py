@@ -518,6 +518,28 @@ def test_fp8_odd_kv_head_counts(hkv, group, path, part):
             H.assert_close(got[i, h * group:(h + 1) * group], want, spec, f"s{i} h{h}")
 
 
+@pytest.mark.parametrize("kv,q", [("f16", "f16"), ("e4m3", "bf16")])
+def test_largest_batch_sampled(kv, q):
+    """The largest batch the calls take (65535 sequences of 0-39 tokens, two KV
+    heads): a grid of one CTA per (sequence, KV head group).  Every output is
+    finite; the first, the last and 200 random sequences match the oracle."""
+    B = 65535
+    rng = np.random.default_rng(77)
+    lens = [int(x) for x in rng.integers(0, 40, B)]
+    spec = wl.Spec("largest batch", B, 4, 2, 64, q, kv, ("fixed", lens), ("factor", 1.2))
+    W = wl.make_workload(spec, 77, poison=True)
+    pool = H.gpu_pool(W)
+    out = H.gpu_step(W, pool)
+    got = H.widen_out(out, q)
+    assert np.isfinite(got).all(), "NaN/inf output: a poisoned slot was read"
+    for i in sorted({0, 1, B - 1} | {int(x) for x in rng.integers(0, B, 200)}):
+        for h in range(2):
+            _, mini = H.mini_case(W, i, h)
+            _, want = H.oracle_mini(W, mini)
+            H.assert_close(got[i, 2 * h:2 * h + 2], want, spec, f"seq {i} kv head {h}")
+    assert pa.pa_device_status(clear=True) == 0
+
+
 @pytest.mark.parametrize("num_seqs", [1, 31, 32, 33, 100])
 def test_balanced_split_batch_sizes(num_seqs):
     """Few (sequence, KV head) pairs: the kernel plans a balanced split from the
