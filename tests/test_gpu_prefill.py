@@ -150,6 +150,35 @@ def test_full_size_sampled_rows(n):
             check_close(got_all[qsl[i] + t][None], want, dt, f"seq {i} token {t}")
 
 
+def test_long_context_chunk_sampled_rows():
+    """A 512-query chunk at the end of 65536- and 40000-token contexts (512 and
+    313 chunks of 128 keys per tile): sampled rows against the oracle on the
+    sequence cut to each row."""
+    spec = wl.PrefillSpec("long context chunk", 2, 32, 8, 128, "bf16", ("fixed", [65536, 40000]),
+                          ("chunk", 512), ("factor", 1.05))
+    W = wl.make_prefill_workload(spec, 31, device="cuda")
+    out, pool = gpu_prefill(W)
+    assert pa.pa_device_status(clear=True) == 0
+    got_all = ref.widen(bits_of(out.cpu()), "bf16")
+    assert np.isfinite(got_all).all()
+    lens = W.context_lens.cpu().numpy()
+    qsl = W.query_start_loc.cpu().numpy()
+    tables = W.block_tables.cpu().numpy()
+    rng = np.random.default_rng(31)
+    for i in range(2):
+        nq = int(qsl[i + 1] - qsl[i])
+        L = int(lens[i])
+        for t in sorted({0, nq - 1, int(rng.integers(nq))}):
+            pos = L - nq + t
+            nb = pos // 16 + 1
+            blocks = tables[i, :nb].astype(np.int64)
+            sub = bits_of(pool[torch.from_numpy(blocks).cuda()].cpu())
+            want = ref.paged_prefill(bits_of(W.q[qsl[i] + t:qsl[i] + t + 1].cpu()), "bf16", sub,
+                                     np.arange(nb)[None, :], np.array([pos + 1]),
+                                     np.array([0, 1]), W.scale, "bf16")
+            check_close(got_all[qsl[i] + t][None], want, "bf16", f"seq {i} token {t}")
+
+
 def test_run_to_run_bitwise_deterministic():
     W = wl.make_prefill_workload(wl.PREFILL_SPECS[2], 12, device="cuda")
     first, _ = gpu_prefill(W)
@@ -332,6 +361,46 @@ def test_e4m3_cache_full_size_sampled_rows(n):
                                  W.scale, "e4m3", S.kv_scale)
         err = np.abs(got_all[qsl[i] + t] - want[0])
         assert err.max() <= ATOL["e4m3"], f"seq {i} token {t}: max err {err.max():.3e}"
+
+
+def test_e4m3_cache_long_context_chunk_sampled_rows():
+    """The long-context chunk over an E4M3 cache: the widening runs 512 and 313
+    chunks per tile; sampled rows and their cache bytes against the oracle."""
+    from paged_kv_cache_296_gb300.runner import PrefillStep
+    spec = wl.PrefillSpec("long context chunk", 2, 32, 8, 128, "bf16", ("fixed", [65536, 40000]),
+                          ("chunk", 512), ("factor", 1.05))
+    W = wl.make_prefill_workload(spec, 32, device="cuda")
+    S = PrefillStep(W, kv_dtype="e4m3")
+    S.step()
+    assert pa.pa_device_status(clear=True) == 0
+    got_all = ref.widen(bits_of(S.out.cpu()), "bf16")
+    assert np.isfinite(got_all).all()
+    lens = W.context_lens.cpu().numpy()
+    qsl = W.query_start_loc.cpu().numpy()
+    tables = W.block_tables.cpu().numpy()
+    k_new, v_new = W.k_new.cpu().float(), W.v_new.cpu().float()
+    rng = np.random.default_rng(32)
+    for i in range(2):
+        nq = int(qsl[i + 1] - qsl[i])
+        L = int(lens[i])
+        for t in sorted({nq - 1, int(rng.integers(nq))}):
+            pos = L - nq + t
+            nb = pos // 16 + 1
+            blocks = torch.from_numpy(tables[i, :nb].astype(np.int64))
+            src = W.pool[blocks.cuda()].cpu().float()
+            for q in range(L - nq, pos + 1):
+                src[q // 16, q % 16, 0] = k_new[qsl[i] + q - (L - nq)]
+                src[q // 16, q % 16, 1] = v_new[qsl[i] + q - (L - nq)]
+            opool = ref.fp8_quantise(bits_of(src), "f32", S.kv_scale)
+            gpool = bits_of(S.pool[blocks.cuda()].cpu())
+            keep = np.zeros(opool.shape, dtype=bool)
+            keep.reshape(nb * 16, -1)[:pos + 1] = True
+            assert np.array_equal(gpool[keep], opool[keep]), f"seq {i}: cache bytes differ"
+            want = ref.paged_prefill(bits_of(W.q[qsl[i] + t:qsl[i] + t + 1].cpu()), "bf16", opool,
+                                     np.arange(nb)[None, :], np.array([pos + 1]),
+                                     np.array([0, 1]), W.scale, "e4m3", S.kv_scale)
+            err = np.abs(got_all[qsl[i] + t] - want[0])
+            assert err.max() <= ATOL["e4m3"], f"seq {i} token {t}: max err {err.max():.3e}"
 
 
 def test_context_length_past_the_table_is_cut_to_it():
