@@ -518,6 +518,18 @@ def test_fp8_odd_kv_head_counts(hkv, group, path, part):
             H.assert_close(got[i, h * group:(h + 1) * group], want, spec, f"s{i} h{h}")
 
 
+def test_very_long_context_balanced_split():
+    """One 131072-token sequence (8192 blocks) beside three short ones: the
+    balanced split gives the long one most of the wave's CTAs and the merge
+    folds their partials.  Every output against the oracle."""
+    lens = [131072, 1, 700, 33]
+    spec = wl.Spec("very long context", len(lens), 8, 2, 128, "f16", "f16", ("fixed", lens),
+                   ("factor", 1.05))
+    W = wl.make_workload(spec, 88, poison=True, table_garbage=True)
+    assert pa.pa_decode_partition_size(len(lens), 2, W.max_blocks_per_seq) == 0  # balanced
+    _full_check(W)
+
+
 @pytest.mark.parametrize("kv,q", [("f16", "f16"), ("e4m3", "bf16")])
 def test_largest_batch_sampled(kv, q):
     """The largest batch the calls take (65535 sequences of 0-39 tokens, two KV
