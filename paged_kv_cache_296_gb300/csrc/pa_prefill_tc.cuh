@@ -70,7 +70,7 @@ struct PrefillTcCfg {
   static constexpr int kRingBytes = KV8 ? 64 * 1024 : 128 * 1024;    // K and V rings
   static constexpr int kRing =                                        // chunks per ring
       KV8 ? kRingBytes / (2 * kChunkBytes8) : kRingBytes / (2 * kPieces * kChunkBytes);
-  // one piece plane of K (or V): the whole ring, or (KV8) the one staged chunk
+  // one piece plane of K (or V): the whole ring, or (KV8) one staged chunk
   static constexpr int kPlaneBytes = KV8 ? kChunkBytes : kRing * kChunkBytes;
   static constexpr int kRingPart = KV8 ? kRing * kChunkBytes8 : kPieces * kPlaneBytes;
   static constexpr int kKOff = kQBytes;                    // K ring
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kR; ++i) {
-      // KV8: a ring slot is released by the converter warp's 32 lanes
+      // KV8: a ring slot is released by every lane of the operand's converter warps
       mbar_init(&full_k[i], 1);
       mbar_init(&empty_k[i], KV8 ? 32 * C::kConvWarps : 1);
       mbar_init(&full_v[i], 1);
@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, KV8>::kThreads, 1)
         const uint64_t nm2 = update_max(row_max(sv), c);
         exp_store(sv, scol, nm2, acc0, acc1);
       } else {
-        // 128 registers a thread (16 warps): one 64-column half at a time, the
+        // 96 registers a thread (18 warps): one 64-column half at a time, the
         // maxima of both, then half 1 and half 0 read again
         float mx;
         {
