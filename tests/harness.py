@@ -5,12 +5,20 @@ The GPU side calls the C ABI through the Python binding; the oracle side takes
 the CPU copies of the inputs, never a value the GPU produced.
 """
 
+import os
+
 import numpy as np
 import torch
 
 from oracle import paged_attention as ref
 from paged_kv_cache_296_gb300 import binding as pa
 from paged_kv_cache_296_gb300.workloads import BLOCK_SIZE
+
+def seeds(n):
+    """The seeds of a random-shape sweep: range(n), or range(PA_RANDOM_SEEDS) when
+    that environment variable asks for a longer sweep."""
+    return range(max(n, int(os.environ.get("PA_RANDOM_SEEDS", "0"))))
+
 
 #: Attention tolerances (max abs error against the float64 oracle).
 ATOL = {"f16": 2e-3, "bf16": 1e-2, "e4m3": 3e-2}

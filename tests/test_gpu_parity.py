@@ -232,7 +232,7 @@ def test_config5_long_fp8_sampled():
 
 # ---------------------------------------------------------------- decode: sweeps and edges
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", H.seeds(24))
 def test_random_shapes(seed):
     spec = wl.random_spec(seed)
     W = wl.make_workload(spec, 1000 + seed, poison=True, table_garbage=True)

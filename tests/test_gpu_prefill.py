@@ -17,6 +17,7 @@ from oracle import paged_attention as ref
 from paged_kv_cache_296_gb300 import binding as pa
 from paged_kv_cache_296_gb300 import workloads as wl
 
+import harness as H
 from harness import ATOL, ULP1, bits_of
 from oracle import e4m3
 
@@ -81,7 +82,7 @@ def random_prefill_spec(seed):
                           ("fixed", nq), ("factor", 1.5))
 
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", H.seeds(24))
 def test_random_shapes(seed):
     W = wl.make_prefill_workload(random_prefill_spec(seed), 3000 + seed, poison=True)
     full_check(W)
@@ -284,7 +285,7 @@ def fp8_check(spec, seed, poison=True):
                            f"{np.nanmax(np.abs(got - want)):.3e} at {np.argwhere(bad)[:3].tolist()}")
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", H.seeds(12))
 def test_e4m3_cache_random_shapes(seed):
     spec = random_prefill_spec(100 + seed)
     fp8_check(spec, 5000 + seed)

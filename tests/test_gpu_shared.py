@@ -147,7 +147,7 @@ def test_shared_prefix_workload_all_outputs(path):
     check_against_oracle(W, pool, out, f"shared prefix, {path}")
 
 
-@pytest.mark.parametrize("seed", range(16))
+@pytest.mark.parametrize("seed", H.seeds(16))
 def test_shared_random_shapes(seed):
     W, groups = random_shared_case(seed)
     pool = H.gpu_pool(W)
